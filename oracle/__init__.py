@@ -1,0 +1,164 @@
+"""CPU oracle for the AlltoAllv + Permute + GroupedMatMul hot path.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  The product
+path (``token_permute_grouped_gb300``) never does, and shares no code with it.
+
+The arithmetic lives in ``a2av_ref.c`` (plain C, double accumulation, OpenMP
+over output rows); this module builds it with gcc and wraps it with ctypes.
+It follows the "Formula" section of the aclnnAlltoAllvGroupedMatMul page:
+permuteOut = Permute(ataOut), gmmY = permuteOut x gmmWeight (one weight
+matrix per local expert), mmY = mmX x mmWeight.
+
+Every function is pinned by tests/test_oracle_pins.py; no function here is
+"parity unpinned".
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "a2av_ref.c")
+_LIB = os.path.join(_HERE, "liba2av_ref.so")
+_lock = threading.Lock()
+_lib = None
+
+DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1}
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(src: str = _SRC, out: str = _LIB, extra_flags=()) -> str:
+    """Compile the oracle with gcc (plain C11 + OpenMP)."""
+    cmd = ["gcc", "-std=c11", "-O2", "-fopenmp", "-fPIC", "-shared", *extra_flags,
+           src, "-o", out, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _declare(lib):
+    i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    lib.a2av_ref_decode.argtypes = [ctypes.c_int, p, i64, p]
+    lib.a2av_ref_plan.argtypes = [i32, i32, p, i64, p, p, p, p]
+    lib.a2av_ref_permute.argtypes = [i32, i32, p, i64, i64, p, p]
+    lib.a2av_ref_grouped_matmul.argtypes = [i32, p, i64, i64, i64, i32, p, p, p, i64, p]
+    lib.a2av_ref_matmul.argtypes = [i64, i64, i64, i32, p, p, p, i64, p]
+    lib.a2av_ref_num_threads.argtypes = []
+    for f in ("a2av_ref_decode", "a2av_ref_plan", "a2av_ref_permute",
+              "a2av_ref_grouped_matmul", "a2av_ref_matmul", "a2av_ref_num_threads"):
+        getattr(lib, f).restype = ctypes.c_int
+    return lib
+
+
+def load_from(path: str):
+    """Load an oracle build (tests use this for deliberately broken copies)."""
+    return _declare(ctypes.CDLL(path))
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if (not os.path.exists(_LIB)
+                    or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)):
+                build()
+            _lib = load_from(_LIB)
+    return _lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, torch.Tensor):
+        assert a.is_contiguous() and a.device.type == "cpu"
+        return a.data_ptr()
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _bits(t: torch.Tensor) -> torch.Tensor:
+    return t.contiguous().view(torch.int16)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise OracleError(f"{what}: oracle returned {rc}")
+
+
+class Oracle:
+    """Thin wrapper; ``impl`` lets tests swap in a deliberately broken build."""
+
+    def __init__(self, impl=None):
+        self.L = impl if impl is not None else lib()
+
+    def num_threads(self) -> int:
+        return int(self.L.a2av_ref_num_threads())
+
+    def decode(self, t: torch.Tensor) -> np.ndarray:
+        b = _bits(t).reshape(-1)
+        out = np.empty(b.numel(), dtype=np.float64)
+        _check(self.L.a2av_ref_decode(DTYPE_CODE[t.dtype], _ptr(b), b.numel(), _ptr(out)), "decode")
+        return out.reshape(tuple(t.shape))
+
+    def plan(self, W: int, e: int, recvCounts, A: int):
+        rc = np.ascontiguousarray(recvCounts, dtype=np.int32)
+        E = W * e
+        src = np.zeros(E, np.int64)
+        dst = np.zeros(E, np.int64)
+        gr = np.zeros(e, np.int64)
+        go = np.zeros(e + 1, np.int64)
+        _check(self.L.a2av_ref_plan(W, e, _ptr(rc), A, _ptr(src), _ptr(dst), _ptr(gr), _ptr(go)), "plan")
+        return src, dst, gr, go
+
+    def permute(self, W: int, e: int, recvCounts, ataOut: torch.Tensor) -> torch.Tensor:
+        rc = np.ascontiguousarray(recvCounts, dtype=np.int32)
+        A, H1 = ataOut.shape
+        out = torch.empty_like(ataOut)
+        _check(self.L.a2av_ref_permute(W, e, _ptr(rc), A, H1, _ptr(_bits(ataOut)),
+                                       _ptr(out.view(torch.int16))), "permute")
+        return out
+
+    def grouped_matmul(self, group_rows, permuteOut: torch.Tensor, gmmWeight: torch.Tensor,
+                       rows=None) -> np.ndarray:
+        gr = np.ascontiguousarray(group_rows, dtype=np.int64)
+        e, H1, N1 = gmmWeight.shape
+        A = permuteOut.shape[0]
+        assert permuteOut.shape[1] == H1 and permuteOut.dtype == gmmWeight.dtype
+        rl = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        n = A if rl is None else len(rl)
+        out = np.empty((n, N1), np.float64)
+        _check(self.L.a2av_ref_grouped_matmul(
+            e, _ptr(gr), A, H1, N1, DTYPE_CODE[gmmWeight.dtype], _ptr(_bits(permuteOut)),
+            _ptr(_bits(gmmWeight)), _ptr(rl), n, _ptr(out)), "grouped_matmul")
+        return out
+
+    def matmul(self, mmX: torch.Tensor, mmWeight: torch.Tensor, rows=None) -> np.ndarray:
+        BS, H2 = mmX.shape
+        H2b, N2 = mmWeight.shape
+        assert H2 == H2b and mmX.dtype == mmWeight.dtype
+        rl = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        n = BS if rl is None else len(rl)
+        out = np.empty((n, N2), np.float64)
+        _check(self.L.a2av_ref_matmul(BS, H2, N2, DTYPE_CODE[mmX.dtype], _ptr(_bits(mmX)),
+                                      _ptr(_bits(mmWeight)), _ptr(rl), n, _ptr(out)), "matmul")
+        return out
+
+    def run(self, W: int, e: int, recvCounts, ataOut, gmmWeight, mmX=None, mmWeight=None,
+            gmm_rows=None, mm_rows=None):
+        """The whole hot path: (permuteOut, gmmY rows, mmY rows or None)."""
+        perm = self.permute(W, e, recvCounts, ataOut)
+        _, _, gr, _ = self.plan(W, e, recvCounts, ataOut.shape[0])
+        gmmY = self.grouped_matmul(gr, perm, gmmWeight, gmm_rows)
+        mmY = None
+        if mmX is not None:
+            mmY = self.matmul(mmX, mmWeight, mm_rows)
+        return perm, gmmY, mmY

@@ -1,0 +1,317 @@
+/*
+ * CPU oracle for the AlltoAllv + Permute + GroupedMatMul hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may load or call
+ * this library; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark do.  It shares no code, header, table or helper with the
+ * CUDA library: it is written straight from the operator's definition, as
+ * plainly as possible, so that a reader can check it against the page by eye.
+ *
+ * Source: "aclnnAlltoAllvGroupedMatMul" (Huawei CANN operator page),
+ *   - "API function": AlltoAllv, Permute and GroupedMatMul for the routed
+ *     experts, with an independent MatMul for the shared expert;
+ *   - "Formula": permuteOut = Permute(ataOut), gmmY = permuteOut x gmmWeight,
+ *     mmY = mmX x mmWeight;
+ *   - "Shape variables": A is the sum of recvCounts; e experts per rank.
+ * Readings where the page is silent (the order of rows inside an expert after
+ * Permute, the layout of recvCounts and gmmWeight) are stated at each
+ * function.
+ *
+ * Element formats: 16-bit floats are passed as raw bit patterns (uint16_t).
+ * dtype 0 = bfloat16, dtype 1 = IEEE binary16.  Products are formed and
+ * summed in double, k ascending, one output element at a time.
+ *
+ * Pins: every function here is checked in tests/test_oracle_pins.py against
+ * facts fixed by the page or by mathematics (sum rule, bijection, identity
+ * cases, numpy float64 matmul, exact integer cases, hand-worked fixtures).
+ *
+ * Return codes: 0 = ok, 1 = bad argument, 2 = recvCounts inconsistent with A.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define REF_OK 0
+#define REF_BAD_ARG 1
+#define REF_BAD_COUNTS 2
+
+/* ---- 16-bit float decoding, from the format definitions ---------------- */
+
+/* bfloat16: the upper half of an IEEE binary32 word. */
+static double bf16_value(uint16_t bits)
+{
+    uint32_t word = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &word, sizeof f);
+    return (double)f;
+}
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction
+ * bits; exponent 0 encodes zero and subnormals, exponent 31 inf and NaN. */
+static double fp16_value(uint16_t bits)
+{
+    int sign = bits >> 15;
+    int expo = (bits >> 10) & 0x1f;
+    int frac = bits & 0x3ff;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)frac, -24);                 /* frac * 2^-14 / 2^10 */
+    else if (expo == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + frac), expo - 25);  /* (1 + frac/2^10) * 2^(expo-15) */
+    return sign ? -v : v;
+}
+
+static double bf16_table[65536];
+static double fp16_table[65536];
+static int tables_ready = 0;
+
+static void build_tables(void)
+{
+    if (tables_ready)
+        return;
+    for (int i = 0; i < 65536; ++i) {
+        bf16_table[i] = bf16_value((uint16_t)i);
+        fp16_table[i] = fp16_value((uint16_t)i);
+    }
+    tables_ready = 1;
+}
+
+static const double *table_for(int dtype)
+{
+    build_tables();
+    return dtype == 0 ? bf16_table : fp16_table;
+}
+
+/* Decode n 16-bit values to double (exposed so tests can pin the decoders). */
+int a2av_ref_decode(int dtype, const uint16_t *bits, int64_t n, double *out)
+{
+    if ((dtype != 0 && dtype != 1) || n < 0 || (n && (!bits || !out)))
+        return REF_BAD_ARG;
+    const double *t = table_for(dtype);
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = t[bits[i]];
+    return REF_OK;
+}
+
+/* ---- Permute bookkeeping ----------------------------------------------- */
+
+/*
+ * Offsets of the (source rank w, local expert j) segments.
+ *
+ * ataOut arrives rank-major: all rows from source 0 (its rows for expert 0,
+ * then expert 1, ...), then all rows from source 1, and so on; segment
+ * (w, j) holds recvCounts[w*e + j] rows (page: "Formula", ataOut =
+ * AlltoAllv(gmmX); "Shape variables": A = sum of recvCounts).
+ *
+ * permuteOut is expert-major: all rows of expert 0, then expert 1, ...
+ * Inside one expert the rows keep their arrival order: source rank
+ * ascending, and the order within a segment unchanged (the page names the
+ * step Permute without fixing the order inside a group; this stable order is
+ * the reading taken).
+ *
+ *   src_off[w*e+j]  first ataOut row of segment (w, j)
+ *   dst_off[w*e+j]  first permuteOut row of segment (w, j)
+ *   group_rows[j]   rows of expert j, summed over sources
+ *   group_off[j]    first permuteOut row of expert j; group_off[e] = A
+ */
+int a2av_ref_plan(int32_t W, int32_t e, const int32_t *recvCounts, int64_t A,
+                  int64_t *src_off, int64_t *dst_off, int64_t *group_rows,
+                  int64_t *group_off)
+{
+    if (W < 1 || e < 1 || !recvCounts || !src_off || !dst_off || !group_rows || !group_off)
+        return REF_BAD_ARG;
+
+    int64_t total = 0;
+    for (int32_t w = 0; w < W; ++w) {
+        for (int32_t j = 0; j < e; ++j) {
+            int32_t c = recvCounts[w * e + j];
+            if (c < 0)
+                return REF_BAD_COUNTS;
+            src_off[w * e + j] = total;
+            total += c;
+        }
+    }
+    if (total != A)
+        return REF_BAD_COUNTS;
+
+    for (int32_t j = 0; j < e; ++j) {
+        group_rows[j] = 0;
+        for (int32_t w = 0; w < W; ++w)
+            group_rows[j] += recvCounts[w * e + j];
+    }
+    group_off[0] = 0;
+    for (int32_t j = 0; j < e; ++j)
+        group_off[j + 1] = group_off[j] + group_rows[j];
+
+    for (int32_t j = 0; j < e; ++j) {
+        int64_t at = group_off[j];
+        for (int32_t w = 0; w < W; ++w) {
+            dst_off[w * e + j] = at;
+            at += recvCounts[w * e + j];
+        }
+    }
+    return REF_OK;
+}
+
+/*
+ * permuteOut = Permute(ataOut) (page: "Formula", routed experts): copy every
+ * row of every segment from its rank-major place to its expert-major place.
+ * A bit copy of H1 16-bit elements per row.
+ */
+int a2av_ref_permute(int32_t W, int32_t e, const int32_t *recvCounts, int64_t A,
+                     int64_t H1, const uint16_t *ataOut, uint16_t *permuteOut)
+{
+    if (W < 1 || e < 1 || H1 < 1 || A < 0 || (A && (!ataOut || !permuteOut)))
+        return REF_BAD_ARG;
+    int64_t E = (int64_t)W * e;
+    int64_t *src_off = malloc(sizeof(int64_t) * E);
+    int64_t *dst_off = malloc(sizeof(int64_t) * E);
+    int64_t *group_rows = malloc(sizeof(int64_t) * e);
+    int64_t *group_off = malloc(sizeof(int64_t) * (e + 1));
+    int rc = a2av_ref_plan(W, e, recvCounts, A, src_off, dst_off, group_rows, group_off);
+    if (rc == REF_OK) {
+        for (int32_t j = 0; j < e; ++j)
+            for (int32_t w = 0; w < W; ++w)
+                for (int64_t r = 0; r < recvCounts[w * e + j]; ++r)
+                    memcpy(permuteOut + (dst_off[w * e + j] + r) * H1,
+                           ataOut + (src_off[w * e + j] + r) * H1,
+                           sizeof(uint16_t) * (size_t)H1);
+    }
+    free(src_off);
+    free(dst_off);
+    free(group_rows);
+    free(group_off);
+    return rc;
+}
+
+/* ---- Products ----------------------------------------------------------- */
+
+/*
+ * out[r][n] = sum_k x[row][k] * w[k][n] in double, k ascending, for the
+ * listed rows of x ([*, K] row-major) and w ([K, N] row-major).
+ */
+static void rows_times_matrix(const double *dec, const uint16_t *x, const uint16_t *w,
+                              int64_t K, int64_t N, const int64_t *rows,
+                              int64_t nrows, const int64_t *row_weight_index,
+                              double *out)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const uint16_t *xr = x + rows[r] * K;
+        const uint16_t *wm = w + (row_weight_index ? row_weight_index[r] : 0) * K * N;
+        double *o = out + r * N;
+        for (int64_t n = 0; n < N; ++n)
+            o[n] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double a = dec[xr[k]];
+            const uint16_t *wk = wm + k * N;
+            for (int64_t n = 0; n < N; ++n)
+                o[n] += a * dec[wk[n]];
+        }
+    }
+}
+
+/*
+ * gmmY = permuteOut x gmmWeight (page: "Formula", routed experts), as a
+ * grouped product: row i of permuteOut belongs to expert j when
+ * group_off[j] <= i < group_off[j+1], and is multiplied by gmmWeight[j],
+ * an [H1, N1] row-major matrix (gmmWeight is [e, H1, N1]).  Row i of gmmY
+ * pairs with row i of permuteOut (expert-major, no un-permute).
+ *
+ * Computes only the listed rows (all of them when rows == NULL).
+ * out is [nrows, N1] double.
+ */
+int a2av_ref_grouped_matmul(int32_t e, const int64_t *group_rows, int64_t A,
+                            int64_t H1, int64_t N1, int32_t dtype,
+                            const uint16_t *permuteOut, const uint16_t *gmmWeight,
+                            const int64_t *rows, int64_t nrows, double *out)
+{
+    if (e < 1 || !group_rows || A < 0 || H1 < 1 || N1 < 1 || (dtype != 0 && dtype != 1))
+        return REF_BAD_ARG;
+    int64_t sum = 0;
+    for (int32_t j = 0; j < e; ++j) {
+        if (group_rows[j] < 0)
+            return REF_BAD_COUNTS;
+        sum += group_rows[j];
+    }
+    if (sum != A)
+        return REF_BAD_COUNTS;
+    if (!rows)
+        nrows = A;
+    if (nrows == 0)
+        return REF_OK;
+    if (!permuteOut || !gmmWeight || !out || nrows < 0)
+        return REF_BAD_ARG;
+
+    int64_t *row_list = malloc(sizeof(int64_t) * nrows);
+    int64_t *expert = malloc(sizeof(int64_t) * nrows);
+    int bad = 0;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        row_list[r] = i;
+        if (i < 0 || i >= A) {
+            bad = 1;
+            break;
+        }
+        int64_t start = 0;
+        int32_t j = 0;
+        while (i >= start + group_rows[j]) {
+            start += group_rows[j];
+            ++j;
+        }
+        expert[r] = j;
+    }
+    if (!bad)
+        rows_times_matrix(table_for(dtype), permuteOut, gmmWeight, H1, N1,
+                          row_list, nrows, expert, out);
+    free(row_list);
+    free(expert);
+    return bad ? REF_BAD_ARG : REF_OK;
+}
+
+/*
+ * mmY = mmX x mmWeight (page: "Formula", shared experts): mmX [BS, H2],
+ * mmWeight [H2, N2], both row-major.  Only the listed rows (all when
+ * rows == NULL); out is [nrows, N2] double.
+ */
+int a2av_ref_matmul(int64_t BS, int64_t H2, int64_t N2, int32_t dtype,
+                    const uint16_t *mmX, const uint16_t *mmWeight,
+                    const int64_t *rows, int64_t nrows, double *out)
+{
+    if (BS < 0 || H2 < 1 || N2 < 1 || (dtype != 0 && dtype != 1))
+        return REF_BAD_ARG;
+    if (!rows)
+        nrows = BS;
+    if (nrows == 0)
+        return REF_OK;
+    if (!mmX || !mmWeight || !out || nrows < 0)
+        return REF_BAD_ARG;
+    int64_t *row_list = malloc(sizeof(int64_t) * nrows);
+    int bad = 0;
+    for (int64_t r = 0; r < nrows; ++r) {
+        row_list[r] = rows ? rows[r] : r;
+        if (row_list[r] < 0 || row_list[r] >= BS)
+            bad = 1;
+    }
+    if (!bad)
+        rows_times_matrix(table_for(dtype), mmX, mmWeight, H2, N2, row_list, nrows,
+                          NULL, out);
+    free(row_list);
+    return bad ? REF_BAD_ARG : REF_OK;
+}
+
+/* Threads the product loops use (the CPU baseline reports it). */
+int a2av_ref_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

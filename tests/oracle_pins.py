@@ -1,0 +1,304 @@
+"""Pins for the CPU oracle: facts fixed by the operator page or by mathematics.
+
+Each pin takes an ``oracle.Oracle`` and raises AssertionError when the oracle
+disagrees with something other than itself: hand-worked fixtures, the sum
+rule and bijection of Permute, cases that reduce to a library routine (numpy
+float64 matmul, numpy/torch float decoding), exact identity / one-hot /
+integer cases, and brute force on tiny inputs.  The same pins run against
+deliberately broken builds of the oracle (test_oracle_mutants.py) to show
+that each plausible mistake is caught.
+
+Page cited throughout: "aclnnAlltoAllvGroupedMatMul", sections "Formula"
+(permuteOut = Permute(ataOut), gmmY = permuteOut x gmmWeight,
+mmY = mmX x mmWeight) and "Shape variables" (A = sum of recvCounts).
+"""
+
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+import torch
+
+from oracle import OracleError
+from token_permute_grouped_gb300.workloads import random_counts
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _expert_of_arrival_rows(W, e, rc):
+    """Brute force: the local expert of every ataOut row, in arrival order."""
+    out = []
+    for w in range(W):
+        for j in range(e):
+            out += [j] * int(rc[w * e + j])
+    return out
+
+
+def _tagged(A, H, dtype):
+    """Row r carries r in base-256 digits in columns 0..2 (exact in bf16/fp16)."""
+    t = torch.zeros(A, H, dtype=torch.float64)
+    r = torch.arange(A, dtype=torch.float64)
+    t[:, 0] = torch.floor(r / 65536)
+    t[:, 1] = torch.floor(r / 256) % 256
+    t[:, 2] = r % 256
+    if H > 3:
+        t[:, 3:] = torch.randn(A, H - 3, generator=torch.Generator().manual_seed(A), dtype=torch.float64)
+    return t.to(dtype)
+
+
+def _untag(t):
+    v = t[:, :3].to(torch.float64)
+    return (v[:, 0] * 65536 + v[:, 1] * 256 + v[:, 2]).to(torch.int64)
+
+
+def _small_cases():
+    # (W, e, A, zero_prob, seed): several shapes, with empty segments/groups.
+    return [(1, 1, 5, 0.0, 0), (1, 4, 9, 0.3, 1), (3, 1, 8, 0.0, 2), (2, 2, 6, 0.5, 3),
+            (4, 3, 40, 0.4, 4), (8, 4, 100, 0.25, 5), (2, 8, 0, 0.0, 6), (5, 2, 1, 0.0, 7)]
+
+
+# ---- decoding ----------------------------------------------------------------
+
+def pin_decode_bf16_all_patterns(orc):
+    bits = torch.arange(-32768, 32768, dtype=torch.int32).to(torch.int16)
+    t = bits.view(torch.bfloat16)
+    got = orc.decode(t)
+    want = t.to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def pin_decode_fp16_all_patterns(orc):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    t = torch.from_numpy(bits.view(np.int16)).view(torch.float16)
+    got = orc.decode(t)
+    want = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+# ---- plan / permute -------------------------------------------------------------
+
+def pin_plan_golden(orc):
+    g = _golden("permute_w2e3.json")
+    src, dst, gr, go = orc.plan(g["W"], g["e"], g["recvCounts"], g["A"])
+    assert src.tolist() == g["src_off"]
+    assert dst.tolist() == g["dst_off"]
+    assert gr.tolist() == g["group_rows"]
+    assert go.tolist() == g["group_off"]
+
+
+def pin_plan_rejects_bad_counts(orc):
+    # Sum rule: A is the sum of recvCounts; negative counts are meaningless.
+    for rc, A in [([1, 2, 3, 4], 9), ([1, 2, 3, 4], 11), ([1, -1, 3, 4], 7)]:
+        try:
+            orc.plan(2, 2, rc, A)
+        except OracleError:
+            continue
+        raise AssertionError(f"plan accepted recvCounts={rc} with A={A}")
+
+
+def pin_permute_golden(orc):
+    g = _golden("permute_w2e3.json")
+    ata = _tagged(g["A"], 8, torch.bfloat16)
+    perm = orc.permute(g["W"], g["e"], g["recvCounts"], ata)
+    assert _untag(perm).tolist() == g["permuted_source_rows"]
+    assert torch.equal(perm.view(torch.int16), ata[g["permuted_source_rows"]].view(torch.int16))
+
+
+def pin_permute_matches_stable_sort(orc):
+    # Brute force: Permute is a stable sort of the arrival rows by local expert.
+    for W, e, A, zp, seed in _small_cases():
+        rc = random_counts(W, e, A, seed, zp)
+        experts = _expert_of_arrival_rows(W, e, rc)
+        want = sorted(range(A), key=lambda r: experts[r])
+        ata = _tagged(A, 4, torch.bfloat16)
+        perm = orc.permute(W, e, rc, ata)
+        assert _untag(perm).tolist() == want, (W, e, rc.tolist())
+
+
+def pin_permute_is_bijection_preserving_rows(orc):
+    for W, e, A, zp, seed in _small_cases() + [(16, 16, 3000, 0.1, 11)]:
+        rc = random_counts(W, e, A, seed, zp)
+        ata = _tagged(A, 16, torch.float16)
+        perm = orc.permute(W, e, rc, ata)
+        idx = _untag(perm)
+        assert sorted(idx.tolist()) == list(range(A))
+        assert torch.equal(perm.view(torch.int16), ata[idx].view(torch.int16))
+
+
+def pin_permute_identity_cases(orc):
+    # W = 1 or e = 1: arrival order already is expert order.
+    for W, e, A, seed in [(1, 1, 17, 0), (1, 6, 50, 1), (7, 1, 33, 2)]:
+        rc = random_counts(W, e, A, seed, 0.2)
+        ata = torch.randn(A, 24, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
+        perm = orc.permute(W, e, rc, ata)
+        assert torch.equal(perm.view(torch.int16), ata.view(torch.int16))
+
+
+def pin_group_rows_sum_rule(orc):
+    for W, e, A, zp, seed in _small_cases():
+        rc = random_counts(W, e, A, seed, zp)
+        _, _, gr, go = orc.plan(W, e, rc, A)
+        assert gr.tolist() == rc.reshape(W, e).sum(0).tolist()
+        assert go[-1] == A and go[0] == 0
+
+
+# ---- grouped matmul -------------------------------------------------------------
+
+def _to16(x, dtype):
+    return torch.tensor(np.asarray(x, dtype=np.float64)).to(dtype)
+
+
+def pin_grouped_matmul_golden(orc):
+    g = _golden("grouped_matmul_w2e2.json")
+    for dtype in (torch.bfloat16, torch.float16):
+        ata = _to16(g["ataOut"], dtype)
+        w = _to16(g["gmmWeight"], dtype)
+        perm, y, _ = orc.run(g["W"], g["e"], g["recvCounts"], ata, w)
+        assert perm.to(torch.float64).tolist() == g["permuteOut"]
+        assert y.tolist() == g["gmmY"]
+        mm = orc.matmul(_to16(g["mmX"], dtype), _to16(g["mmWeight"], dtype))
+        assert mm.tolist() == g["mmY"]
+
+
+def pin_single_group_is_numpy_matmul(orc):
+    # W = 1, e = 1: one plain product; numpy's float64 matmul is the library check.
+    rng = np.random.default_rng(5)
+    for A, H, N, dtype in [(33, 40, 24, torch.bfloat16), (64, 128, 72, torch.float16), (1, 8, 8, torch.bfloat16)]:
+        x = torch.from_numpy(rng.standard_normal((A, H))).to(dtype)
+        w = torch.from_numpy(rng.standard_normal((1, H, N))).to(dtype)
+        _, y, _ = orc.run(1, 1, [A], x, w)
+        ref = x.to(torch.float64).numpy() @ w[0].to(torch.float64).numpy()
+        np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_grouped_blocks_match_numpy(orc):
+    # Each expert block of gmmY is a standalone product of that block.
+    rng = np.random.default_rng(6)
+    for W, e, A, zp, seed in [(2, 2, 50, 0.0, 1), (4, 3, 70, 0.4, 2), (3, 5, 0, 0.0, 3)]:
+        rc = random_counts(W, e, A, seed, zp)
+        H, N = 48, 40
+        x = torch.from_numpy(rng.standard_normal((A, H))).to(torch.bfloat16)
+        w = torch.from_numpy(rng.standard_normal((e, H, N))).to(torch.bfloat16)
+        perm, y, _ = orc.run(W, e, rc, x, w)
+        experts = _expert_of_arrival_rows(W, e, rc)
+        order = sorted(range(A), key=lambda r: experts[r])
+        xs = x.to(torch.float64).numpy()
+        start = 0
+        for j in range(e):
+            rows = [r for r in order if experts[r] == j]
+            if rows:
+                ref = xs[rows] @ w[j].to(torch.float64).numpy()
+                np.testing.assert_allclose(y[start:start + len(rows)], ref, rtol=1e-12, atol=1e-12)
+            start += len(rows)
+        assert start == A
+
+
+def pin_identity_weight_exact(orc):
+    # gmmWeight[j] = I  =>  gmmY == permuteOut exactly.
+    W, e, A, H = 3, 4, 90, 32
+    rc = random_counts(W, e, A, 9, 0.3)
+    x = torch.randn(A, H, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    w = torch.eye(H).repeat(e, 1, 1).to(torch.bfloat16)
+    perm, y, _ = orc.run(W, e, rc, x, w)
+    assert np.array_equal(y, perm.to(torch.float64).numpy())
+
+
+def pin_scaled_one_hot_weight_exact(orc):
+    # gmmWeight[j][k][n] = 2^j [k == pi(n)]  =>  gmmY[i][n] = 2^{j(i)} permuteOut[i][pi(n)].
+    W, e, A, H, N = 2, 5, 80, 24, 16
+    rc = random_counts(W, e, A, 4, 0.3)
+    pi = np.random.default_rng(3).permutation(H)[:N]
+    w = torch.zeros(e, H, N, dtype=torch.float64)
+    for j in range(e):
+        w[j, pi, np.arange(N)] = 2.0 ** j
+    x = torch.randn(A, H, generator=torch.Generator().manual_seed(2)).to(torch.float16)
+    perm, y, _ = orc.run(W, e, rc, x, w.to(torch.float16))
+    _, _, gr, _ = orc.plan(W, e, rc, A)
+    scale = np.repeat(2.0 ** np.arange(e), gr)
+    want = perm.to(torch.float64).numpy()[:, pi] * scale[:, None]
+    assert np.array_equal(y, want)
+
+
+def pin_one_hot_activations_exact(orc):
+    # Arrival row r = unit vector e_{k(r)}  =>  its gmmY row = gmmWeight[j(r)][k(r)].
+    W, e, A, H, N = 3, 3, 45, 20, 12
+    rc = random_counts(W, e, A, 8, 0.2)
+    k_of = np.random.default_rng(4).integers(0, H, A)
+    x = torch.zeros(A, H, dtype=torch.float64)
+    x[np.arange(A), k_of] = 1.0
+    w = torch.randn(e, H, N, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    _, y, _ = orc.run(W, e, rc, x.to(torch.bfloat16), w)
+    experts = _expert_of_arrival_rows(W, e, rc)
+    order = sorted(range(A), key=lambda r: experts[r])
+    wd = w.to(torch.float64).numpy()
+    want = np.stack([wd[experts[r], k_of[r]] for r in order])
+    assert np.array_equal(y, want)
+
+
+def pin_integer_inputs_exact(orc):
+    # Small integers: every partial sum is an integer far below 2^53, so the
+    # result is exact and equals numpy's int64 product.
+    rng = np.random.default_rng(7)
+    W, e, A, H, N = 4, 2, 60, 64, 24
+    rc = random_counts(W, e, A, 10, 0.2)
+    xi = rng.integers(-4, 5, (A, H))
+    wi = rng.integers(-4, 5, (e, H, N))
+    x = torch.tensor(xi, dtype=torch.float64).to(torch.bfloat16)
+    w = torch.tensor(wi, dtype=torch.float64).to(torch.bfloat16)
+    _, y, _ = orc.run(W, e, rc, x, w)
+    experts = _expert_of_arrival_rows(W, e, rc)
+    order = sorted(range(A), key=lambda r: experts[r])
+    want = np.stack([xi[r] @ wi[experts[r]] for r in order]) if A else np.zeros((0, N))
+    assert np.array_equal(y, want.astype(np.float64))
+
+
+def pin_row_subset_equals_full(orc):
+    W, e, A, H, N = 2, 3, 40, 16, 8
+    rc = random_counts(W, e, A, 12, 0.2)
+    x = torch.randn(A, H, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    w = torch.randn(e, H, N, generator=torch.Generator().manual_seed(6)).to(torch.bfloat16)
+    perm, full, _ = orc.run(W, e, rc, x, w)
+    _, _, gr, _ = orc.plan(W, e, rc, A)
+    rows = [A - 1, 0, 7, 7, 19]
+    sub = orc.grouped_matmul(gr, perm, w, rows)
+    assert np.array_equal(sub, full[rows])
+
+
+# ---- shared expert ---------------------------------------------------------------
+
+def pin_shared_matmul_numpy(orc):
+    rng = np.random.default_rng(8)
+    for BS, H, N, dtype in [(17, 40, 24, torch.bfloat16), (32, 64, 48, torch.float16)]:
+        x = torch.from_numpy(rng.standard_normal((BS, H))).to(dtype)
+        w = torch.from_numpy(rng.standard_normal((H, N))).to(dtype)
+        y = orc.matmul(x, w)
+        ref = x.to(torch.float64).numpy() @ w.to(torch.float64).numpy()
+        np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+        rows = [BS - 1, 3]
+        assert np.array_equal(orc.matmul(x, w, rows), y[rows])
+
+
+def pin_shared_identity_and_integer_exact(orc):
+    rng = np.random.default_rng(9)
+    x = torch.randn(12, 16, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16)
+    y = orc.matmul(x, torch.eye(16).to(torch.bfloat16))
+    assert np.array_equal(y, x.to(torch.float64).numpy())
+    xi = rng.integers(-4, 5, (20, 96))
+    wi = rng.integers(-4, 5, (96, 40))
+    y = orc.matmul(torch.tensor(xi, dtype=torch.float64).to(torch.float16),
+                   torch.tensor(wi, dtype=torch.float64).to(torch.float16))
+    assert np.array_equal(y, (xi @ wi).astype(np.float64))
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
