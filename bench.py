@@ -1,0 +1,454 @@
+"""Benchmark of the Permute + GroupedMatMul (+ shared-expert MatMul) hot path.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--permute-out] [--path fused|split|default] [--impl reference]
+
+One step = one call of the whole hot path (segment scan, permute, routed
+grouped GEMM, shared-expert GEMM) on one rank's synthetic inputs, resident in
+HBM.  Prints one JSON line (rank 0).  Metric: algorithmic TFLOP/s,
+2 * A * H1 * N1 + 2 * BS * H2 * N2 per step, summed over ranks, divided by the
+max over ranks of the device time of the K timed steps.
+
+Under torchrun (N > 1) every rank runs its own expert-parallel rank's share
+(its own recvCounts and tensors): weak scaling, no collective on the data path.
+
+--impl reference times the CPU oracle (float64, OpenMP) on the host cores on a
+bounded sample of the same workload and prints the same line with
+"impl": "reference".
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from token_permute_grouped_gb300 import binding, build  # noqa: E402
+from token_permute_grouped_gb300.workloads import HEADLINE, WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "permute+grouped-GEMM TFLOP/s, % of GB300 bf16 dense peak; us per call"
+L2_BYTES = 129 * 2**20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def flops_of(wl, A):
+    return 2.0 * A * wl.H1 * wl.N1 + 2.0 * wl.BS * wl.H2 * wl.N2
+
+
+def algorithmic_bytes(wl, A, permute_out):
+    """Each input read once, each output written once (16-bit elements)."""
+    b = 2 * (A * wl.H1 + wl.e * wl.H1 * wl.N1 + A * wl.N1)
+    b += 2 * (wl.BS * wl.H2 + wl.H2 * wl.N2 + wl.BS * wl.N2)
+    b += 4 * wl.W * wl.e
+    if permute_out:
+        b += 2 * A * wl.H1
+    return b
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "token_permute_grouped_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, permute_out, path):
+    """DRAM bytes per launch of the GEMM kernel from a committed ncu summary,
+    only while the kernel sources are unchanged since the capture."""
+    for f in glob.glob(os.path.join(ROOT, "profiles", "*.json")):
+        try:
+            with open(f) as fh:
+                s = json.load(fh)
+        except (OSError, ValueError):
+            continue
+        if (s.get("workload") == workload and s.get("permute_out") == permute_out
+                and s.get("path") == path and s.get("source_hash") == source_hash()):
+            return s.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ distributed glue
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def reduce_max(x: float, world, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def timed_region(step, steps, world, device, sync):
+    """Barrier + sync on both sides of exactly `steps` calls of step(i);
+    returns (this rank's seconds, max over ranks)."""
+    barrier(world)
+    sync()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(i)
+    sync()
+    barrier(world)
+    dt = time.perf_counter() - t0
+    return dt, reduce_max(dt, world, device)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    world, rank, local = dist_env()
+    assert torch.cuda.is_available(), "bench.py needs a GPU (use --impl reference for the CPU oracle)"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    build.build()
+    binding.load()
+
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl, seed=0, rank=rank)
+    A = inp.A
+    dt = wl.torch_dtype
+    plan = binding.Plan(wl.W, wl.e, A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, dt,
+                        want_permute_out=args.permute_out, path=args.path, device=dev)
+    launches_per_call = binding.a2av_gmm_launch_count(plan.desc)
+
+    # Input replicas, rotated so that no step finds its inputs in L2.
+    set_bytes = algorithmic_bytes(wl, A, args.permute_out)
+    reps = max(2, -(-3 * L2_BYTES // max(set_bytes, 1)))
+    reps = min(reps, 64)
+    host = {"ataOut": inp.ataOut, "gmmWeight": inp.gmmWeight, "mmX": inp.mmX, "mmWeight": inp.mmWeight}
+    rc_dev = torch.from_numpy(inp.recvCounts).to(dev)
+    sets = []
+    for _ in range(reps):
+        s = {k: (v.to(dev) if v is not None else None) for k, v in host.items()}
+        s["gmmY"] = torch.empty(A, wl.N1, dtype=dt, device=dev)
+        s["mmY"] = torch.empty(wl.BS, wl.N2, dtype=dt, device=dev) if wl.BS else None
+        s["perm"] = torch.empty(A, wl.H1, dtype=dt, device=dev) if args.permute_out else None
+        sets.append(s)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        s = sets[i % reps]
+        plan.run(s["ataOut"], rc_dev, s["gmmWeight"], s["mmX"], s["mmWeight"], gmmY=s["gmmY"], mmY=s["mmY"],
+                 permuteOut=s["perm"], stream=stream)
+
+    sync = torch.cuda.synchronize
+    for i in range(args.warmup):
+        step(i)
+    sync()
+    st, code = binding.a2av_gmm_read_device_status(plan.workspace)
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({code})")
+
+    # Per-call device time on the launching stream (every call is one GEMM
+    # launch on the default path, so this is also that kernel's duration).
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+
+    def timed_step(i):
+        if i == 0:
+            ev[0].record(stream)
+        step(i)
+        ev[i + 1].record(stream)
+
+    with ClockSampler(local) as clocks:
+        wall, wall_max = timed_region(timed_step, args.steps, world, dev, sync)
+    per_call_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    dev_s = sum(per_call_ms) / 1e3
+    dev_s_max = reduce_max(dev_s, world, dev)
+    flops = flops_of(wl, A)
+    total_flops = reduce_sum(flops * args.steps, world, dev)
+    tflops = total_flops / dev_s_max / 1e12
+    ms_per_step = dev_s_max * 1e3 / args.steps
+
+    # End to end through the same public call with host buffers: this step's
+    # activations (ataOut, recvCounts, mmX) copied in from pinned memory, the
+    # results (gmmY, mmY) read back.  Weights stay resident, as in a model.
+    pin = {k: (v.pin_memory() if v is not None else None) for k, v in
+           {"ataOut": inp.ataOut, "mmX": inp.mmX}.items()}
+    rc_pin = torch.from_numpy(inp.recvCounts).pin_memory()
+    out_y = torch.empty(A, wl.N1, dtype=dt).pin_memory()
+    out_mm = torch.empty(wl.BS, wl.N2, dtype=dt).pin_memory() if wl.BS else None
+    h2d = pin["ataOut"].numel() * 2 + rc_pin.numel() * 4 + (pin["mmX"].numel() * 2 if wl.BS else 0)
+    d2h = out_y.numel() * 2 + (out_mm.numel() * 2 if wl.BS else 0)
+
+    def e2e_step(i):
+        s = sets[i % reps]
+        s["ataOut"].copy_(pin["ataOut"], non_blocking=True)
+        rc_dev.copy_(rc_pin, non_blocking=True)
+        if wl.BS:
+            s["mmX"].copy_(pin["mmX"], non_blocking=True)
+        step(i)
+        out_y.copy_(s["gmmY"], non_blocking=True)
+        if wl.BS:
+            out_mm.copy_(s["mmY"], non_blocking=True)
+
+    e2e_step(0)
+    sync()
+    e2e_steps = max(3, min(args.steps, 20))
+    _, e2e_max = timed_region(e2e_step, e2e_steps, world, dev, sync)
+    e2e_tflops = reduce_sum(flops * e2e_steps, world, dev) / e2e_max / 1e12
+
+    if rank != 0:
+        barrier(world)
+        return
+    pk, pk_kind = peaks()
+    peak_tf = pk["bf16_tflops"]
+    per_call_us = statistics.median(per_call_ms) * 1e3
+    achieved = flops / (dev_s / args.steps) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic (seeded routing and N(0,1) tensors; no dataset)",
+        "config": {
+            "workload": wl.name, "W": wl.W, "e": wl.e, "A": A, "H1": wl.H1, "N1": wl.N1,
+            "BS": wl.BS, "H2": wl.H2, "N2": wl.N2, "path": args.path,
+            "permute_out": bool(args.permute_out), "accumulate": "fp32",
+            "us_per_call_median": round(per_call_us, 2),
+            "us_per_call_min": round(min(per_call_ms) * 1e3, 2),
+            "pct_of_bf16_peak": round(100 * tflops / world / peak_tf, 2),
+            "pct_of_bf16_sustained": round(100 * tflops / world / pk["bf16_tflops_sustained"], 2),
+            "gflop_per_call": round(flops / 1e9, 3),
+            "l2": f"inputs rotated over {reps} replicas ({reps * set_bytes / 2**20:.0f} MiB > 129 MiB L2)",
+            "group_rows": inp.recvCounts.reshape(wl.W, wl.e).sum(0).tolist(),
+            "launches_per_call": launches_per_call,
+        },
+        "roofline": {
+            "bound": "tensor",
+            "achieved": round(achieved, 2),
+            "peak": peak_tf,
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak_tf, 4),
+            "traffic": profiled_traffic(wl.name, bool(args.permute_out), args.path),
+            "kernel": "grouped_gemm_kernel",
+            "peak_source": f"{pk_kind} bf16 dense burst (MEASURED_PEAKS.json bf16_tflops)" if pk_kind == "measured"
+            else "fallback 1.9 PFLOP/s",
+            "algorithmic_bytes": algorithmic_bytes(wl, A, args.permute_out),
+        },
+        "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
+                "inputs_copied": "ataOut, recvCounts, mmX (weights resident)"},
+        "gpu_launches": launches_per_call * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def oracle_sample(wl, inp, seconds, seed=0):
+    """Time the oracle on a seeded sample of output rows; returns
+    (FLOPs done, seconds, rows, threads, description).  The oracle's permute
+    (a copy of every row) runs once, untimed, to give it its own input."""
+    import oracle
+    orc = oracle.Oracle()
+    A = inp.A
+    perm = orc.permute(wl.W, wl.e, inp.recvCounts, inp.ataOut)
+    _, _, gr, _ = orc.plan(wl.W, wl.e, inp.recvCounts, A)
+    rng = np.random.default_rng(seed)
+    per_row_routed = 2.0 * wl.H1 * wl.N1
+    per_row_shared = 2.0 * wl.H2 * wl.N2
+    total_rows = A + wl.BS
+    chunk = max(orc.num_threads(), 8)
+    flops = 0.0
+    rows_done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds and rows_done < total_rows:
+        r = rng.integers(0, total_rows, chunk)
+        routed = r[r < A]
+        shared = r[r >= A] - A
+        if len(routed):
+            orc.grouped_matmul(gr, perm, inp.gmmWeight, routed)
+            flops += per_row_routed * len(routed)
+        if len(shared):
+            orc.matmul(inp.mmX, inp.mmWeight, shared)
+            flops += per_row_shared * len(shared)
+        rows_done += chunk
+    el = time.perf_counter() - t0
+    desc = (f"{rows_done} output rows drawn uniformly from the {total_rows} rows of gmmY and mmY "
+            f"of {wl.name} (float64 oracle, full K per row)")
+    return flops, el, rows_done, orc.num_threads(), desc
+
+
+def cpu_baseline(wl, inp, seconds):
+    flops, el, rows, threads, desc = oracle_sample(wl, inp, seconds)
+    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": desc, "seconds": round(el, 2)}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return  # rank 0 alone times the oracle
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl, seed=0)
+    per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(wl, inp, per_step / 4)
+    tot_f = tot_s = 0.0
+    threads = 1
+    desc = ""
+    for i in range(args.steps):
+        f, s, _, threads, desc = oracle_sample(wl, inp, per_step, seed=i + 1)
+        tot_f += f
+        tot_s += s
+    tf = tot_f / tot_s / 1e12
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(tf, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_s * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "W": wl.W, "e": wl.e, "A": inp.A, "H1": wl.H1, "N1": wl.N1,
+                   "BS": wl.BS, "H2": wl.H2, "N2": wl.N2, "seconds_per_step": per_step},
+        "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--permute-out", action="store_true")
+    ap.add_argument("--path", default="default", choices=["default", "fused", "split"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

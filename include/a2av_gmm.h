@@ -1,0 +1,143 @@
+/*
+ * a2av_gmm — Permute + GroupedMatMul (+ shared-expert MatMul) on one GB300.
+ *
+ * The receive side of an expert-parallel MoE layer, after the AlltoAllv has
+ * landed on this GPU.  Operation ("aclnnAlltoAllvGroupedMatMul" operator
+ * page, "API function" and "Formula"):
+ *
+ *     permuteOut = Permute(ataOut)             routed experts
+ *     gmmY       = permuteOut x gmmWeight      one [H1, N1] matrix per expert
+ *     mmY        = mmX x mmWeight              shared expert, independent
+ *
+ * Two-phase call, as on that page ("... is called to obtain the input
+ * parameters and compute the required workspace size ... Then ... is called
+ * to perform computation"): a2av_gmm_workspace_size() validates the
+ * descriptor and sizes the workspace on the host; a2av_gmm_run() enqueues the
+ * work on a CUDA stream.  Both return a status code ("Returns": status code;
+ * the first phase implements input parameter verification).
+ *
+ * Shapes and ranges ("Shape variables"):
+ *     W   ranks in the expert-parallel domain (sources of ataOut)
+ *     e   experts on this rank, 1 <= e <= 32, and W * e <= 256
+ *     A   rows received = sum of recvCounts (0 allowed: only mmY is computed)
+ *     H1  routed hidden size, 0 < H1 < 65536
+ *     N1  routed output width, 0 < N1 < 65536
+ *     BS  shared-expert rows (0 = no shared expert)
+ *     H2  shared hidden size, 0 < H2 <= 12288 (when BS > 0)
+ *     N2  shared output width, 0 < N2 < 65536 (when BS > 0)
+ * This library additionally needs H1, N1, H2, N2 to be multiples of 8 (rows
+ * start on 16-byte boundaries) and A <= 2^31 - 1.
+ *
+ * Layouts (all row-major, contiguous, 16-byte aligned, device memory):
+ *     ataOut     [A, H1]     rank-major: all rows from source 0 (its rows for
+ *                            expert 0, then expert 1, ...), then source 1, ...
+ *     recvCounts [W * e]     int32, entry w * e + j = rows from source w for
+ *                            local expert j
+ *     gmmWeight  [e, H1, N1]
+ *     mmX        [BS, H2],  mmWeight [H2, N2],  mmY [BS, N2]
+ *     permuteOut [A, H1]     expert-major: rows of expert 0 (source 0 first,
+ *                            arrival order kept), then expert 1, ...
+ *     gmmY       [A, N1]     row i pairs with row i of permuteOut
+ * Element type: bf16 or fp16 for every tensor (same type throughout);
+ * products accumulate in fp32 and are rounded to the element type (nearest
+ * even).
+ *
+ * Ownership: the caller owns every buffer, including the workspace.  The
+ * library allocates nothing, never synchronises inside a2av_gmm_run, and
+ * keeps no pointer after the call returns; the workspace may be reused once
+ * the stream has passed the call.  Results are deterministic: the same inputs
+ * give bitwise the same outputs ("Deterministic computing").
+ *
+ * Errors found on the device (recvCounts that do not sum to A, a negative
+ * count) cannot be returned by the asynchronous call: the kernels then write
+ * no output and record the error in the workspace, where
+ * a2av_gmm_read_device_status() finds it.
+ */
+#ifndef A2AV_GMM_H
+#define A2AV_GMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *a2av_stream_t;
+
+typedef enum {
+    A2AV_OK = 0,
+    A2AV_ERR_NULLPTR = 1,      /* a required pointer is NULL */
+    A2AV_ERR_INVALID = 2,      /* shape, range or dtype outside the limits above */
+    A2AV_ERR_UNSUPPORTED = 3,  /* allowed by the operator, not by this build (alignment) */
+    A2AV_ERR_WORKSPACE = 4,    /* workspace too small or misaligned */
+    A2AV_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
+    A2AV_ERR_DEVICE_CHECK = 6  /* the device found inconsistent recvCounts */
+} a2av_status;
+
+typedef enum { A2AV_BF16 = 0, A2AV_FP16 = 1 } a2av_dtype;
+
+/* Execution path.  Both give bitwise-identical outputs. */
+typedef enum {
+    A2AV_PATH_DEFAULT = 0,     /* the fastest path this build has */
+    A2AV_PATH_FUSED = 1,       /* the grouped GEMM gathers its A rows from ataOut */
+    A2AV_PATH_SPLIT = 2        /* a permute kernel first, then the grouped GEMM */
+} a2av_path;
+
+typedef struct {
+    int32_t W, e;              /* ranks, local experts */
+    int64_t A, H1, N1;         /* routed experts */
+    int64_t BS, H2, N2;        /* shared expert; BS = 0: none */
+    int32_t dtype;             /* a2av_dtype */
+    int32_t want_permute_out;  /* nonzero: permuteOut is written */
+    int32_t path;              /* a2av_path */
+    int32_t reserved;          /* set to 0 */
+} a2av_gmm_desc;
+
+/*
+ * Phase 1 (host only, touches no GPU).  Validates *desc against the limits
+ * above and writes the workspace size in bytes to *bytes.
+ * Returns A2AV_ERR_NULLPTR if desc or bytes is NULL, A2AV_ERR_INVALID or
+ * A2AV_ERR_UNSUPPORTED for a bad descriptor, else A2AV_OK.
+ */
+a2av_status a2av_gmm_workspace_size(const a2av_gmm_desc *desc, size_t *bytes);
+
+/*
+ * Phase 2.  Enqueues the whole hot path on `stream` and returns without
+ * waiting.  Pointers are device pointers.  mmX, mmWeight and mmY may be NULL
+ * when desc->BS == 0; permuteOut may be NULL unless desc->want_permute_out.
+ * ataOut and gmmY may be NULL when desc->A == 0.  workspace must be 256-byte
+ * aligned and at least the size phase 1 returned.
+ * Returns: the phase-1 codes for the descriptor; A2AV_ERR_NULLPTR for a
+ * missing required pointer; A2AV_ERR_UNSUPPORTED for a pointer that is not
+ * 16-byte aligned; A2AV_ERR_WORKSPACE; A2AV_ERR_CUDA when a launch fails.
+ */
+a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut,
+                         const int32_t *recvCounts, const void *gmmWeight,
+                         const void *mmX, const void *mmWeight, void *permuteOut,
+                         void *gmmY, void *mmY, void *workspace,
+                         size_t workspace_bytes, a2av_stream_t stream);
+
+/*
+ * Waits for `stream`, then reads the device-side status a2av_gmm_run left in
+ * `workspace`: A2AV_OK, or A2AV_ERR_DEVICE_CHECK (recvCounts negative or not
+ * summing to A; outputs were not written), or A2AV_ERR_CUDA (a kernel gave up
+ * waiting on one of its own pipeline barriers).  The raw device word is
+ * written to *code when code is not NULL.  For tests and diagnostics: it
+ * synchronises.
+ */
+a2av_status a2av_gmm_read_device_status(const void *workspace, a2av_stream_t stream,
+                                        int32_t *code);
+
+/* A static, human-readable name for a status code. */
+const char *a2av_gmm_status_string(a2av_status status);
+
+/* Kernels a2av_gmm_run launches for this descriptor (0 on a bad descriptor). */
+int32_t a2av_gmm_launch_count(const a2av_gmm_desc *desc);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* A2AV_GMM_H */

@@ -1,0 +1,141 @@
+"""The C ABI on the host: exports, phase-1 validation, phase-2 argument checks.
+
+No GPU needed: every call here returns before the library touches CUDA.
+"""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from token_permute_grouped_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "a2av_gmm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(a2av_gmm_\w+)\s*\(", text)))
+
+
+def test_header_declares_binding_exports():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True).stdout
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}\b", out), name
+
+
+def ws(**kw):
+    base = dict(W=8, e=4, A=16000, H1=4096, N1=1024, BS=2048, H2=4096, N2=1024)
+    base.update(kw)
+    d = binding.make_desc(**{k: base[k] for k in ("W", "e", "A", "H1", "N1", "BS", "H2", "N2")},
+                          dtype=kw.get("dtype", torch.bfloat16), want_permute_out=kw.get("perm", False),
+                          path=kw.get("path", "default"))
+    for f in ("dtype", "reserved", "path"):
+        if f"raw_{f}" in kw:
+            setattr(d, f, kw[f"raw_{f}"])
+    n = ctypes.c_size_t(0)
+    st = binding.load().a2av_gmm_workspace_size(ctypes.byref(d), ctypes.byref(n))
+    return st, n.value
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, 0),
+    ({"e": 32, "W": 8}, 0),
+    ({"e": 33, "W": 1}, 2),             # e <= 32
+    ({"e": 32, "W": 9}, 2),             # e * W <= 256
+    ({"W": 0}, 2),
+    ({"H1": 65536}, 2),                 # 0 < H1 < 65536
+    ({"H1": 0}, 2),
+    ({"N1": 65536}, 2),
+    ({"H2": 12288}, 0),                 # 0 < H2 <= 12288
+    ({"H2": 12296}, 2),
+    ({"N2": 65536}, 2),
+    ({"BS": 0, "H2": 0, "N2": 0}, 0),   # no shared expert
+    ({"A": 0}, 0),                      # a rank may receive nothing
+    ({"A": -1}, 2),
+    ({"A": 2**31}, 2),
+    ({"raw_dtype": 7}, 2),
+    ({"raw_reserved": 1}, 2),
+    ({"raw_path": 9}, 2),
+    ({"H1": 4100}, 3),                  # rows must start 16-byte aligned
+    ({"N2": 1020}, 3),
+    ({"dtype": torch.float16}, 0),
+])
+def test_phase1_validation(lib, kw, status):
+    assert ws(**kw)[0] == status
+
+
+def test_workspace_sizes(lib):
+    assert ws()[1] == 256
+    assert ws(path="fused")[1] == 256
+    st, n = ws(path="split", A=1000, H1=512)
+    assert st == 0 and n == 256 + 1000 * 512 * 2
+    assert ws(path="split", A=1000, H1=512, perm=True)[1] == 256  # stages in permuteOut
+    assert ws(path="split", A=0)[1] == 256
+
+
+def test_launch_counts(lib):
+    d = binding.make_desc(8, 4, 1000, 512, 256, path="fused")
+    assert binding.a2av_gmm_launch_count(d) == 1
+    d = binding.make_desc(8, 4, 1000, 512, 256, path="split")
+    assert binding.a2av_gmm_launch_count(d) == 2
+    d = binding.make_desc(8, 4, 0, 512, 256, path="split")
+    assert binding.a2av_gmm_launch_count(d) == 1
+    d = binding.make_desc(8, 40, 1000, 512, 256)
+    assert binding.a2av_gmm_launch_count(d) == 0
+
+
+def _run(lib, d, **ptrs):
+    names = ["ataOut", "recvCounts", "gmmWeight", "mmX", "mmWeight", "permuteOut", "gmmY", "mmY", "workspace"]
+    args = [ctypes.c_void_p(ptrs.get(n, 0x10000 + 0x1000 * i)) for i, n in enumerate(names)]
+    return lib.a2av_gmm_run(ctypes.byref(d), *args, ptrs.get("wsbytes", 1 << 20), None)
+
+
+def test_phase2_argument_checks(lib):
+    d = binding.make_desc(8, 4, 1000, 512, 256, 64, 128, 64, want_permute_out=True)
+    assert _run(lib, d, ataOut=0) == 1
+    assert _run(lib, d, recvCounts=0) == 1
+    assert _run(lib, d, gmmWeight=0) == 1
+    assert _run(lib, d, mmX=0) == 1
+    assert _run(lib, d, permuteOut=0) == 1
+    assert _run(lib, d, workspace=0) == 1
+    assert _run(lib, d, gmmY=0x10008) == 3        # not 16-byte aligned
+    assert _run(lib, d, recvCounts=0x10002) == 3
+    assert _run(lib, d, workspace=0x10080) == 4   # not 256-byte aligned
+    assert _run(lib, d, wsbytes=100) == 4
+    d.e = 99
+    assert _run(lib, d) == 2
+    # A = 0 and no shared expert: ataOut, gmmY, mmX... may all be NULL
+    d = binding.make_desc(8, 4, 0, 512, 256, path="split")
+    d2 = binding.make_desc(8, 4, 0, 512, 256, 64, 128, 64)
+    assert _run(lib, d2, mmY=0) == 1
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert binding.a2av_gmm_status_string(code)
+    assert "unknown" in binding.a2av_gmm_status_string(42)
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "nope.so"))
+    with pytest.raises(ImportError):
+        binding.load()

@@ -1,0 +1,180 @@
+"""ctypes binding of liba2av_gmm.so: argument marshalling only.
+
+Same names as the C ABI in include/a2av_gmm.h.  Every step of the hot path
+runs in the library's CUDA kernels; this module only checks tensors, sizes the
+outputs and workspace with torch, and passes raw device pointers and the
+current CUDA stream.  There is no CPU fallback: without the built library
+every entry point raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+A2AV_OK = 0
+STATUS_NAMES = {0: "A2AV_OK", 1: "A2AV_ERR_NULLPTR", 2: "A2AV_ERR_INVALID", 3: "A2AV_ERR_UNSUPPORTED",
+                4: "A2AV_ERR_WORKSPACE", 5: "A2AV_ERR_CUDA", 6: "A2AV_ERR_DEVICE_CHECK"}
+DTYPES = {torch.bfloat16: 0, torch.float16: 1}
+PATHS = {"default": 0, "fused": 1, "split": 2}
+
+# Every symbol include/a2av_gmm.h declares.
+EXPORTS = ("a2av_gmm_workspace_size", "a2av_gmm_run", "a2av_gmm_read_device_status",
+           "a2av_gmm_status_string", "a2av_gmm_launch_count")
+
+
+class A2avError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_int32), ("e", ctypes.c_int32),
+                ("A", ctypes.c_int64), ("H1", ctypes.c_int64), ("N1", ctypes.c_int64),
+                ("BS", ctypes.c_int64), ("H2", ctypes.c_int64), ("N2", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("want_permute_out", ctypes.c_int32),
+                ("path", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load the built library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise ImportError(f"CUDA library not built: {_build.LIB} (run __graft_entry__.build())")
+        L = ctypes.CDLL(_build.LIB)
+        p, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+        L.a2av_gmm_workspace_size.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(sz)]
+        L.a2av_gmm_workspace_size.restype = ctypes.c_int
+        L.a2av_gmm_run.argtypes = [ctypes.POINTER(Desc), p, p, p, p, p, p, p, p, p, sz, p]
+        L.a2av_gmm_run.restype = ctypes.c_int
+        L.a2av_gmm_read_device_status.argtypes = [p, p, ctypes.POINTER(i32)]
+        L.a2av_gmm_read_device_status.restype = ctypes.c_int
+        L.a2av_gmm_status_string.argtypes = [ctypes.c_int]
+        L.a2av_gmm_status_string.restype = ctypes.c_char_p
+        L.a2av_gmm_launch_count.argtypes = [ctypes.POINTER(Desc)]
+        L.a2av_gmm_launch_count.restype = i32
+        _lib = L
+    return _lib
+
+
+def make_desc(W, e, A, H1, N1, BS=0, H2=0, N2=0, dtype=torch.bfloat16, want_permute_out=False,
+              path="default") -> Desc:
+    return Desc(W, e, A, H1, N1, BS, H2, N2, DTYPES[dtype], int(bool(want_permute_out)), PATHS[path], 0)
+
+
+def a2av_gmm_workspace_size(desc: Desc) -> int:
+    n = ctypes.c_size_t(0)
+    st = load().a2av_gmm_workspace_size(ctypes.byref(desc), ctypes.byref(n))
+    if st != A2AV_OK:
+        raise A2avError(st, "a2av_gmm_workspace_size")
+    return n.value
+
+
+def a2av_gmm_launch_count(desc: Desc) -> int:
+    return int(load().a2av_gmm_launch_count(ctypes.byref(desc)))
+
+
+def a2av_gmm_status_string(status: int) -> str:
+    return load().a2av_gmm_status_string(status).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def a2av_gmm_run(desc: Desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permuteOut, gmmY, mmY,
+                 workspace: torch.Tensor, stream=None) -> None:
+    """Raw phase 2: device tensors (or None) in, enqueued on the stream."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = load().a2av_gmm_run(ctypes.byref(desc), _ptr(ataOut), _ptr(recvCounts), _ptr(gmmWeight),
+                             _ptr(mmX), _ptr(mmWeight), _ptr(permuteOut), _ptr(gmmY), _ptr(mmY),
+                             _ptr(workspace), workspace.numel(), ctypes.c_void_p(s.cuda_stream))
+    if st != A2AV_OK:
+        raise A2avError(st, "a2av_gmm_run")
+
+
+def a2av_gmm_read_device_status(workspace: torch.Tensor, stream=None) -> tuple[int, int]:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    code = ctypes.c_int32(0)
+    st = load().a2av_gmm_read_device_status(_ptr(workspace), ctypes.c_void_p(s.cuda_stream),
+                                             ctypes.byref(code))
+    return st, code.value
+
+
+def _check(t, name, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+
+
+class Plan:
+    """Descriptor + workspace for one shape, reusable across calls."""
+
+    def __init__(self, W, e, A, H1, N1, BS=0, H2=0, N2=0, dtype=torch.bfloat16,
+                 want_permute_out=False, path="default", device=None):
+        self.desc = make_desc(W, e, A, H1, N1, BS, H2, N2, dtype, want_permute_out, path)
+        self.dtype = dtype
+        self.device = torch.device(device) if device is not None else torch.device("cuda")
+        self.workspace = torch.empty(a2av_gmm_workspace_size(self.desc), dtype=torch.uint8, device=self.device)
+
+    def run(self, ataOut, recvCounts, gmmWeight, mmX=None, mmWeight=None, gmmY=None, mmY=None,
+            permuteOut=None, stream=None):
+        d = self.desc
+        if d.A:
+            _check(ataOut, "ataOut", self.dtype, 2)
+        _check(recvCounts, "recvCounts", torch.int32, 1)
+        _check(gmmWeight, "gmmWeight", self.dtype, 3)
+        if tuple(gmmWeight.shape) != (d.e, d.H1, d.N1):
+            raise ValueError("gmmWeight shape")
+        if recvCounts.numel() != d.W * d.e:
+            raise ValueError("recvCounts length")
+        if gmmY is None:
+            gmmY = torch.empty(d.A, d.N1, dtype=self.dtype, device=self.device)
+        if d.want_permute_out and permuteOut is None:
+            permuteOut = torch.empty(d.A, d.H1, dtype=self.dtype, device=self.device)
+        if d.BS:
+            _check(mmX, "mmX", self.dtype, 2)
+            _check(mmWeight, "mmWeight", self.dtype, 2)
+            if mmY is None:
+                mmY = torch.empty(d.BS, d.N2, dtype=self.dtype, device=self.device)
+        a2av_gmm_run(d, ataOut if d.A else None, recvCounts, gmmWeight, mmX, mmWeight,
+                     permuteOut if d.want_permute_out else None, gmmY if d.A else None,
+                     mmY if d.BS else None, self.workspace, stream)
+        return gmmY, mmY, permuteOut
+
+
+def a2av_gmm(ataOut, recvCounts, gmmWeight, mmX=None, mmWeight=None, return_permute=False,
+             W=None, path="default"):
+    """permuteOut = Permute(ataOut); gmmY = permuteOut x gmmWeight; mmY = mmX x mmWeight.
+
+    Returns (gmmY, mmY or None, permuteOut or None).  W defaults to
+    len(recvCounts) // e.
+    """
+    e, H1, N1 = gmmWeight.shape
+    if W is None:
+        W = recvCounts.numel() // e
+    BS, H2, N2 = (0, 0, 0)
+    if mmX is not None:
+        BS, H2 = mmX.shape
+        N2 = mmWeight.shape[1]
+    plan = Plan(W, e, ataOut.shape[0], H1, N1, BS, H2, N2, gmmWeight.dtype, return_permute, path,
+                device=gmmWeight.device)
+    return plan.run(ataOut, recvCounts, gmmWeight, mmX, mmWeight)

@@ -1,0 +1,245 @@
+// C ABI of the library (declared in include/a2av_gmm.h).
+//
+// Two-phase call of the "aclnnAlltoAllvGroupedMatMul" page: phase 1 checks the
+// parameters and sizes the workspace ("The first-phase API implements input
+// parameter verification"), phase 2 runs on a stream.  Limits come from the
+// page's "Shape variables" list.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "a2av_gmm.h"
+#include "kernels.h"
+#include "plan.cuh"
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;  // status word, padded to keep what follows aligned
+constexpr int kMaxDevices = 64;
+constexpr int kBM = 128;
+
+bool mult8(int64_t v) { return v % 8 == 0; }
+
+a2av_status validate(const a2av_gmm_desc *d) {
+    if (!d) return A2AV_ERR_NULLPTR;
+    if (d->W < 1 || d->e < 1 || d->e > a2av::kMaxExperts) return A2AV_ERR_INVALID;
+    if (static_cast<int64_t>(d->W) * d->e > a2av::kMaxSegments) return A2AV_ERR_INVALID;
+    if (d->H1 <= 0 || d->H1 >= 65536 || d->N1 <= 0 || d->N1 >= 65536) return A2AV_ERR_INVALID;
+    if (d->A < 0 || d->A > INT32_MAX) return A2AV_ERR_INVALID;
+    if (d->BS < 0 || d->BS > INT32_MAX) return A2AV_ERR_INVALID;
+    if (d->BS > 0) {
+        if (d->H2 <= 0 || d->H2 > 12288 || d->N2 <= 0 || d->N2 >= 65536) return A2AV_ERR_INVALID;
+    }
+    if (d->dtype != A2AV_BF16 && d->dtype != A2AV_FP16) return A2AV_ERR_INVALID;
+    if (d->path < A2AV_PATH_DEFAULT || d->path > A2AV_PATH_SPLIT) return A2AV_ERR_INVALID;
+    if (d->reserved != 0) return A2AV_ERR_INVALID;
+    if (!mult8(d->H1) || !mult8(d->N1)) return A2AV_ERR_UNSUPPORTED;
+    if (d->BS > 0 && (!mult8(d->H2) || !mult8(d->N2))) return A2AV_ERR_UNSUPPORTED;
+    return A2AV_OK;
+}
+
+bool use_split(const a2av_gmm_desc *d) { return d->path == A2AV_PATH_SPLIT; }
+
+// Bytes of the expert-major staging buffer the split path needs when the
+// caller does not ask for permuteOut.
+size_t staging_bytes(const a2av_gmm_desc *d) {
+    if (!use_split(d) || d->want_permute_out || d->A == 0) return 0;
+    const size_t b = static_cast<size_t>(d->A) * d->H1 * 2;
+    return (b + 255) / 256 * 256;
+}
+
+// Tile width: the fewest column tiles of at most 256, then the narrowest
+// multiple of 16 that covers N with that many tiles.
+int pick_bn(int64_t N) {
+    const int64_t tiles = (N + 255) / 256;
+    int64_t bn = (N + tiles - 1) / tiles;
+    bn = (bn + 15) / 16 * 16;
+    return static_cast<int>(std::max<int64_t>(bn, 16));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+CUtensorMapDataType tmap_type(int32_t dtype) {
+    return dtype == A2AV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// [rows, cols] row-major; box = 64 columns x 128 rows, 128-byte swizzle.
+bool make_rows_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int32_t dtype) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+    cuuint32_t box[2] = {64, kBM};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, tmap_type(dtype), 2, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [groups, K, N] row-major weights; box = 64 columns (N) x 64 rows (K) x 1.
+bool make_weight_map(CUtensorMap *m, const void *ptr, int64_t groups, int64_t K, int64_t N, int32_t dtype) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K),
+                          static_cast<cuuint64_t>(groups)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(N * 2), static_cast<cuuint64_t>(K * N * 2)};
+    cuuint32_t box[3] = {64, 64, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, tmap_type(dtype), 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+a2av_status a2av_gmm_workspace_size(const a2av_gmm_desc *desc, size_t *bytes) {
+    if (!desc || !bytes) return A2AV_ERR_NULLPTR;
+    const a2av_status s = validate(desc);
+    if (s != A2AV_OK) return s;
+    *bytes = kStatusBytes + staging_bytes(desc);
+    return A2AV_OK;
+}
+
+int32_t a2av_gmm_launch_count(const a2av_gmm_desc *desc) {
+    if (validate(desc) != A2AV_OK) return 0;
+    return (use_split(desc) && desc->A > 0) ? 2 : 1;
+}
+
+a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const int32_t *recvCounts,
+                         const void *gmmWeight, const void *mmX, const void *mmWeight, void *permuteOut,
+                         void *gmmY, void *mmY, void *workspace, size_t workspace_bytes,
+                         a2av_stream_t stream_handle) {
+    const a2av_status vs = validate(desc);
+    if (vs != A2AV_OK) return vs;
+    const a2av_gmm_desc &d = *desc;
+    const bool has_routed = d.A > 0;
+    const bool has_shared = d.BS > 0;
+    if (!recvCounts || !gmmWeight || !workspace) return A2AV_ERR_NULLPTR;
+    if (has_routed && (!ataOut || !gmmY)) return A2AV_ERR_NULLPTR;
+    if (has_routed && d.want_permute_out && !permuteOut) return A2AV_ERR_NULLPTR;
+    if (has_shared && (!mmX || !mmWeight || !mmY)) return A2AV_ERR_NULLPTR;
+    const void *ptrs[] = {ataOut, gmmWeight, mmX, mmWeight, gmmY, mmY,
+                          d.want_permute_out ? permuteOut : nullptr};
+    for (const void *q : ptrs)
+        if (!aligned16(q)) return A2AV_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(recvCounts) & 3u) != 0) return A2AV_ERR_UNSUPPORTED;
+    size_t need = 0;
+    a2av_gmm_workspace_size(desc, &need);
+    if (workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return A2AV_ERR_WORKSPACE;
+
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    const int sms = sm_count();
+    if (sms <= 0) return A2AV_ERR_CUDA;
+    int32_t *status = static_cast<int32_t *>(workspace);
+    void *perm_out = d.want_permute_out ? permuteOut : nullptr;
+    const bool split = use_split(&d);
+
+    a2av::GemmLaunch g;
+    std::memset(&g, 0, sizeof g);
+    g.recvCounts = recvCounts;
+    g.W = d.W;
+    g.e = d.e;
+    g.A = static_cast<int32_t>(d.A);
+    g.H1 = static_cast<int32_t>(d.H1);
+    g.N1 = static_cast<int32_t>(d.N1);
+    g.bn1 = pick_bn(d.N1);
+    g.BS = has_shared ? static_cast<int32_t>(d.BS) : 0;
+    g.H2 = has_shared ? static_cast<int32_t>(d.H2) : 0;
+    g.N2 = has_shared ? static_cast<int32_t>(d.N2) : 0;
+    g.bn2 = has_shared ? pick_bn(d.N2) : 0;
+    g.gmmY = gmmY;
+    g.mmY = mmY;
+    g.status = status;
+    g.bf16 = d.dtype == A2AV_BF16;
+    g.gather = split ? 0 : 1;
+    g.ataOut = ataOut;
+    g.permuteOut = split ? nullptr : perm_out;
+
+    if (!make_weight_map(&g.tmB_routed, gmmWeight, d.e, d.H1, d.N1, d.dtype)) return A2AV_ERR_CUDA;
+    if (has_shared) {
+        if (!make_rows_map(&g.tmA_shared, mmX, d.BS, d.H2, d.dtype)) return A2AV_ERR_CUDA;
+        if (!make_weight_map(&g.tmB_shared, mmWeight, 1, d.H2, d.N2, d.dtype)) return A2AV_ERR_CUDA;
+    }
+
+    bool permute_ran = false;
+    if (has_routed) {
+        if (split) {
+            // Expert-major rows go to permuteOut, or to the staging area.
+            void *dst = perm_out ? perm_out : static_cast<uint8_t *>(workspace) + kStatusBytes;
+            a2av::PermuteLaunch pl{recvCounts, d.W, d.e, static_cast<int32_t>(d.A),
+                                   static_cast<int32_t>(d.H1), ataOut, dst, status, 1};
+            if (a2av::launch_permute(pl, sms, stream) != cudaSuccess) return A2AV_ERR_CUDA;
+            permute_ran = true;
+            if (!make_rows_map(&g.tmA_routed, dst, d.A, d.H1, d.dtype)) return A2AV_ERR_CUDA;
+        } else if (perm_out) {
+            if (!make_rows_map(&g.tmA_routed, perm_out, d.A, d.H1, d.dtype)) return A2AV_ERR_CUDA;
+        }
+    }
+    g.write_status = permute_ran ? 0 : 1;
+
+    // Persistent grid: at most one CTA per SM, never more CTAs than tiles.
+    const int64_t tn1 = (d.N1 + g.bn1 - 1) / g.bn1;
+    int64_t tiles = ((d.A + kBM - 1) / kBM + d.e) * tn1;
+    if (has_shared) tiles += ((d.BS + kBM - 1) / kBM) * ((d.N2 + g.bn2 - 1) / g.bn2);
+    g.grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(sms, tiles)));
+    if (a2av::launch_grouped_gemm(g, stream) != cudaSuccess) return A2AV_ERR_CUDA;
+    return A2AV_OK;
+}
+
+a2av_status a2av_gmm_read_device_status(const void *workspace, a2av_stream_t stream, int32_t *code) {
+    if (!workspace) return A2AV_ERR_NULLPTR;
+    int32_t word = 0;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return A2AV_ERR_CUDA;
+    if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return A2AV_ERR_CUDA;
+    if (code) *code = word;
+    if (word & a2av::kStatusTimeout) return A2AV_ERR_CUDA;
+    if (word & a2av::kStatusBadCounts) return A2AV_ERR_DEVICE_CHECK;
+    return A2AV_OK;
+}
+
+const char *a2av_gmm_status_string(a2av_status status) {
+    switch (status) {
+        case A2AV_OK: return "ok";
+        case A2AV_ERR_NULLPTR: return "a required pointer is NULL";
+        case A2AV_ERR_INVALID: return "shape, range or dtype outside the operator's limits";
+        case A2AV_ERR_UNSUPPORTED: return "not supported by this build (alignment)";
+        case A2AV_ERR_WORKSPACE: return "workspace too small or misaligned";
+        case A2AV_ERR_CUDA: return "CUDA call failed, or a kernel gave up waiting";
+        case A2AV_ERR_DEVICE_CHECK: return "recvCounts negative or not summing to A";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

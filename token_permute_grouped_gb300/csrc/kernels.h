@@ -1,0 +1,50 @@
+// Host-side launch descriptions of the CUDA kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace a2av {
+
+// Row gather ataOut (rank-major) -> dst (expert-major).
+struct PermuteLaunch {
+    const int32_t *recvCounts;
+    int32_t W, e;
+    int32_t A;
+    int32_t H1;           // elements per row (multiple of 8)
+    const void *ataOut;   // [A, H1]
+    void *dst;            // [A, H1]
+    int32_t *status;      // device status word
+    int32_t write_status; // 1: this kernel stores the word (first kernel of a call)
+};
+
+cudaError_t launch_permute(const PermuteLaunch &p, int num_sms, cudaStream_t stream);
+
+// Persistent grouped GEMM over e routed groups (+ one shared group).
+struct GemmLaunch {
+    const int32_t *recvCounts;
+    int32_t W, e;
+    int32_t A;
+    int32_t H1, N1, bn1;  // routed: K, N, tile width
+    int32_t BS, H2, N2, bn2;  // shared: rows, K, N, tile width (BS = 0: none)
+    void *gmmY;
+    void *mmY;
+    int32_t *status;
+    int32_t write_status;
+    int32_t bf16;         // 1: bf16, 0: fp16
+    int32_t gather;       // 1: A rows gathered from ataOut (fused permute)
+    const void *ataOut;   // for gather
+    void *permuteOut;     // for gather: written from the staged A tiles (may be NULL)
+    int32_t grid;         // persistent CTAs
+    CUtensorMap tmA_routed;   // expert-major A (split path) or permuteOut store map (fused)
+    CUtensorMap tmB_routed;   // gmmWeight [e, H1, N1]
+    CUtensorMap tmA_shared;   // mmX [BS, H2]
+    CUtensorMap tmB_shared;   // mmWeight as [1, H2, N2]
+};
+
+cudaError_t launch_grouped_gemm(const GemmLaunch &p, cudaStream_t stream);
+size_t grouped_gemm_smem_bytes();
+
+}  // namespace a2av

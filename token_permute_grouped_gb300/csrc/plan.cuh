@@ -1,0 +1,94 @@
+// Scan step: offsets of the (source rank, local expert) segments, computed on
+// the device from recvCounts by one warp, into shared memory.
+//
+// "aclnnAlltoAllvGroupedMatMul", Formula: permuteOut = Permute(ataOut).
+// ataOut is rank-major (segment w*e + j holds recvCounts[w*e + j] rows);
+// permuteOut is expert-major (segment order j*W + w, arrival order kept
+// inside each expert).  "Shape variables": A is the sum of recvCounts.
+#pragma once
+
+#include <cstdint>
+
+namespace a2av {
+
+constexpr int kMaxSegments = 256;  // W * e <= 256
+constexpr int kMaxExperts = 32;    // e <= 32
+
+// Device status word bits (written into the workspace).
+constexpr int32_t kStatusBadCounts = 1;  // a negative count, or sum != A
+constexpr int32_t kStatusTimeout = 2;    // a pipeline wait gave up
+
+struct SegmentTable {
+    int32_t src[kMaxSegments];      // rank-major index -> first ataOut row
+    int32_t dst[kMaxSegments + 1];  // expert-major index -> first permuteOut row; dst[E] = A
+    int32_t tmp[kMaxSegments];      // counts in expert-major order
+};
+
+// Exclusive prefix sum of n <= 256 values in place, by one warp; returns the
+// total.  Lane l owns entries [8l, 8l + 8).
+__device__ __forceinline__ int64_t warp_exclusive_scan_256(int32_t *a, int n, int lane) {
+    int32_t v[8];
+    int64_t local = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        int i = lane * 8 + k;
+        v[k] = i < n ? a[i] : 0;
+        local += v[k];
+    }
+    int64_t inc = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int64_t t = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += t;
+    }
+    int64_t run = inc - local;
+    int64_t total = __shfl_sync(0xffffffffu, inc, 31);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        int i = lane * 8 + k;
+        if (i < n) a[i] = static_cast<int32_t>(run);
+        run += v[k];
+    }
+    __syncwarp();
+    return total;
+}
+
+// One full warp calls this.  Returns true when every count is >= 0 and the
+// counts sum to A; the table is only meaningful then.
+__device__ __forceinline__ bool build_segment_table(const int32_t *__restrict__ recvCounts, int W,
+                                                    int e, int64_t A, SegmentTable &t, int lane) {
+    const int E = W * e;
+    bool bad = false;
+    for (int i = lane; i < E; i += 32) {
+        int32_t c = recvCounts[i];
+        bad |= c < 0;
+        t.src[i] = c;
+        t.tmp[(i % e) * W + i / e] = c;  // segment (w = i / e, j = i % e) in expert-major slot
+    }
+    __syncwarp();
+    bad = __any_sync(0xffffffffu, bad);
+    int64_t total_r = warp_exclusive_scan_256(t.src, E, lane);
+    for (int i = lane; i < E; i += 32) t.dst[i] = t.tmp[i];
+    __syncwarp();
+    int64_t total_e = warp_exclusive_scan_256(t.dst, E, lane);
+    if (lane == 0) t.dst[E] = static_cast<int32_t>(total_e);
+    __syncwarp();
+    return !bad && total_r == A && total_e == A;
+}
+
+// First ataOut row feeding permuteOut row d (0 <= d < A): the last
+// expert-major segment starting at or before d (empty segments share their
+// start with the next one, so the search skips them).
+__device__ __forceinline__ int32_t source_row(const SegmentTable &t, int W, int e, int32_t d) {
+    const int E = W * e;
+    int lo = 0, hi = E;  // invariant: dst[lo] <= d < dst[hi]
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (t.dst[mid] <= d) lo = mid;
+        else hi = mid;
+    }
+    const int j = lo / W, w = lo % W;
+    return t.src[w * e + j] + (d - t.dst[lo]);
+}
+
+}  // namespace a2av

@@ -129,19 +129,24 @@ def rounded(x: np.ndarray, shape, dtype: torch.dtype) -> torch.Tensor:
     return torch.from_numpy(x).reshape(shape).to(dtype)
 
 
-def _topk_counts(scores: np.ndarray, k: int, e: int) -> np.ndarray:
-    """Hits on experts 0..e-1 of each token's top-k (scores: [tokens, E])."""
+def _topk_counts(scores: np.ndarray, k: int, lo: int, e: int) -> np.ndarray:
+    """Hits on experts lo..lo+e-1 of each token's top-k (scores: [tokens, E])."""
     top = np.argpartition(-scores, k - 1, axis=1)[:, :k]
-    return np.bincount(top.ravel(), minlength=scores.shape[1])[:e]
+    return np.bincount(top.ravel(), minlength=scores.shape[1])[lo:lo + e]
 
 
-def recv_counts(wl: Workload, seed: int = 0) -> np.ndarray:
-    """recvCounts of rank 0, int32, index w * e + j (source rank major)."""
+def recv_counts(wl: Workload, seed: int = 0, rank: int = 0) -> np.ndarray:
+    """recvCounts of one rank, int32, index w * e + j (source rank major).
+
+    Every rank sees the same routing draw; rank r owns global experts
+    r*e .. r*e + e - 1.
+    """
     W, e = wl.W, wl.e
     E = W * e
+    lo = rank * e
     rng = _rng(seed, STREAM_ROUTING)
     if wl.routing == "uniform":
-        rc = rng.multinomial(wl.A_total, [1.0 / E] * E)
+        rc = _rng(seed, STREAM_ROUTING, rank).multinomial(wl.A_total, [1.0 / E] * E)
         return rc.astype(np.int32)
 
     rc = np.zeros(E, dtype=np.int64)
@@ -150,7 +155,7 @@ def recv_counts(wl: Workload, seed: int = 0) -> np.ndarray:
         for w in range(W):
             logits = rng.standard_normal((wl.tokens_per_source, E), dtype=np.float32)
             logits += bias.astype(np.float32)
-            rc[w * e:(w + 1) * e] = _topk_counts(logits, wl.topk, e)
+            rc[w * e:(w + 1) * e] = _topk_counts(logits, wl.topk, lo, e)
     elif wl.routing == "zipf":
         # Popularity p_x proportional to rank(x)^-s over a seeded ranking of
         # the E experts; each token samples K distinct experts with
@@ -161,12 +166,12 @@ def recv_counts(wl: Workload, seed: int = 0) -> np.ndarray:
         logp = -wl.zipf_s * np.log(popularity_rank.astype(np.float64))
         for w in range(W):
             g = rng.gumbel(size=(wl.tokens_per_source, E))
-            rc[w * e:(w + 1) * e] = _topk_counts(logp[None, :] + g, wl.topk, e)
+            rc[w * e:(w + 1) * e] = _topk_counts(logp[None, :] + g, wl.topk, lo, e)
         # Force round(frac * E) empty segments: first the least popular local
         # experts for every source (whole empty GEMM groups), then single
         # (w, j) segments inside experts that keep rows.
         n_empty = int(round(wl.empty_fraction * E))
-        local_by_pop = np.argsort(-logp[:e], kind="stable")[::-1]  # least popular first
+        local_by_pop = np.argsort(-logp[lo:lo + e], kind="stable")[::-1]  # least popular first
         whole = n_empty // W
         for j in local_by_pop[:whole]:
             rc[j::e] = 0
@@ -193,9 +198,11 @@ class Inputs:
         return int(self.ataOut.shape[0])
 
 
-def make_inputs(wl: Workload, seed: int = 0) -> Inputs:
-    """All inputs of one workload, as CPU tensors (see module docstring)."""
-    rc = recv_counts(wl, seed)
+def make_inputs(wl: Workload, seed: int = 0, rank: int = 0) -> Inputs:
+    """All inputs of one workload for one rank, as CPU tensors (see module
+    docstring).  Tensor values are drawn from seed + rank."""
+    rc = recv_counts(wl, seed, rank)
+    seed = seed + rank
     A = int(rc.astype(np.int64).sum())
     dt = wl.torch_dtype
     act = normal_f32(A * wl.H1, seed, STREAM_ATAOUT)
