@@ -133,11 +133,14 @@ def test_paths_agree_bitwise(path):
 def test_device_detects_bad_counts(path, bad):
     inp = edge_inputs("ragged_multi_tile", seed=6)
     rc = inp.recvCounts.copy()
+    big = int(np.argmax(rc))
+    other = (big + 1) % len(rc)
     if bad == "sum_too_small":
-        rc[3] -= 1
+        rc[big] -= 1
     else:
-        rc[3] = -rc[3]
-        rc[4] += 2 * inp.recvCounts[3]  # keeps the sum equal to A
+        rc[big] = -rc[big]
+        rc[other] += 2 * inp.recvCounts[big]  # keeps the sum equal to A
+    assert rc.sum() == inp.recvCounts.sum() - (bad == "sum_too_small")
     bad_inp = Inputs(inp.wl, rc, inp.ataOut, inp.gmmWeight, inp.mmX, inp.mmWeight)
     gmmY, mmY, perm, (st, code) = run_gpu(bad_inp, path, sentinel=0x1234)
     assert st == 6 and code & 1

@@ -45,7 +45,7 @@ constexpr int kMmaWarp = 4;
 constexpr int kThreads = 9 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
-constexpr int kGatherLag = 2;  // cp.async groups kept in flight per producer thread
+constexpr int kGatherLag = 3;  // cp.async groups kept in flight per producer thread
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 static_assert(kGatherLag < STAGES, "gather lag must leave a free stage");
@@ -412,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const bool shared = w.g >= e;
             const int acc = tl & 1;
             if (!wait_phase(C, &C.tfull[acc], (tl >> 1) & 1, p.status)) break;
+            __syncwarp();  // lanes leave the wait independently; tcgen05.ld needs the whole warp
             tc_fence_after_sync();
             const int N = shared ? p.N2 : p.N1;
             const int bn = shared ? p.bn2 : p.bn1;
