@@ -73,7 +73,9 @@ typedef enum {
     A2AV_ERR_UNSUPPORTED = 3,  /* allowed by the operator, not by this build (alignment) */
     A2AV_ERR_WORKSPACE = 4,    /* workspace too small or misaligned */
     A2AV_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
-    A2AV_ERR_DEVICE_CHECK = 6  /* the device found inconsistent recvCounts */
+    A2AV_ERR_DEVICE_CHECK = 6, /* the device found inconsistent recvCounts */
+    A2AV_ERR_SCRATCH_LIMIT = 7 /* a2av_gmm_run_static_scratch: the problem needs more
+                                  scratch than the library's static array holds */
 } a2av_status;
 
 typedef enum { A2AV_BF16 = 0, A2AV_FP16 = 1 } a2av_dtype;
@@ -129,6 +131,49 @@ a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut,
  */
 a2av_status a2av_gmm_read_device_status(const void *workspace, a2av_stream_t stream,
                                         int32_t *code);
+
+/*
+ * Same computation as a2av_gmm_run, for callers that cannot allocate device
+ * memory.  (The operator page has no counterpart: this entry point exists
+ * only in this library.)
+ *
+ * Who needs it: code that is handed only its inputs and outputs and has no
+ * way to obtain a workspace, for example an operator plugged into a
+ * framework or runtime that owns the whole device memory pool, or a
+ * latency-critical loop that must not call cudaMalloc, which can block the
+ * host and synchronise the device.
+ *
+ * Instead of a caller-provided workspace it uses one scratch array that the
+ * library defines in device memory: A2AV_STATIC_SCRATCH_BYTES bytes, held on
+ * every GPU that loads the library until the process exits.  The fused
+ * path needs only its 256-byte status area; the split path without
+ * permuteOut also stages A * H1 * 2 bytes there.  A descriptor whose
+ * workspace (as a2av_gmm_workspace_size reports it) exceeds the array is
+ * rejected with A2AV_ERR_SCRATCH_LIMIT before anything is enqueued.  This
+ * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ * the array's device address once; make that first call before any stream
+ * capture begins.
+ *
+ * Sharing: every call on a device uses the same array, and the array keeps
+ * the previous call's contents.  The kernels overwrite every scratch byte
+ * they later read (the status word is stored afresh at the start of each
+ * call), so nothing needs clearing between calls.  Two calls that may run at
+ * the same time on the GPU (different streams without ordering between
+ * them) race on the array: order them on one stream or with events.  The
+ * device status word of this call cannot be read back; on inconsistent
+ * recvCounts the outputs are left unwritten, as with a2av_gmm_run.
+ *
+ * Arguments and other return codes are those of a2av_gmm_run.
+ */
+#define A2AV_STATIC_SCRATCH_BYTES ((size_t)256 + ((size_t)8 << 20))
+a2av_status a2av_gmm_run_static_scratch(const a2av_gmm_desc *desc, const void *ataOut,
+                                        const int32_t *recvCounts, const void *gmmWeight,
+                                        const void *mmX, const void *mmWeight,
+                                        void *permuteOut, void *gmmY, void *mmY,
+                                        a2av_stream_t stream);
 
 /* A static, human-readable name for a status code. */
 const char *a2av_gmm_status_string(a2av_status status);

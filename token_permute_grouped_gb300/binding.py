@@ -18,13 +18,15 @@ from . import build as _build
 
 A2AV_OK = 0
 STATUS_NAMES = {0: "A2AV_OK", 1: "A2AV_ERR_NULLPTR", 2: "A2AV_ERR_INVALID", 3: "A2AV_ERR_UNSUPPORTED",
-                4: "A2AV_ERR_WORKSPACE", 5: "A2AV_ERR_CUDA", 6: "A2AV_ERR_DEVICE_CHECK"}
+                4: "A2AV_ERR_WORKSPACE", 5: "A2AV_ERR_CUDA", 6: "A2AV_ERR_DEVICE_CHECK",
+                7: "A2AV_ERR_SCRATCH_LIMIT"}
+STATIC_SCRATCH_BYTES = 256 + (8 << 20)  # A2AV_STATIC_SCRATCH_BYTES
 DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 PATHS = {"default": 0, "fused": 1, "split": 2}
 
 # Every symbol include/a2av_gmm.h declares.
 EXPORTS = ("a2av_gmm_workspace_size", "a2av_gmm_run", "a2av_gmm_read_device_status",
-           "a2av_gmm_status_string", "a2av_gmm_launch_count")
+           "a2av_gmm_status_string", "a2av_gmm_launch_count", "a2av_gmm_run_static_scratch")
 
 
 class A2avError(RuntimeError):
@@ -66,6 +68,8 @@ def load():
         L.a2av_gmm_status_string.restype = ctypes.c_char_p
         L.a2av_gmm_launch_count.argtypes = [ctypes.POINTER(Desc)]
         L.a2av_gmm_launch_count.restype = i32
+        L.a2av_gmm_run_static_scratch.argtypes = [ctypes.POINTER(Desc), p, p, p, p, p, p, p, p, p]
+        L.a2av_gmm_run_static_scratch.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -104,6 +108,17 @@ def a2av_gmm_run(desc: Desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permu
                              _ptr(workspace), workspace.numel(), ctypes.c_void_p(s.cuda_stream))
     if st != A2AV_OK:
         raise A2avError(st, "a2av_gmm_run")
+
+
+def a2av_gmm_run_static_scratch(desc: Desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permuteOut, gmmY,
+                                mmY, stream=None) -> int:
+    """Phase 2 without a workspace, for callers that cannot allocate device
+    memory: the library's own static device scratch array stands in for it.
+    Returns the status code (0 = enqueued)."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(load().a2av_gmm_run_static_scratch(
+        ctypes.byref(desc), _ptr(ataOut), _ptr(recvCounts), _ptr(gmmWeight), _ptr(mmX), _ptr(mmWeight),
+        _ptr(permuteOut), _ptr(gmmY), _ptr(mmY), ctypes.c_void_p(s.cuda_stream)))
 
 
 def a2av_gmm_read_device_status(workspace: torch.Tensor, stream=None) -> tuple[int, int]:

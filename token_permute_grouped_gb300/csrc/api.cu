@@ -14,6 +14,10 @@
 #include "kernels.h"
 #include "plan.cuh"
 
+// Scratch for a2av_gmm_run_static_scratch: callers that cannot allocate get
+// this array instead of a workspace.  One per device, alive until exit.
+static __device__ __align__(256) uint8_t g_static_scratch[A2AV_STATIC_SCRATCH_BYTES];
+
 namespace {
 
 constexpr size_t kStatusBytes = 256;  // status word, padded to keep what follows aligned
@@ -119,6 +123,23 @@ int sm_count() {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Device address of g_static_scratch on the current device, looked up once
+// per device.  In host code the symbol name is only a host-side stand-in,
+// never a device address, so it must go through cudaGetSymbolAddress.
+void *static_scratch_address() {
+    static void *addr[kMaxDevices] = {nullptr};
+    static std::mutex lock;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> guard(lock);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -218,6 +239,20 @@ a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const in
     return A2AV_OK;
 }
 
+a2av_status a2av_gmm_run_static_scratch(const a2av_gmm_desc *desc, const void *ataOut,
+                                        const int32_t *recvCounts, const void *gmmWeight, const void *mmX,
+                                        const void *mmWeight, void *permuteOut, void *gmmY, void *mmY,
+                                        a2av_stream_t stream) {
+    size_t need = 0;
+    const a2av_status s = a2av_gmm_workspace_size(desc, &need);
+    if (s != A2AV_OK) return s;
+    if (need > A2AV_STATIC_SCRATCH_BYTES) return A2AV_ERR_SCRATCH_LIMIT;
+    void *scratch = static_scratch_address();
+    if (!scratch) return A2AV_ERR_CUDA;
+    return a2av_gmm_run(desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permuteOut, gmmY, mmY, scratch,
+                        A2AV_STATIC_SCRATCH_BYTES, stream);
+}
+
 a2av_status a2av_gmm_read_device_status(const void *workspace, a2av_stream_t stream, int32_t *code) {
     if (!workspace) return A2AV_ERR_NULLPTR;
     int32_t word = 0;
@@ -238,6 +273,7 @@ const char *a2av_gmm_status_string(a2av_status status) {
         case A2AV_ERR_WORKSPACE: return "workspace too small or misaligned";
         case A2AV_ERR_CUDA: return "CUDA call failed, or a kernel gave up waiting";
         case A2AV_ERR_DEVICE_CHECK: return "recvCounts negative or not summing to A";
+        case A2AV_ERR_SCRATCH_LIMIT: return "needs more scratch than the static scratch array holds";
     }
     return "unknown status";
 }
