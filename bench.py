@@ -78,7 +78,7 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload, permute_out, path):
+def profiled_traffic(workload, permute_out, path, tiles):
     """DRAM bytes per launch of the GEMM kernel from a committed ncu summary,
     only while the kernel sources are unchanged since the capture."""
     for f in glob.glob(os.path.join(ROOT, "profiles", "*.json")):
@@ -88,7 +88,8 @@ def profiled_traffic(workload, permute_out, path):
         except (OSError, ValueError):
             continue
         if (s.get("workload") == workload and s.get("permute_out") == permute_out
-                and s.get("path") == path and s.get("source_hash") == source_hash()):
+                and s.get("path") == path and s.get("tiles") == tiles
+                and s.get("source_hash") == source_hash()):
             return s.get("dram_bytes_per_launch")
     return None
 
@@ -218,7 +219,7 @@ def run_gpu(args):
     A = inp.A
     dt = wl.torch_dtype
     plan = binding.Plan(wl.W, wl.e, A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, dt,
-                        want_permute_out=args.permute_out, path=args.path, device=dev)
+                        want_permute_out=args.permute_out, path=args.path, device=dev, tiles=args.tiles)
     launches_per_call = binding.a2av_gmm_launch_count(plan.desc)
 
     # Input replicas, rotated so that no step finds its inputs in L2.
@@ -319,7 +320,7 @@ def run_gpu(args):
         "data": "synthetic (seeded routing and N(0,1) tensors; no dataset)",
         "config": {
             "workload": wl.name, "W": wl.W, "e": wl.e, "A": A, "H1": wl.H1, "N1": wl.N1,
-            "BS": wl.BS, "H2": wl.H2, "N2": wl.N2, "path": args.path,
+            "BS": wl.BS, "H2": wl.H2, "N2": wl.N2, "path": args.path, "tiles": args.tiles,
             "permute_out": bool(args.permute_out), "accumulate": "fp32",
             "us_per_call_median": round(per_call_us, 2),
             "us_per_call_min": round(min(per_call_ms) * 1e3, 2),
@@ -336,7 +337,7 @@ def run_gpu(args):
             "peak": peak_tf,
             "unit": "TFLOP/s",
             "frac": round(achieved / peak_tf, 4),
-            "traffic": profiled_traffic(wl.name, bool(args.permute_out), args.path),
+            "traffic": profiled_traffic(wl.name, bool(args.permute_out), args.path, args.tiles),
             "kernel": "grouped_gemm_kernel",
             "peak_source": f"{pk_kind} bf16 dense burst (MEASURED_PEAKS.json bf16_tflops)" if pk_kind == "measured"
             else "fallback 1.9 PFLOP/s",
@@ -437,6 +438,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--permute-out", action="store_true")
     ap.add_argument("--path", default="default", choices=["default", "fused", "split"])
+    ap.add_argument("--tiles", default="default", choices=["default", "single", "pair"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -87,6 +87,13 @@ typedef enum {
     A2AV_PATH_SPLIT = 2        /* a permute kernel first, then the grouped GEMM */
 } a2av_path;
 
+/* GEMM tile shape.  All give bitwise-identical outputs. */
+typedef enum {
+    A2AV_TILES_DEFAULT = 0,    /* the faster shape for this build */
+    A2AV_TILES_SINGLE = 1,     /* 128-row tiles, one CTA each */
+    A2AV_TILES_PAIR = 2        /* 256-row tiles on a cluster of two CTAs */
+} a2av_tiles;
+
 typedef struct {
     int32_t W, e;              /* ranks, local experts */
     int64_t A, H1, N1;         /* routed experts */
@@ -94,7 +101,7 @@ typedef struct {
     int32_t dtype;             /* a2av_dtype */
     int32_t want_permute_out;  /* nonzero: permuteOut is written */
     int32_t path;              /* a2av_path */
-    int32_t reserved;          /* set to 0 */
+    int32_t tiles;             /* a2av_tiles */
 } a2av_gmm_desc;
 
 /*

@@ -11,7 +11,7 @@ from token_permute_grouped_gb300 import binding
 TOL = 2e-2  # |gpu - ref| <= TOL * max(1, |ref|), against the float64 oracle
 
 
-def run_gpu(inp, path="default", want_perm=True, guard_rows=0, sentinel=None):
+def run_gpu(inp, path="default", want_perm=True, guard_rows=0, sentinel=None, tiles="default"):
     """Run the hot path on cuda:0; returns CPU tensors (gmmY, mmY, permuteOut, status).
 
     With guard_rows, each output gets extra rows after its end, pre-filled with
@@ -21,7 +21,7 @@ def run_gpu(inp, path="default", want_perm=True, guard_rows=0, sentinel=None):
     dev = torch.device("cuda:0")
     dt = wl.torch_dtype
     plan = binding.Plan(wl.W, wl.e, inp.A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, dt,
-                        want_permute_out=want_perm, path=path, device=dev)
+                        want_permute_out=want_perm, path=path, device=dev, tiles=tiles)
 
     def out(rows, cols):
         t = torch.empty(rows + guard_rows, cols, dtype=dt, device=dev)

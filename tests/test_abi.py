@@ -47,7 +47,7 @@ def ws(**kw):
     d = binding.make_desc(**{k: base[k] for k in ("W", "e", "A", "H1", "N1", "BS", "H2", "N2")},
                           dtype=kw.get("dtype", torch.bfloat16), want_permute_out=kw.get("perm", False),
                           path=kw.get("path", "default"))
-    for f in ("dtype", "reserved", "path"):
+    for f in ("dtype", "tiles", "path"):
         if f"raw_{f}" in kw:
             setattr(d, f, kw[f"raw_{f}"])
     n = ctypes.c_size_t(0)
@@ -72,7 +72,8 @@ def ws(**kw):
     ({"A": -1}, 2),
     ({"A": 2**31}, 2),
     ({"raw_dtype": 7}, 2),
-    ({"raw_reserved": 1}, 2),
+    ({"raw_tiles": 3}, 2),
+    ({"raw_tiles": 2}, 0),
     ({"raw_path": 9}, 2),
     ({"H1": 4100}, 3),                  # rows must start 16-byte aligned
     ({"N2": 1020}, 3),
@@ -83,8 +84,8 @@ def test_phase1_validation(lib, kw, status):
 
 
 def test_workspace_sizes(lib):
-    assert ws()[1] == 256
     assert ws(path="fused")[1] == 256
+    assert ws(path="default", A=100, H1=64)[1] == 256 + 100 * 64 * 2  # default is the split path
     st, n = ws(path="split", A=1000, H1=512)
     assert st == 0 and n == 256 + 1000 * 512 * 2
     assert ws(path="split", A=1000, H1=512, perm=True)[1] == 256  # stages in permuteOut
@@ -94,6 +95,8 @@ def test_workspace_sizes(lib):
 def test_launch_counts(lib):
     d = binding.make_desc(8, 4, 1000, 512, 256, path="fused")
     assert binding.a2av_gmm_launch_count(d) == 1
+    d = binding.make_desc(8, 4, 1000, 512, 256)
+    assert binding.a2av_gmm_launch_count(d) == 2
     d = binding.make_desc(8, 4, 1000, 512, 256, path="split")
     assert binding.a2av_gmm_launch_count(d) == 2
     d = binding.make_desc(8, 4, 0, 512, 256, path="split")

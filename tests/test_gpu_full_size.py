@@ -30,6 +30,13 @@ def test_full_size_workload(orc, name):
     inp = make_inputs(wl, seed=0)
     gmmY, mmY, _, (st, code) = run_gpu(inp, "default", want_perm=False)
     assert st == 0, code
+    # Every path and tile shape gives the same bits as the default one.
+    for path, tiles in (("split", "single"), ("fused", "pair")):
+        y2, m2, _, (st, code) = run_gpu(inp, path, want_perm=False, tiles=tiles)
+        assert st == 0, code
+        assert torch.equal(gmmY.view(torch.int16), y2.view(torch.int16)), (path, tiles)
+        if mmY is not None:
+            assert torch.equal(mmY.view(torch.int16), m2.view(torch.int16)), (path, tiles)
     gmmY2, mmY2, perm, (st, code) = run_gpu(inp, "default", want_perm=True)
     assert st == 0, code
     # Asking for permuteOut must not change the products.

@@ -16,6 +16,7 @@ from token_permute_grouped_gb300.workloads import WORKLOADS, SMALL, Inputs, cust
 pytestmark = pytest.mark.gpu
 
 PATHS = ["fused", "split"]
+TILES = ["single", "pair"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -58,11 +59,13 @@ def edge_inputs(name, seed=1):
     return custom_inputs(W, e, H1, N1, rc, dt, BS, H2, N2, seed=seed)
 
 
+@pytest.mark.parametrize("tiles", TILES)
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("name", sorted(EDGE))
-def test_edge_cases(orc, name, path):
+def test_edge_cases(orc, name, path, tiles):
     inp = edge_inputs(name)
-    gmmY, mmY, perm, (st, code) = run_gpu(inp, path, want_perm=True, guard_rows=3, sentinel=0x7FC1)
+    gmmY, mmY, perm, (st, code) = run_gpu(inp, path, want_perm=True, guard_rows=3, sentinel=0x7FC1,
+                                          tiles=tiles)
     assert st == 0, code
     check_full(orc, inp, gmmY, mmY, perm)
     # Nothing written past the ends (guard rows keep the sentinel).
@@ -81,15 +84,16 @@ def _integer_inputs(W, e, H1, N1, rc, BS, H2, N2, dtype, seed):
                   mk(BS, H2) if BS else None, mk(H2, N2) if BS else None)
 
 
+@pytest.mark.parametrize("tiles", TILES)
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-def test_integer_inputs_bit_exact(orc, path, dtype):
+def test_integer_inputs_bit_exact(orc, path, dtype, tiles):
     # |x|, |w| <= 4 and K <= 1024: every partial sum is an integer below 2^24,
     # exact in the fp32 accumulator in any order, so the output must be the
     # one nearest-even rounding of the exact (oracle) value.
     rc = [50, 0, 130, 7, 0, 260, 1, 90]
     inp = _integer_inputs(2, 4, 1024, 320, rc, 200, 512, 136, dtype, 3)
-    gmmY, mmY, perm, (st, _) = run_gpu(inp, path)
+    gmmY, mmY, perm, (st, _) = run_gpu(inp, path, tiles=tiles)
     assert st == 0
     ref_perm, ref_y, ref_mm = orc.run(2, 4, inp.recvCounts, inp.ataOut, inp.gmmWeight, inp.mmX, inp.mmWeight)
     assert_bits_equal(perm, ref_perm, "permuteOut")
@@ -110,27 +114,31 @@ def test_identity_weight_reproduces_permute_out(orc, path):
     assert_bits_equal(perm, orc.permute(W, e, inp.recvCounts, inp.ataOut), "permuteOut")
 
 
+@pytest.mark.parametrize("tiles", TILES)
 @pytest.mark.parametrize("path", PATHS)
-def test_deterministic(path):
+def test_deterministic(path, tiles):
     inp = edge_inputs("ragged_multi_tile", seed=4)
-    a = run_gpu(inp, path)
-    b = run_gpu(inp, path)
+    a = run_gpu(inp, path, tiles=tiles)
+    b = run_gpu(inp, path, tiles=tiles)
     for x, y in zip(a[:3], b[:3]):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
 
 
+@pytest.mark.parametrize("tiles", TILES)
 @pytest.mark.parametrize("path", PATHS)
-def test_paths_agree_bitwise(path):
+def test_paths_agree_bitwise(path, tiles):
+    # Same fp32 accumulation order on every path and tile shape.
     inp = edge_inputs("fp16_mixed", seed=5)
-    ref = run_gpu(inp, "split")
-    got = run_gpu(inp, path)
+    ref = run_gpu(inp, "split", tiles="single")
+    got = run_gpu(inp, path, tiles=tiles)
     for x, y in zip(ref[:3], got[:3]):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
 
 
+@pytest.mark.parametrize("tiles", TILES)
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("bad", ["sum_too_small", "negative"])
-def test_device_detects_bad_counts(path, bad):
+def test_device_detects_bad_counts(path, bad, tiles):
     inp = edge_inputs("ragged_multi_tile", seed=6)
     rc = inp.recvCounts.copy()
     big = int(np.argmax(rc))
@@ -142,7 +150,7 @@ def test_device_detects_bad_counts(path, bad):
         rc[other] += 2 * inp.recvCounts[big]  # keeps the sum equal to A
     assert rc.sum() == inp.recvCounts.sum() - (bad == "sum_too_small")
     bad_inp = Inputs(inp.wl, rc, inp.ataOut, inp.gmmWeight, inp.mmX, inp.mmWeight)
-    gmmY, mmY, perm, (st, code) = run_gpu(bad_inp, path, sentinel=0x1234)
+    gmmY, mmY, perm, (st, code) = run_gpu(bad_inp, path, sentinel=0x1234, tiles=tiles)
     assert st == 6 and code & 1
     # Nothing written at all, shared expert included.
     for t in (gmmY, mmY, perm):

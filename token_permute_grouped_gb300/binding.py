@@ -23,6 +23,7 @@ STATUS_NAMES = {0: "A2AV_OK", 1: "A2AV_ERR_NULLPTR", 2: "A2AV_ERR_INVALID", 3: "
 STATIC_SCRATCH_BYTES = 256 + (8 << 20)  # A2AV_STATIC_SCRATCH_BYTES
 DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 PATHS = {"default": 0, "fused": 1, "split": 2}
+TILES = {"default": 0, "single": 1, "pair": 2}
 
 # Every symbol include/a2av_gmm.h declares.
 EXPORTS = ("a2av_gmm_workspace_size", "a2av_gmm_run", "a2av_gmm_read_device_status",
@@ -40,7 +41,7 @@ class Desc(ctypes.Structure):
                 ("A", ctypes.c_int64), ("H1", ctypes.c_int64), ("N1", ctypes.c_int64),
                 ("BS", ctypes.c_int64), ("H2", ctypes.c_int64), ("N2", ctypes.c_int64),
                 ("dtype", ctypes.c_int32), ("want_permute_out", ctypes.c_int32),
-                ("path", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("path", ctypes.c_int32), ("tiles", ctypes.c_int32)]
 
 
 _lib = None
@@ -75,8 +76,9 @@ def load():
 
 
 def make_desc(W, e, A, H1, N1, BS=0, H2=0, N2=0, dtype=torch.bfloat16, want_permute_out=False,
-              path="default") -> Desc:
-    return Desc(W, e, A, H1, N1, BS, H2, N2, DTYPES[dtype], int(bool(want_permute_out)), PATHS[path], 0)
+              path="default", tiles="default") -> Desc:
+    return Desc(W, e, A, H1, N1, BS, H2, N2, DTYPES[dtype], int(bool(want_permute_out)), PATHS[path],
+                TILES[tiles])
 
 
 def a2av_gmm_workspace_size(desc: Desc) -> int:
@@ -144,8 +146,8 @@ class Plan:
     """Descriptor + workspace for one shape, reusable across calls."""
 
     def __init__(self, W, e, A, H1, N1, BS=0, H2=0, N2=0, dtype=torch.bfloat16,
-                 want_permute_out=False, path="default", device=None):
-        self.desc = make_desc(W, e, A, H1, N1, BS, H2, N2, dtype, want_permute_out, path)
+                 want_permute_out=False, path="default", device=None, tiles="default"):
+        self.desc = make_desc(W, e, A, H1, N1, BS, H2, N2, dtype, want_permute_out, path, tiles)
         self.dtype = dtype
         self.device = torch.device(device) if device is not None else torch.device("cuda")
         self.workspace = torch.empty(a2av_gmm_workspace_size(self.desc), dtype=torch.uint8, device=self.device)
@@ -177,7 +179,7 @@ class Plan:
 
 
 def a2av_gmm(ataOut, recvCounts, gmmWeight, mmX=None, mmWeight=None, return_permute=False,
-             W=None, path="default"):
+             W=None, path="default", tiles="default"):
     """permuteOut = Permute(ataOut); gmmY = permuteOut x gmmWeight; mmY = mmX x mmWeight.
 
     Returns (gmmY, mmY or None, permuteOut or None).  W defaults to
@@ -191,5 +193,5 @@ def a2av_gmm(ataOut, recvCounts, gmmWeight, mmX=None, mmWeight=None, return_perm
         BS, H2 = mmX.shape
         N2 = mmWeight.shape[1]
     plan = Plan(W, e, ataOut.shape[0], H1, N1, BS, H2, N2, gmmWeight.dtype, return_permute, path,
-                device=gmmWeight.device)
+                device=gmmWeight.device, tiles=tiles)
     return plan.run(ataOut, recvCounts, gmmWeight, mmX, mmWeight)

@@ -38,13 +38,27 @@ a2av_status validate(const a2av_gmm_desc *d) {
     }
     if (d->dtype != A2AV_BF16 && d->dtype != A2AV_FP16) return A2AV_ERR_INVALID;
     if (d->path < A2AV_PATH_DEFAULT || d->path > A2AV_PATH_SPLIT) return A2AV_ERR_INVALID;
-    if (d->reserved != 0) return A2AV_ERR_INVALID;
+    if (d->tiles < A2AV_TILES_DEFAULT || d->tiles > A2AV_TILES_PAIR) return A2AV_ERR_INVALID;
     if (!mult8(d->H1) || !mult8(d->N1)) return A2AV_ERR_UNSUPPORTED;
     if (d->BS > 0 && (!mult8(d->H2) || !mult8(d->N2))) return A2AV_ERR_UNSUPPORTED;
     return A2AV_OK;
 }
 
-bool use_split(const a2av_gmm_desc *d) { return d->path == A2AV_PATH_SPLIT; }
+// Defaults: the combination measured fastest on GB300 for the benchmark
+// workloads (permute kernel + TMA-fed grouped GEMM on CTA pairs).
+bool use_split(const a2av_gmm_desc *d) { return d->path != A2AV_PATH_FUSED; }
+
+bool use_pair(const a2av_gmm_desc *d) { return d->tiles != A2AV_TILES_SINGLE; }
+
+// Clusters (pair) or CTAs (single) of the GEMM that fit on the device at once.
+int coresident_units(bool pair) {
+    static int cache[kMaxDevices][2] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int &c = cache[dev][pair ? 1 : 0];
+    if (c == 0) c = a2av::grouped_gemm_max_coresident(pair ? 1 : 0);
+    return c;
+}
 
 // Bytes of the expert-major staging buffer the split path needs when the
 // caller does not ask for permuteOut.
@@ -81,13 +95,15 @@ CUtensorMapDataType tmap_type(int32_t dtype) {
     return dtype == A2AV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
-// [rows, cols] row-major; box = 64 columns x 128 rows, 128-byte swizzle.
-bool make_rows_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int32_t dtype) {
+// [rows, cols] row-major; box = 64 columns x box_rows rows, 128-byte swizzle.
+// box_rows = 128 for tile loads, 1 for row gathers (tile::gather4).
+bool make_rows_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int32_t dtype,
+                   uint32_t box_rows = kBM) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
-    cuuint32_t box[2] = {64, kBM};
+    cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, tmap_type(dtype), 2, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -224,17 +240,28 @@ a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const in
             if (a2av::launch_permute(pl, sms, stream) != cudaSuccess) return A2AV_ERR_CUDA;
             permute_ran = true;
             if (!make_rows_map(&g.tmA_routed, dst, d.A, d.H1, d.dtype)) return A2AV_ERR_CUDA;
-        } else if (perm_out) {
-            if (!make_rows_map(&g.tmA_routed, perm_out, d.A, d.H1, d.dtype)) return A2AV_ERR_CUDA;
+        } else {
+            // Maps over ataOut in arrival order: a one-row box for row gathers,
+            // and 8 .. 128-row boxes for runs of rows from one segment.
+            if (!make_rows_map(&g.tmA_routed, ataOut, d.A, d.H1, d.dtype, 1)) return A2AV_ERR_CUDA;
+            for (int k = 0; k < 5; ++k)
+                if (!make_rows_map(&g.tmA_box[k], ataOut, d.A, d.H1, d.dtype, 8u << k)) return A2AV_ERR_CUDA;
         }
     }
     g.write_status = permute_ran ? 0 : 1;
 
-    // Persistent grid: at most one CTA per SM, never more CTAs than tiles.
+    // Persistent grid: as many CTAs (pair: clusters of two) as fit on the
+    // device at once, never more than there can be tiles.
+    const bool pair = use_pair(&d);
+    const int64_t tile_m = pair ? 2 * kBM : kBM;
     const int64_t tn1 = (d.N1 + g.bn1 - 1) / g.bn1;
-    int64_t tiles = ((d.A + kBM - 1) / kBM + d.e) * tn1;
-    if (has_shared) tiles += ((d.BS + kBM - 1) / kBM) * ((d.N2 + g.bn2 - 1) / g.bn2);
-    g.grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(sms, tiles)));
+    int64_t tiles = ((d.A + tile_m - 1) / tile_m + d.e) * tn1;
+    if (has_shared) tiles += ((d.BS + tile_m - 1) / tile_m) * ((d.N2 + g.bn2 - 1) / g.bn2);
+    int units = coresident_units(pair);
+    if (units <= 0) units = pair ? sms / 2 : sms;
+    g.pair = pair ? 1 : 0;
+    const int64_t n_units = std::max<int64_t>(1, std::min<int64_t>(units, tiles));
+    g.grid = static_cast<int32_t>(n_units * (pair ? 2 : 1));
     if (a2av::launch_grouped_gemm(g, stream) != cudaSuccess) return A2AV_ERR_CUDA;
     return A2AV_OK;
 }

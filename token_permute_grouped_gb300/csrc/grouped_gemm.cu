@@ -6,21 +6,33 @@
 // fusion with the MatMul for shared experts"); here the shared product is one
 // more group in the same persistent launch.
 //
-// Tiles: 128 rows x bn columns (bn <= 256, chosen per group on the host),
-// K in steps of 64 16-bit elements (one 128-byte swizzle row).  Per CTA:
-//   warps 0-3  producers.  Split path: one thread issues TMA loads of the
-//              expert-major A tile and the weight tile.  Fused path: the 128
-//              threads gather A rows straight from ataOut with cp.async
-//              (the permute happens in the operand load), written in the
-//              128-byte-swizzled layout the tensor core reads; weights by TMA.
-//              When permuteOut is wanted, each gathered A tile of the first
-//              column tile is also stored to permuteOut by a TMA store.
-//   warp 4     one thread issues tcgen05.mma (M=128, N=bn, K=16) into TMEM.
+// Tiles: TILE_M rows x bn columns (bn <= 256, chosen per group on the host),
+// K in steps of 64 16-bit elements (one 128-byte swizzle row).  Two tile
+// shapes share the code:
+//   single   one CTA computes a 128-row tile (tcgen05 cta_group::1);
+//   pair     a cluster of two CTAs computes a 256-row tile with one
+//            cta_group::2 MMA: each CTA stages its own 128 A rows and half of
+//            the bn weight columns, so each CTA moves half the weight bytes
+//            per FLOP.  The even CTA issues the MMAs; both hold half of the
+//            accumulator rows in their own TMEM.
+// Per CTA:
+//   warp 0     producer.  Split path: one thread issues TMA loads of the
+//              expert-major A rows and the weight columns.  Fused path: the
+//              permute happens in the operand load: the CTA's 128 A rows are
+//              read from their arrival places in ataOut, as one TMA box per
+//              aligned block of rows that lies in one (source, expert)
+//              segment and a TMA row gather (tile::gather4) for each 4-row
+//              group that straddles a segment boundary, all landing in the
+//              128-byte-swizzled layout the tensor core reads.
+//   warps 1-3  fused path with permuteOut wanted: copy the rows of every
+//              first-column tile from ataOut to permuteOut, independently of
+//              the shared-memory pipeline.
+//   warp 4     one thread issues tcgen05.mma (K=16 each) into TMEM.
 //   warps 5-8  epilogue: TMEM -> registers -> bf16/fp16 (nearest even) ->
 //              global, rows past the group's end masked.
-// TMEM holds two 128 x 256 fp32 accumulators so the epilogue of one tile
-// overlaps the main loop of the next.  Every wait is bounded: on timeout the
-// CTA records kStatusTimeout in the status word and winds down.
+// TMEM holds two 128-lane x 256-column fp32 accumulators so the epilogue of
+// one tile overlaps the main loop of the next.  Every wait is bounded: on
+// timeout the CTA records kStatusTimeout in the status word and winds down.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -32,23 +44,25 @@ namespace a2av {
 
 namespace {
 
-constexpr int BM = 128;
+constexpr int BM = 128;  // rows per CTA
 constexpr int BK = 64;
-constexpr int BN_MAX = 256;
-constexpr int STAGES = 4;
-constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;                  // 16 KB
-constexpr uint32_t B_ATOM_BYTES = BK * 64 * 2;                   // 64 K-rows x 64 N: 8 KB
-constexpr uint32_t B_STAGE_BYTES = (BN_MAX / 64) * B_ATOM_BYTES;  // 32 KB
+constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
+constexpr uint32_t B_ATOM_BYTES = BK * 64 * 2;   // 64 K-rows x 64 N: 8 KB
 constexpr int kProducerWarps = 4;
-constexpr int kProducerThreads = kProducerWarps * 32;
 constexpr int kMmaWarp = 4;
 constexpr int kThreads = 9 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
-constexpr int kGatherLag = 3;  // cp.async groups kept in flight per producer thread
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-static_assert(kGatherLag < STAGES, "gather lag must leave a free stage");
+template <bool PAIR>
+struct Shape {
+    static constexpr int kCtas = PAIR ? 2 : 1;
+    static constexpr int TILE_M = BM * kCtas;
+    // Weight columns one CTA stages: bn (<= 256) or bn / 2 (<= 128).
+    static constexpr uint32_t B_STAGE_BYTES = (PAIR ? 2 : 4) * B_ATOM_BYTES;
+    static constexpr int STAGES = PAIR ? 6 : 4;
+};
 
 struct GroupInfo {
     int32_t row0;        // first A-operand row (routed: expert-major row)
@@ -57,29 +71,32 @@ struct GroupInfo {
     int32_t tile_start;  // first linear tile of this group
 };
 
+template <int STAGES>
 struct Control {
-    uint64_t full[STAGES];     // A and B of a stage are in shared memory
+    uint64_t full[STAGES];     // A and B of a stage landed (pair: in both CTAs; used in the even CTA)
     uint64_t empty[STAGES];    // the MMAs reading a stage have completed
-    uint64_t written[STAGES];  // fused path: every producer thread's rows landed
     uint64_t tfull[2];         // accumulator ready for the epilogue
-    uint64_t tempty[2];        // epilogue drained the accumulator
+    uint64_t tempty[2];        // epilogue drained the accumulator (pair: both CTAs, used in the even CTA)
     uint32_t tmem_base;
     int32_t abort;
     int32_t ngroups;
     int32_t total_tiles;
-    int32_t store_x[STAGES];   // fused path: permuteOut tile coordinates per stage
-    int32_t store_y[STAGES];
     GroupInfo g[kMaxExperts + 2];  // routed, shared, sentinel
     SegmentTable seg;
 };
 
-constexpr size_t kSmemBytes = 1024 + STAGES * (A_STAGE_BYTES + B_STAGE_BYTES) + sizeof(Control);
+template <bool PAIR>
+constexpr size_t smem_bytes() {
+    return 1024 + Shape<PAIR>::STAGES * (A_STAGE_BYTES + Shape<PAIR>::B_STAGE_BYTES) +
+           sizeof(Control<Shape<PAIR>::STAGES>);
+}
 
 struct Tile {
     int g, m, n;
 };
 
-__device__ __forceinline__ Tile decode_tile(const Control &c, int t) {
+template <typename C>
+__device__ __forceinline__ Tile decode_tile(const C &c, int t) {
     int g = 0;
     while (t >= c.g[g + 1].tile_start) ++g;
     const int local = t - c.g[g].tile_start;
@@ -88,42 +105,166 @@ __device__ __forceinline__ Tile decode_tile(const Control &c, int t) {
 }
 
 // Bounded wait on an mbarrier phase.  False: gave up (or another role did);
-// the abort flag and the status word are set.
-__device__ __noinline__ bool wait_phase(Control &c, uint64_t *bar, uint32_t parity, int32_t *status) {
+// the abort flag and the status word are set.  CLUSTER: acquire at cluster
+// scope (the arrivals come from the peer CTA too).
+template <bool CLUSTER = false>
+__device__ __noinline__ bool wait_phase(int32_t *abort_flag, uint64_t *bar, uint32_t parity, int32_t *status) {
     const uint32_t b = smem_u32(bar);
-    if (mbar_try_wait(b, parity)) return true;
+    auto try_once = [&]() -> bool {
+        if constexpr (CLUSTER) {
+            uint32_t ok;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(ok)
+                : "r"(b), "r"(parity)
+                : "memory");
+            return ok != 0;
+        } else {
+            return mbar_try_wait(b, parity);
+        }
+    };
+    if (try_once()) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(b, parity)) return true;
-        if (*reinterpret_cast<volatile int32_t *>(&c.abort)) return false;
+            if (try_once()) return true;
+        if (*reinterpret_cast<volatile int32_t *>(abort_flag)) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
-            *reinterpret_cast<volatile int32_t *>(&c.abort) = 1;
+            *reinterpret_cast<volatile int32_t *>(abort_flag) = 1;
             atomicOr(status, kStatusTimeout);
             return false;
         }
     }
 }
 
-__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
+// ---- cluster (CTA pair) helpers
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
 }
 
-__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(src), "r"(x), "r"(y)
-                 : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
 }
 
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// ---- TMA loads; PAIR: the barrier may live in the peer CTA (cta_group::2).
+
+template <bool PAIR>
+__device__ __forceinline__ void tma_2d(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y) {
+    if constexpr (PAIR) {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+            " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y)
+            : "memory");
+    } else {
+        tma_load_2d(dst, tmap, bar, x, y);
+    }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tma_3d(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y,
+                                       int32_t z) {
+    if constexpr (PAIR) {
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z)
+            : "memory");
+    } else {
+        tma_load_3d(dst, tmap, bar, x, y, z);
+    }
+}
+
+// Four rows (r0..r3, any order) of a 2-D tensor whose map has a one-row box;
+// they land as a 4-row box at dst in the map's swizzled layout.
+template <bool PAIR>
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3) {
+    if constexpr (PAIR) {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+            ".cta_group::2 [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+            : "memory");
+    } else {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+            : "memory");
+    }
+}
+
+// ---- tcgen05 for either tile shape
+
+template <bool PAIR>
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                    uint32_t accumulate) {
+    if constexpr (PAIR) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        mma_f16(d_tmem, a_desc, b_desc, idesc, accumulate);
+    }
+}
+
+// One arrival on `bar` (pair: on the barrier at that offset in both CTAs)
+// when this thread's earlier tcgen05 operations have completed.
+template <bool PAIR>
+__device__ __forceinline__ void commit(uint32_t bar) {
+    if constexpr (PAIR) {
+        const uint16_t both = 3;
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+            " [%0], %1;" ::"r"(bar),
+            "h"(both)
+            : "memory");
+    } else {
+        mma_commit(bar);
+    }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc_all(uint32_t dst_smem) {
+    if constexpr (PAIR) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+        tmem_alloc(dst_smem, kTmemCols);
+        tmem_relinquish();
+    }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tmem_free_all(uint32_t taddr) {
+    if constexpr (PAIR) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kTmemCols)
+                     : "memory");
+    } else {
+        tmem_dealloc(taddr, kTmemCols);
+    }
 }
 
 template <bool BF16>
@@ -138,21 +279,29 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
     }
 }
 
-template <bool BF16, bool GATHER>
+template <bool BF16, bool GATHER, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmLaunch p) {
+    using S = Shape<PAIR>;
+    constexpr int STAGES = S::STAGES;
+    constexpr int TILE_M = S::TILE_M;
+    constexpr int kCtas = S::kCtas;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *base_ptr = smem_raw + (base - raw);
     const uint32_t a_smem = base;
     const uint32_t b_smem = base + STAGES * A_STAGE_BYTES;
-    Control &C = *reinterpret_cast<Control *>(base_ptr + STAGES * (A_STAGE_BYTES + B_STAGE_BYTES));
+    Control<STAGES> &C =
+        *reinterpret_cast<Control<STAGES> *>(base_ptr + STAGES * (A_STAGE_BYTES + S::B_STAGE_BYTES));
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int e = p.e;
+    const uint32_t rank = PAIR ? cluster_rank() : 0;  // 0: this CTA issues the MMAs
+    const int unit = blockIdx.x / kCtas;                // CTA (pair) index in the persistent grid
+    const int nunits = gridDim.x / kCtas;
 
-    // ---- prologue: plan (warp 0), TMEM (MMA warp), barriers (warp 1)
+    // ---- prologue: plan (warp 0), barriers (warp 1), TMEM (MMA warp)
     if (warp == 0) {
         const bool good = build_segment_table(p.recvCounts, p.W, e, p.A, C.seg, lane);
         const int tn1 = (p.N1 + p.bn1 - 1) / p.bn1;
@@ -160,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if (lane < e) {
             row0 = C.seg.dst[lane * p.W];
             rows = C.seg.dst[(lane + 1) * p.W] - row0;
-            tiles = good ? ((rows + BM - 1) / BM) * tn1 : 0;
+            tiles = good ? ((rows + TILE_M - 1) / TILE_M) * tn1 : 0;
         }
         int inc = tiles;
 #pragma unroll
@@ -175,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             if (p.BS > 0) {
                 const int tn2 = (p.N2 + p.bn2 - 1) / p.bn2;
                 C.g[e] = GroupInfo{0, p.BS, tn2, total};
-                total += good ? ((p.BS + BM - 1) / BM) * tn2 : 0;
+                total += good ? ((p.BS + TILE_M - 1) / TILE_M) * tn2 : 0;
                 ng = e + 1;
             }
             C.g[ng] = GroupInfo{0, 0, 1, total};
@@ -192,17 +341,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             for (int s = 0; s < STAGES; ++s) {
                 mbar_init(smem_u32(&C.full[s]), 1);
                 mbar_init(smem_u32(&C.empty[s]), 1);
-                mbar_init(smem_u32(&C.written[s]), kProducerThreads);
             }
             for (int a = 0; a < 2; ++a) {
                 mbar_init(smem_u32(&C.tfull[a]), 1);
-                mbar_init(smem_u32(&C.tempty[a]), 4);
+                mbar_init(smem_u32(&C.tempty[a]), 4 * kCtas);
             }
             fence_barrier_init();
         }
     } else if (warp == 2) {
         if (lane == 0) {
-            if (!GATHER) prefetch_tensormap(&p.tmA_routed);
+            if (p.A > 0) prefetch_tensormap(&p.tmA_routed);
             prefetch_tensormap(&p.tmB_routed);
             if (p.BS > 0) {
                 prefetch_tensormap(&p.tmA_shared);
@@ -210,183 +358,156 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             }
         }
     } else if (warp == kMmaWarp) {
-        tmem_alloc(smem_u32(&C.tmem_base), kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_all<PAIR>(smem_u32(&C.tmem_base));
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();
+    else __syncthreads();
     tc_fence_after_sync();
 
     const int total = C.total_tiles;
+    const uint32_t full0 = smem_u32(&C.full[0]);
 
     if (warp < kProducerWarps) {
         // =========================================================== producers
-        if (!GATHER) {
-            if (threadIdx.x == 0) {
-                uint32_t it = 0;  // stages issued
-                bool ok = true;
-                for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                    const Tile w = decode_tile(C, t);
-                    const bool shared = w.g >= e;
-                    const CUtensorMap *ta = shared ? &p.tmA_shared : &p.tmA_routed;
-                    const CUtensorMap *tb = shared ? &p.tmB_shared : &p.tmB_routed;
-                    const int K = shared ? p.H2 : p.H1;
-                    const int bn = shared ? p.bn2 : p.bn1;
-                    const int nb = (bn + 63) / 64;
-                    const int y = C.g[w.g].row0 + w.m * BM;
-                    const int xn = w.n * bn;
-                    const int z = shared ? 0 : w.g;
-                    const uint32_t bytes = A_STAGE_BYTES + nb * B_ATOM_BYTES;
-                    const int kblocks = (K + BK - 1) / BK;
-                    for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                        const int s = it % STAGES;
-                        if (!wait_phase(C, &C.empty[s], ((it / STAGES) & 1) ^ 1, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t fb = smem_u32(&C.full[s]);
-                        mbar_arrive_expect_tx(fb, bytes);
-                        tma_load_2d(a_smem + s * A_STAGE_BYTES, ta, fb, kb * BK, y);
-                        for (int c = 0; c < nb; ++c)
-                            tma_load_3d(b_smem + s * B_STAGE_BYTES + c * B_ATOM_BYTES, tb, fb, xn + c * 64,
-                                        kb * BK, z);
-                    }
-                }
-                // Tail: wait until the MMAs released every stage we filled.
-                for (int i = 0; i < STAGES && ok; ++i, ++it)
-                    ok = wait_phase(C, &C.empty[it % STAGES], ((it / STAGES) & 1) ^ 1, p.status);
-            }
-        } else {
-            const int ptid = threadIdx.x;     // 0..127
-            const int chunk = lane & 7;       // 16-byte chunk of the 128-byte row slice
-            const int rsub = warp * 32 + (lane >> 3);  // rows rsub + 4 * i, i < 8
-            const uint16_t *ata = static_cast<const uint16_t *>(p.ataOut);
-            const bool want_perm = p.permuteOut != nullptr;
-            uint32_t issued = 0, completed = 0;
-            uint32_t store_bits = 0;  // stages whose A tile goes to permuteOut
+        if (warp == 0) {
+            uint32_t it = 0;  // stages issued
             bool ok = true;
-
-            auto complete_oldest = [&]() -> bool {
-                const int s = completed % STAGES;
-                const uint32_t par = (completed / STAGES) & 1;
-                fence_proxy_async_smem();
-                mbar_arrive(smem_u32(&C.written[s]));
-                bool good = true;
-                if (ptid == 0) {
-                    good = wait_phase(C, &C.written[s], par, p.status);
-                    if (good) {
-                        if ((store_bits >> s) & 1) {
-                            tma_store_2d(&p.tmA_routed, a_smem + s * A_STAGE_BYTES, C.store_x[s],
-                                         C.store_y[s]);
-                            bulk_wait_read_all();
-                        }
-                        mbar_arrive(smem_u32(&C.full[s]));
-                    }
-                }
-                ++completed;
-                return good;
-            };
-
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int t = unit; t < total && ok; t += nunits) {
                 const Tile w = decode_tile(C, t);
                 const bool shared = w.g >= e;
+                const CUtensorMap *tb = shared ? &p.tmB_shared : &p.tmB_routed;
                 const int K = shared ? p.H2 : p.H1;
                 const int bn = shared ? p.bn2 : p.bn1;
-                const int nb = (bn + 63) / 64;
-                const int xn = w.n * bn;
-                const int y = C.g[w.g].row0 + w.m * BM;
+                const int bnc = bn / kCtas;           // weight columns this CTA stages
+                const int nb = (bnc + 63) / 64;
+                const int y = C.g[w.g].row0 + w.m * TILE_M + rank * BM;  // this CTA's first row
+                const int xn = w.n * bn + rank * bnc;
+                const int z = shared ? 0 : w.g;
+                const uint32_t bytes = kCtas * (A_STAGE_BYTES + nb * B_ATOM_BYTES);
                 const int kblocks = (K + BK - 1) / BK;
-                const bool store = want_perm && !shared && w.n == 0;
-                // Source row of each of this thread's 8 rows (nullptr: zero fill).
-                const uint16_t *src[8];
+                // Fused path: lane l owns tile rows 4l .. 4l+3 (expert-major rows
+                // y + 4l + k; they may run past the group, and those results
+                // are masked).  Rows of one segment come from consecutive
+                // ataOut rows, so an aligned block of 8 .. 128 tile rows that
+                // lies in one segment is one ordinary TMA box; only 4-row
+                // groups that straddle a segment boundary (or the end of A)
+                // use a row gather.  box_level: 0 = gather4 of this lane's
+                // rows, k >= 1 = this lane loads the box of 4 << k rows it
+                // starts, -1 = another lane's box covers these rows.
+                int32_t src[4] = {0, 0, 0, 0};
+                int box_level = 0;
+                if (GATHER && !shared) {
+                    const int nseg = p.W * e;  // sentinel segment: past the last row
+                    int seg_first = nseg, seg_last = nseg;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = rsub + 4 * i;
-                    if (!shared) {
-                        const int d = y + r;  // expert-major row; may run into the next group
-                        src[i] = d < p.A ? ata + static_cast<size_t>(source_row(C.seg, p.W, e, d)) * p.H1
-                                         : nullptr;
-                    } else {
-                        src[i] = nullptr;  // shared rows arrive by TMA
+                    for (int k = 0; k < 4; ++k) {
+                        const int d = y + 4 * lane + k;
+                        const int sg = d < p.A ? segment_of(C.seg, p.W, e, d) : nseg;
+                        src[k] = sg < nseg ? source_row_in(C.seg, p.W, e, sg, d) : p.A - 1;
+                        if (k == 0) seg_first = sg;
+                        if (k == 3) seg_last = sg;
                     }
+                    int best = 0;
+#pragma unroll
+                    for (int k = 1; k <= 5; ++k) {
+                        const int g0 = lane & ~((1 << k) - 1);
+                        const int sf = __shfl_sync(0xffffffffu, seg_first, g0);
+                        const int sl = __shfl_sync(0xffffffffu, seg_last, g0 + (1 << k) - 1);
+                        if (sf == sl && sf < nseg) best = k;
+                    }
+                    box_level = best == 0 ? 0 : ((lane & ((1 << best) - 1)) == 0 ? best : -1);
                 }
-                for (int kb = 0; kb < kblocks; ++kb, ++issued) {
-                    const int s = issued % STAGES;
-                    if (!wait_phase(C, &C.empty[s], ((issued / STAGES) & 1) ^ 1, p.status)) {
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    bool free_slot = true;
+                    if (lane == 0)
+                        free_slot = wait_phase(&C.abort, &C.empty[s], ((it / STAGES) & 1) ^ 1, p.status);
+                    if (!__shfl_sync(0xffffffffu, free_slot, 0)) {
                         ok = false;
                         break;
                     }
+                    const uint32_t fb_own = full0 + s * sizeof(uint64_t);
+                    const uint32_t fb = PAIR ? map_to_rank(fb_own, 0) : fb_own;  // the MMA CTA's barrier
                     const uint32_t a_st = a_smem + s * A_STAGE_BYTES;
-                    if (ptid == 0) {
-                        const uint32_t fb = smem_u32(&C.full[s]);
-                        const CUtensorMap *tb = shared ? &p.tmB_shared : &p.tmB_routed;
-                        const int z = shared ? 0 : w.g;
-                        asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(fb),
-                                     "r"(nb * B_ATOM_BYTES + (shared ? A_STAGE_BYTES : 0u))
-                                     : "memory");
-                        if (shared) tma_load_2d(a_st, &p.tmA_shared, fb, kb * BK, y);
+                    if (lane == 0 && rank == 0) mbar_arrive_expect_tx(fb_own, bytes);
+                    __syncwarp();
+                    if (GATHER && !shared) {
+                        if (box_level == 0)
+                            tma_gather4<PAIR>(a_st + lane * 512, &p.tmA_routed, fb, kb * BK, src[0], src[1],
+                                              src[2], src[3]);
+                        else if (box_level > 0)
+                            tma_2d<PAIR>(a_st + lane * 512, &p.tmA_box[box_level - 1], fb, kb * BK, src[0]);
+                    } else if (lane == 0) {
+                        tma_2d<PAIR>(a_st, shared ? &p.tmA_shared : &p.tmA_routed, fb, kb * BK,
+                                     shared ? w.m * TILE_M + static_cast<int>(rank) * BM : y);
+                    }
+                    if (lane == 0)
                         for (int c = 0; c < nb; ++c)
-                            tma_load_3d(b_smem + s * B_STAGE_BYTES + c * B_ATOM_BYTES, tb, fb, xn + c * 64,
-                                        kb * BK, z);
-                        C.store_x[s] = kb * BK;
-                        C.store_y[s] = y;
-                    }
-                    if (!shared) {
-                        const int col = kb * BK + chunk * 8;
-                        const bool col_ok = col < K;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int r = rsub + 4 * i;
-                            const uint32_t dst = a_st + r * 128 + ((chunk ^ (r & 7)) << 4);
-                            const bool live = col_ok && src[i] != nullptr;
-                            cp_async_16_zfill(dst, live ? src[i] + col : ata, live ? 16u : 0u);
-                        }
-                    }
-                    cp_async_commit();
-                    store_bits = (store_bits & ~(1u << s)) | ((store ? 1u : 0u) << s);
-                    if (issued + 1 - completed > kGatherLag) {
-                        cp_async_wait<kGatherLag>();
-                        if (!complete_oldest()) {
-                            ok = false;
-                            break;
-                        }
-                    }
+                            tma_3d<PAIR>(b_smem + s * S::B_STAGE_BYTES + c * B_ATOM_BYTES, tb, fb, xn + c * 64,
+                                         kb * BK, z);
                 }
             }
-            cp_async_wait<0>();
-            while (ok && completed < issued) ok = complete_oldest();
-            if (ptid == 0) {
-                bulk_wait_all();
-                for (int i = 0; i < STAGES && ok; ++i, ++issued)
-                    ok = wait_phase(C, &C.empty[issued % STAGES], ((issued / STAGES) & 1) ^ 1, p.status);
+            // Tail: wait until the MMAs released every stage we filled.
+            if (lane == 0)
+                for (int i = 0; i < STAGES && ok; ++i, ++it)
+                    ok = wait_phase(&C.abort, &C.empty[it % STAGES], ((it / STAGES) & 1) ^ 1, p.status);
+        } else if (GATHER && p.permuteOut != nullptr) {
+            // Warps 1-3 write permuteOut for this CTA's rows of the tiles of
+            // the first column, straight from ataOut (16-byte vectors, 4 in
+            // flight per lane), independent of the shared-memory pipeline.
+            const int cw = warp - 1;  // 0..2
+            const int vpr = p.H1 / 8;
+            const uint4 *ata = static_cast<const uint4 *>(p.ataOut);
+            uint4 *perm = static_cast<uint4 *>(p.permuteOut);
+            for (int t = unit; t < total; t += nunits) {
+                const Tile w = decode_tile(C, t);
+                if (w.g >= e || w.n != 0) continue;
+                const int first = w.m * TILE_M + static_cast<int>(rank) * BM;  // row within the group
+                const int r_end = min(BM, C.g[w.g].rows - first);
+                const int y = C.g[w.g].row0 + first;
+                for (int r = cw; r < r_end; r += kProducerWarps - 1) {
+                    const int d = y + r;
+                    const uint4 *in = ata + static_cast<size_t>(source_row(C.seg, p.W, e, d)) * vpr;
+                    uint4 *out = perm + static_cast<size_t>(d) * vpr;
+                    int v = lane;
+                    for (; v + 96 < vpr; v += 128) {
+                        const uint4 a = in[v], b = in[v + 32], c = in[v + 64], f = in[v + 96];
+                        out[v] = a;
+                        out[v + 32] = b;
+                        out[v + 64] = c;
+                        out[v + 96] = f;
+                    }
+                    for (; v < vpr; v += 32) out[v] = in[v];
+                }
             }
         }
     } else if (warp == kMmaWarp) {
         // =========================================================== MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc1 = instr_desc_f16(BF16, BM, p.bn1);
-            const uint32_t idesc2 = instr_desc_f16(BF16, BM, p.bn2 > 0 ? p.bn2 : 16);
+        if (lane == 0 && rank == 0) {
+            const uint32_t idesc1 = instr_desc_f16(BF16, TILE_M, p.bn1);
+            const uint32_t idesc2 = instr_desc_f16(BF16, TILE_M, p.bn2 > 0 ? p.bn2 : 16);
             uint32_t it = 0, tl = 0;  // stages consumed, tiles done
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tl) {
+            for (int t = unit; t < total && ok; t += nunits, ++tl) {
                 const Tile w = decode_tile(C, t);
                 const bool shared = w.g >= e;
                 const int K = shared ? p.H2 : p.H1;
                 const uint32_t idesc = shared ? idesc2 : idesc1;
                 const int kblocks = (K + BK - 1) / BK;
                 const int acc = tl & 1;
-                if (!wait_phase(C, &C.tempty[acc], ((tl >> 1) & 1) ^ 1, p.status)) break;
+                if (!wait_phase<PAIR>(&C.abort, &C.tempty[acc], ((tl >> 1) & 1) ^ 1, p.status)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = C.tmem_base + acc * kAccCols;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % STAGES;
-                    if (!wait_phase(C, &C.full[s], (it / STAGES) & 1, p.status)) {
+                    if (!wait_phase(&C.abort, &C.full[s], (it / STAGES) & 1, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
                     const uint32_t a0 = a_smem + s * A_STAGE_BYTES;
-                    const uint32_t b0 = b_smem + s * B_STAGE_BYTES;
+                    const uint32_t b0 = b_smem + s * S::B_STAGE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart;
@@ -394,29 +515,32 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         // B: N-major, 128-byte swizzle; 64-column atoms 8 KB apart
                         //    (leading offset), 8-row K groups 1024 B apart
                         //    (stride offset); a K step of 16 rows is 2 KB.
+                        // Pair: both CTAs hold their operand halves at these
+                        // same offsets.
                         const uint64_t ad = smem_desc(a0 + kk * 32, 16, 1024, kSwizzle128B);
                         const uint64_t bd = smem_desc(b0 + kk * 2048, B_ATOM_BYTES, 1024, kSwizzle128B);
-                        mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                        mma<PAIR>(d_tmem, ad, bd, idesc, (kb | kk) != 0);
                     }
-                    mma_commit(smem_u32(&C.empty[s]));
+                    commit<PAIR>(smem_u32(&C.empty[s]));
                 }
-                if (ok) mma_commit(smem_u32(&C.tfull[acc]));
+                if (ok) commit<PAIR>(smem_u32(&C.tfull[acc]));
             }
         }
     } else {
         // =========================================================== epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may read
+        const uint32_t tempty0 = smem_u32(&C.tempty[0]);
         uint32_t tl = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tl) {
+        for (int t = unit; t < total; t += nunits, ++tl) {
             const Tile w = decode_tile(C, t);
             const bool shared = w.g >= e;
             const int acc = tl & 1;
-            if (!wait_phase(C, &C.tfull[acc], (tl >> 1) & 1, p.status)) break;
+            if (!wait_phase(&C.abort, &C.tfull[acc], (tl >> 1) & 1, p.status)) break;
             __syncwarp();  // lanes leave the wait independently; tcgen05.ld needs the whole warp
             tc_fence_after_sync();
             const int N = shared ? p.N2 : p.N1;
             const int bn = shared ? p.bn2 : p.bn1;
-            const int row = w.m * BM + q * 32 + lane;
+            const int row = w.m * TILE_M + static_cast<int>(rank) * BM + q * 32 + lane;
             const bool valid = row < C.g[w.g].rows;
             const int n0 = w.n * bn;
             const size_t out_row = static_cast<size_t>(shared ? row : C.g[w.g].row0 + row);
@@ -444,35 +568,86 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&C.tempty[acc]));
+            if (lane == 0) {
+                const uint32_t te = tempty0 + acc * sizeof(uint64_t);
+                if constexpr (PAIR) mbar_arrive_cluster(map_to_rank(te, 0));
+                else mbar_arrive(te);
+            }
         }
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();
+    else __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after_sync();
-        tmem_dealloc(C.tmem_base, kTmemCols);
+        tmem_free_all<PAIR>(C.tmem_base);
     }
 }
 
-template <bool BF16, bool GATHER>
+template <bool BF16, bool GATHER, bool PAIR>
 cudaError_t launch_variant(const GemmLaunch &p, cudaStream_t stream) {
-    auto kern = grouped_gemm_kernel<BF16, GATHER>;
+    auto kern = grouped_gemm_kernel<BF16, GATHER, PAIR>;
+    constexpr size_t smem = smem_bytes<PAIR>();
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kSmemBytes));
+                                           static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    kern<<<p.grid, kThreads, kSmemBytes, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = Shape<PAIR>::kCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 1 : 0;
+    err = cudaLaunchKernelEx(&cfg, kern, p);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
+}
+
+template <bool BF16, bool GATHER, bool PAIR>
+int max_units_for() {
+    auto kern = grouped_gemm_kernel<BF16, GATHER, PAIR>;
+    constexpr size_t smem = smem_bytes<PAIR>();
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 1024, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = Shape<PAIR>::kCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+    return n;
 }
 
 }  // namespace
 
-size_t grouped_gemm_smem_bytes() { return kSmemBytes; }
+size_t grouped_gemm_smem_bytes(int pair) { return pair ? smem_bytes<true>() : smem_bytes<false>(); }
+
+int grouped_gemm_max_coresident(int pair) {
+    // Clusters (pair) or CTAs (single) that fit on the device at once.
+    return pair ? max_units_for<true, true, true>() : max_units_for<true, true, false>();
+}
 
 cudaError_t launch_grouped_gemm(const GemmLaunch &p, cudaStream_t stream) {
-    if (p.bf16) return p.gather ? launch_variant<true, true>(p, stream) : launch_variant<true, false>(p, stream);
-    return p.gather ? launch_variant<false, true>(p, stream) : launch_variant<false, false>(p, stream);
+    const bool pair = p.pair != 0;
+#define A2AV_LAUNCH(B, G)                                                                          \
+    (pair ? launch_variant<B, G, true>(p, stream) : launch_variant<B, G, false>(p, stream))
+    if (p.bf16) return p.gather ? A2AV_LAUNCH(true, true) : A2AV_LAUNCH(true, false);
+    return p.gather ? A2AV_LAUNCH(false, true) : A2AV_LAUNCH(false, false);
+#undef A2AV_LAUNCH
 }
 
 }  // namespace a2av

@@ -36,15 +36,18 @@ struct GemmLaunch {
     int32_t bf16;         // 1: bf16, 0: fp16
     int32_t gather;       // 1: A rows gathered from ataOut (fused permute)
     const void *ataOut;   // for gather
-    void *permuteOut;     // for gather: written from the staged A tiles (may be NULL)
-    int32_t grid;         // persistent CTAs
-    CUtensorMap tmA_routed;   // expert-major A (split path) or permuteOut store map (fused)
+    void *permuteOut;     // for gather: rows copied by warps 1-3 (may be NULL)
+    int32_t pair;         // 1: 256-row tiles on CTA pairs (cta_group::2), 0: 128-row tiles
+    int32_t grid;         // persistent CTAs (pair: an even number, two per cluster)
+    CUtensorMap tmA_routed;   // split: expert-major A, 128-row box; fused: ataOut, 1-row box (gather)
+    CUtensorMap tmA_box[5];   // fused: ataOut with 8, 16, 32, 64, 128-row boxes (contiguous runs)
     CUtensorMap tmB_routed;   // gmmWeight [e, H1, N1]
     CUtensorMap tmA_shared;   // mmX [BS, H2]
     CUtensorMap tmB_shared;   // mmWeight as [1, H2, N2]
 };
 
 cudaError_t launch_grouped_gemm(const GemmLaunch &p, cudaStream_t stream);
-size_t grouped_gemm_smem_bytes();
+size_t grouped_gemm_smem_bytes(int pair);
+int grouped_gemm_max_coresident(int pair);  // CTAs (single) or clusters (pair) resident at once
 
 }  // namespace a2av

@@ -76,19 +76,28 @@ __device__ __forceinline__ bool build_segment_table(const int32_t *__restrict__ 
     return !bad && total_r == A && total_e == A;
 }
 
-// First ataOut row feeding permuteOut row d (0 <= d < A): the last
-// expert-major segment starting at or before d (empty segments share their
-// start with the next one, so the search skips them).
-__device__ __forceinline__ int32_t source_row(const SegmentTable &t, int W, int e, int32_t d) {
-    const int E = W * e;
-    int lo = 0, hi = E;  // invariant: dst[lo] <= d < dst[hi]
+// Expert-major segment holding permuteOut row d (0 <= d < A): the last
+// segment starting at or before d (empty segments share their start with the
+// next one, so the search skips them).
+__device__ __forceinline__ int segment_of(const SegmentTable &t, int W, int e, int32_t d) {
+    int lo = 0, hi = W * e;  // invariant: dst[lo] <= d < dst[hi]
     while (hi - lo > 1) {
         int mid = (lo + hi) >> 1;
         if (t.dst[mid] <= d) lo = mid;
         else hi = mid;
     }
-    const int j = lo / W, w = lo % W;
-    return t.src[w * e + j] + (d - t.dst[lo]);
+    return lo;
+}
+
+// ataOut row feeding permuteOut row d, given its expert-major segment.
+__device__ __forceinline__ int32_t source_row_in(const SegmentTable &t, int W, int e, int seg, int32_t d) {
+    const int j = seg / W, w = seg % W;
+    return t.src[w * e + j] + (d - t.dst[seg]);
+}
+
+// ataOut row feeding permuteOut row d (0 <= d < A).
+__device__ __forceinline__ int32_t source_row(const SegmentTable &t, int W, int e, int32_t d) {
+    return source_row_in(t, W, e, segment_of(t, W, e, d), d);
 }
 
 }  // namespace a2av
