@@ -501,11 +501,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const uint32_t d_tmem = C.tmem_base + acc * kAccCols;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % STAGES;
+                    // Operands arrive by TMA (async proxy), as the MMA reads
+                    // them: the barrier phase alone orders the two, and no
+                    // tcgen05 fence is needed here.
                     if (!wait_phase(&C.abort, &C.full[s], (it / STAGES) & 1, p.status)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after_sync();
                     const uint32_t a0 = a_smem + s * A_STAGE_BYTES;
                     const uint32_t b0 = b_smem + s * S::B_STAGE_BYTES;
 #pragma unroll
