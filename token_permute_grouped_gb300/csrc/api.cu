@@ -68,9 +68,14 @@ size_t staging_bytes(const a2av_gmm_desc *d) {
     return (b + 255) / 256 * 256;
 }
 
-// Tile width: the fewest column tiles of at most 256, then the narrowest
-// multiple of 16 that covers N with that many tiles.
-int pick_bn(int64_t N) {
+// Tile width.  When N is a multiple of 64 the width is a whole number of
+// 64-column atoms per CTA, so a stage's weight columns are one TMA load (the
+// TMA issue rate, not bandwidth, bounds the main loop): up to 256, the last
+// tile zero-filled past N.  Otherwise the fewest column tiles of at most 256,
+// each the narrowest multiple of 16 that covers N.
+int pick_bn(int64_t N, int ctas) {
+    const int64_t atom = 64 * ctas;
+    if (N % 64 == 0) return static_cast<int>(std::min<int64_t>(256, (N + atom - 1) / atom * atom));
     const int64_t tiles = (N + 255) / 256;
     int64_t bn = (N + tiles - 1) / tiles;
     bn = (bn + 15) / 16 * 16;
@@ -120,6 +125,24 @@ bool make_weight_map(CUtensorMap *m, const void *ptr, int64_t groups, int64_t K,
     cuuint32_t box[3] = {64, 64, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, tmap_type(dtype), 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same weights seen as 4-D: [groups][N / 64 atoms][K][64 columns], box =
+// 64 columns x 64 K rows x `atoms` atoms.  One load then fills a stage's
+// weight columns in the layout of consecutive 64-column atoms (8 KB apart),
+// the same bytes as `atoms` loads of the 3-D map.  Needs N % 64 == 0.
+bool make_weight_map_atoms(CUtensorMap *m, const void *ptr, int64_t groups, int64_t K, int64_t N,
+                           int32_t dtype, uint32_t atoms) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N / 64),
+                          static_cast<cuuint64_t>(groups)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(N * 2), 128, static_cast<cuuint64_t>(K * N * 2)};
+    cuuint32_t box[4] = {64, 64, atoms, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, tmap_type(dtype), 4, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -211,11 +234,11 @@ a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const in
     g.A = static_cast<int32_t>(d.A);
     g.H1 = static_cast<int32_t>(d.H1);
     g.N1 = static_cast<int32_t>(d.N1);
-    g.bn1 = pick_bn(d.N1);
+    g.bn1 = pick_bn(d.N1, use_pair(&d) ? 2 : 1);
     g.BS = has_shared ? static_cast<int32_t>(d.BS) : 0;
     g.H2 = has_shared ? static_cast<int32_t>(d.H2) : 0;
     g.N2 = has_shared ? static_cast<int32_t>(d.N2) : 0;
-    g.bn2 = has_shared ? pick_bn(d.N2) : 0;
+    g.bn2 = has_shared ? pick_bn(d.N2, use_pair(&d) ? 2 : 1) : 0;
     g.gmmY = gmmY;
     g.mmY = mmY;
     g.status = status;
@@ -228,6 +251,18 @@ a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const in
     if (has_shared) {
         if (!make_rows_map(&g.tmA_shared, mmX, d.BS, d.H2, d.dtype)) return A2AV_ERR_CUDA;
         if (!make_weight_map(&g.tmB_shared, mmWeight, 1, d.H2, d.N2, d.dtype)) return A2AV_ERR_CUDA;
+    }
+    // One-load weight stages where the columns come in whole 64-wide atoms.
+    const int cta_cols = use_pair(&d) ? 2 : 1;
+    if (d.N1 % 64 == 0 && (g.bn1 / cta_cols) % 64 == 0) {
+        if (!make_weight_map_atoms(&g.tmB4_routed, gmmWeight, d.e, d.H1, d.N1, d.dtype, g.bn1 / cta_cols / 64))
+            return A2AV_ERR_CUDA;
+        g.b4_routed = 1;
+    }
+    if (has_shared && d.N2 % 64 == 0 && (g.bn2 / cta_cols) % 64 == 0) {
+        if (!make_weight_map_atoms(&g.tmB4_shared, mmWeight, 1, d.H2, d.N2, d.dtype, g.bn2 / cta_cols / 64))
+            return A2AV_ERR_CUDA;
+        g.b4_shared = 1;
     }
 
     bool permute_ran = false;

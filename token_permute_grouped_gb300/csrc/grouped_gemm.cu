@@ -191,6 +191,24 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const void *tmap, uint32_t 
     }
 }
 
+template <bool PAIR>
+__device__ __forceinline__ void tma_4d(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y,
+                                       int32_t z, int32_t w) {
+    if constexpr (PAIR) {
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+            " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+            : "memory");
+    } else {
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+            : "memory");
+    }
+}
+
 // Four rows (r0..r3, any order) of a 2-D tensor whose map has a one-row box;
 // they land as a 4-row box at dst in the map's swizzled layout.
 template <bool PAIR>
@@ -377,6 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const Tile w = decode_tile(C, t);
                 const bool shared = w.g >= e;
                 const CUtensorMap *tb = shared ? &p.tmB_shared : &p.tmB_routed;
+                const CUtensorMap *tb4 = shared ? &p.tmB4_shared : &p.tmB4_routed;
+                const bool b4 = shared ? p.b4_shared : p.b4_routed;
                 const int K = shared ? p.H2 : p.H1;
                 const int bn = shared ? p.bn2 : p.bn1;
                 const int bnc = bn / kCtas;           // weight columns this CTA stages
@@ -442,10 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         tma_2d<PAIR>(a_st, shared ? &p.tmA_shared : &p.tmA_routed, fb, kb * BK,
                                      shared ? w.m * TILE_M + static_cast<int>(rank) * BM : y);
                     }
-                    if (lane == 0)
-                        for (int c = 0; c < nb; ++c)
-                            tma_3d<PAIR>(b_smem + s * S::B_STAGE_BYTES + c * B_ATOM_BYTES, tb, fb, xn + c * 64,
-                                         kb * BK, z);
+                    if (lane == 0) {
+                        if (b4)  // all the stage's weight atoms in one load
+                            tma_4d<PAIR>(b_smem + s * S::B_STAGE_BYTES, tb4, fb, 0, kb * BK, xn / 64, z);
+                        else
+                            for (int c = 0; c < nb; ++c)
+                                tma_3d<PAIR>(b_smem + s * S::B_STAGE_BYTES + c * B_ATOM_BYTES, tb, fb,
+                                             xn + c * 64, kb * BK, z);
+                    }
                 }
             }
             // Tail: wait until the MMAs released every stage we filled.
@@ -487,6 +511,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if (lane == 0 && rank == 0) {
             const uint32_t idesc1 = instr_desc_f16(BF16, TILE_M, p.bn1);
             const uint32_t idesc2 = instr_desc_f16(BF16, TILE_M, p.bn2 > 0 ? p.bn2 : 16);
+            // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; a K
+            //    step of 16 elements is 32 bytes along the row.
+            // B: N-major, 128-byte swizzle; 64-column atoms 8 KB apart
+            //    (leading offset), 8-row K groups 1024 B apart (stride
+            //    offset); a K step of 16 rows is 2 KB.
+            // Pair: both CTAs hold their operand halves at the same offsets.
+            const uint64_t a_desc0 = smem_desc(a_smem, 16, 1024, kSwizzle128B);
+            const uint64_t b_desc0 = smem_desc(b_smem, B_ATOM_BYTES, 1024, kSwizzle128B);
+            const uint32_t empty0 = smem_u32(&C.empty[0]);
             uint32_t it = 0, tl = 0;  // stages consumed, tiles done
             bool ok = true;
             for (int t = unit; t < total && ok; t += nunits, ++tl) {
@@ -501,29 +534,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const uint32_t d_tmem = C.tmem_base + acc * kAccCols;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % STAGES;
+                    const uint32_t par = (it / STAGES) & 1;
                     // Operands arrive by TMA (async proxy), as the MMA reads
                     // them: the barrier phase alone orders the two, and no
                     // tcgen05 fence is needed here.
-                    if (!wait_phase(&C.abort, &C.full[s], (it / STAGES) & 1, p.status)) {
+                    if (!mbar_try_wait(full0 + s * sizeof(uint64_t), par) &&
+                        !wait_phase(&C.abort, &C.full[s], par, p.status)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t a0 = a_smem + s * A_STAGE_BYTES;
-                    const uint32_t b0 = b_smem + s * S::B_STAGE_BYTES;
+                    // Descriptor start addresses are in 16-byte units, so a
+                    // stage or K step is a plain add to the base descriptor.
+                    const uint64_t ad0 = a_desc0 + ((s * A_STAGE_BYTES) >> 4);
+                    const uint64_t bd0 = b_desc0 + ((s * S::B_STAGE_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart;
-                        //    a K step of 16 elements is 32 bytes along the row.
-                        // B: N-major, 128-byte swizzle; 64-column atoms 8 KB apart
-                        //    (leading offset), 8-row K groups 1024 B apart
-                        //    (stride offset); a K step of 16 rows is 2 KB.
-                        // Pair: both CTAs hold their operand halves at these
-                        // same offsets.
-                        const uint64_t ad = smem_desc(a0 + kk * 32, 16, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(b0 + kk * 2048, B_ATOM_BYTES, 1024, kSwizzle128B);
-                        mma<PAIR>(d_tmem, ad, bd, idesc, (kb | kk) != 0);
-                    }
-                    commit<PAIR>(smem_u32(&C.empty[s]));
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma<PAIR>(d_tmem, ad0 + 2 * kk, bd0 + 128 * kk, idesc, (kb | kk) != 0);
+                    commit<PAIR>(empty0 + s * sizeof(uint64_t));
                 }
                 if (ok) commit<PAIR>(smem_u32(&C.tfull[acc]));
             }

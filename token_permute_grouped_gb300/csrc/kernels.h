@@ -44,6 +44,9 @@ struct GemmLaunch {
     CUtensorMap tmB_routed;   // gmmWeight [e, H1, N1]
     CUtensorMap tmA_shared;   // mmX [BS, H2]
     CUtensorMap tmB_shared;   // mmWeight as [1, H2, N2]
+    CUtensorMap tmB4_routed;  // gmmWeight as 64-column atoms: one load per stage (when b4_routed)
+    CUtensorMap tmB4_shared;  // mmWeight likewise (when b4_shared)
+    int32_t b4_routed, b4_shared;
 };
 
 cudaError_t launch_grouped_gemm(const GemmLaunch &p, cudaStream_t stream);
