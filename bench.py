@@ -466,7 +466,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--permute-out", action="store_true")
-    ap.add_argument("--path", default="default", choices=["default", "fused", "split"])
+    ap.add_argument("--path", default="default", choices=["default", "fused", "split", "split_runs"])
     ap.add_argument("--tiles", default="default", choices=["default", "single", "pair"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

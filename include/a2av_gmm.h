@@ -80,11 +80,15 @@ typedef enum {
 
 typedef enum { A2AV_BF16 = 0, A2AV_FP16 = 1 } a2av_dtype;
 
-/* Execution path.  Both give bitwise-identical outputs. */
+/* Execution path.  All give bitwise-identical outputs. */
 typedef enum {
-    A2AV_PATH_DEFAULT = 0,     /* the fastest path this build has */
-    A2AV_PATH_FUSED = 1,       /* the grouped GEMM gathers its A rows from ataOut */
-    A2AV_PATH_SPLIT = 2        /* a permute kernel first, then the grouped GEMM */
+    A2AV_PATH_DEFAULT = 0,     /* chosen from the shapes: SPLIT_RUNS when N1 <= 1024 and
+                                  the (source, expert) runs average >= 512 rows, else SPLIT */
+    A2AV_PATH_FUSED = 1,       /* one kernel: the grouped GEMM gathers its A rows from ataOut */
+    A2AV_PATH_SPLIT = 2,       /* a permute kernel stages every row expert-major, then the GEMM */
+    A2AV_PATH_SPLIT_RUNS = 3   /* the permute kernel stages only the 128-row halves of a GEMM
+                                  tile that straddle a run boundary; the GEMM reads the
+                                  others in place from ataOut */
 } a2av_path;
 
 /* GEMM tile shape.  All give bitwise-identical outputs. */

@@ -75,6 +75,7 @@ def ws(**kw):
     ({"raw_tiles": 3}, 2),
     ({"raw_tiles": 2}, 0),
     ({"raw_path": 9}, 2),
+    ({"raw_path": 3}, 0),
     ({"H1": 4100}, 3),                  # rows must start 16-byte aligned
     ({"N2": 1020}, 3),
     ({"dtype": torch.float16}, 0),

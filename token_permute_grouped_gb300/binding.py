@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "A2AV_OK", 1: "A2AV_ERR_NULLPTR", 2: "A2AV_ERR_INVALID", 3: "
                 7: "A2AV_ERR_SCRATCH_LIMIT"}
 STATIC_SCRATCH_BYTES = 256 + (8 << 20)  # A2AV_STATIC_SCRATCH_BYTES
 DTYPES = {torch.bfloat16: 0, torch.float16: 1}
-PATHS = {"default": 0, "fused": 1, "split": 2}
+PATHS = {"default": 0, "fused": 1, "split": 2, "split_runs": 3}
 TILES = {"default": 0, "single": 1, "pair": 2}
 
 # Every symbol include/a2av_gmm.h declares.

@@ -37,16 +37,27 @@ a2av_status validate(const a2av_gmm_desc *d) {
         if (d->H2 <= 0 || d->H2 > 12288 || d->N2 <= 0 || d->N2 >= 65536) return A2AV_ERR_INVALID;
     }
     if (d->dtype != A2AV_BF16 && d->dtype != A2AV_FP16) return A2AV_ERR_INVALID;
-    if (d->path < A2AV_PATH_DEFAULT || d->path > A2AV_PATH_SPLIT) return A2AV_ERR_INVALID;
+    if (d->path < A2AV_PATH_DEFAULT || d->path > A2AV_PATH_SPLIT_RUNS) return A2AV_ERR_INVALID;
     if (d->tiles < A2AV_TILES_DEFAULT || d->tiles > A2AV_TILES_PAIR) return A2AV_ERR_INVALID;
     if (!mult8(d->H1) || !mult8(d->N1)) return A2AV_ERR_UNSUPPORTED;
     if (d->BS > 0 && (!mult8(d->H2) || !mult8(d->N2))) return A2AV_ERR_UNSUPPORTED;
     return A2AV_OK;
 }
 
-// Defaults: the combination measured fastest on GB300 for the benchmark
-// workloads (permute kernel + TMA-fed grouped GEMM on CTA pairs).
-bool use_split(const a2av_gmm_desc *d) { return d->path != A2AV_PATH_FUSED; }
+// Defaults follow GB300 measurements.  The permute kernel + TMA-fed GEMM
+// beats the one-kernel fused path everywhere (its row gathers cost TMA
+// instructions, the main loop's bottleneck).  Staging only the straddling
+// halves saves most of the permute traffic but makes the GEMM read colder A
+// rows; it wins only when the permute is a large share of the call (narrow
+// outputs, N1 <= 1024) and runs are long (>= 4 halves on average).
+int resolve_path(const a2av_gmm_desc *d) {
+    if (d->path != A2AV_PATH_DEFAULT) return d->path;
+    const int64_t runs = static_cast<int64_t>(d->W) * d->e;
+    if (d->N1 <= 1024 && d->A >= 512 * runs) return A2AV_PATH_SPLIT_RUNS;
+    return A2AV_PATH_SPLIT;
+}
+
+bool use_split(const a2av_gmm_desc *d) { return resolve_path(d) != A2AV_PATH_FUSED; }
 
 bool use_pair(const a2av_gmm_desc *d) { return d->tiles != A2AV_TILES_SINGLE; }
 
@@ -270,11 +281,19 @@ a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const in
         if (split) {
             // Expert-major rows go to permuteOut, or to the staging area.
             void *dst = perm_out ? perm_out : static_cast<uint8_t *>(workspace) + kStatusBytes;
+            // SPLIT_RUNS without permuteOut: only the 128-row halves that
+            // straddle a segment boundary are staged; the GEMM reads the rest
+            // in place.
+            const int32_t partial = (!perm_out && resolve_path(&d) == A2AV_PATH_SPLIT_RUNS) ? 1 : 0;
             a2av::PermuteLaunch pl{recvCounts, d.W, d.e, static_cast<int32_t>(d.A),
-                                   static_cast<int32_t>(d.H1), ataOut, dst, status, 1};
+                                   static_cast<int32_t>(d.H1), ataOut, dst, status, 1, partial};
             if (a2av::launch_permute(pl, sms, stream) != cudaSuccess) return A2AV_ERR_CUDA;
             permute_ran = true;
             if (!make_rows_map(&g.tmA_routed, dst, d.A, d.H1, d.dtype)) return A2AV_ERR_CUDA;
+            if (partial) {
+                if (!make_rows_map(&g.tmA_direct, ataOut, d.A, d.H1, d.dtype)) return A2AV_ERR_CUDA;
+                g.direct_halves = 1;
+            }
         } else {
             // Maps over ataOut in arrival order: a one-row box for row gathers,
             // and 8 .. 128-row boxes for runs of rows from one segment.

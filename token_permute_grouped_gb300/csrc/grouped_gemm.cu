@@ -369,10 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     } else if (warp == 2) {
         if (lane == 0) {
             if (p.A > 0) prefetch_tensormap(&p.tmA_routed);
-            prefetch_tensormap(&p.tmB_routed);
+            if (p.direct_halves) prefetch_tensormap(&p.tmA_direct);
+            prefetch_tensormap(p.b4_routed ? &p.tmB4_routed : &p.tmB_routed);
             if (p.BS > 0) {
                 prefetch_tensormap(&p.tmA_shared);
-                prefetch_tensormap(&p.tmB_shared);
+                prefetch_tensormap(p.b4_shared ? &p.tmB4_shared : &p.tmB_shared);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -415,6 +416,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 // use a row gather.  box_level: 0 = gather4 of this lane's
                 // rows, k >= 1 = this lane loads the box of 4 << k rows it
                 // starts, -1 = another lane's box covers these rows.
+                // Split path: a half whose rows of this group lie in one segment
+                // is read straight from ataOut; the permute kernel staged only
+                // the halves that straddle a segment boundary.
+                bool direct = false;
+                int32_t direct_row = 0;
+                if (!GATHER && !shared && p.direct_halves) {
+                    const int g_end = C.g[w.g].row0 + C.g[w.g].rows;
+                    if (y < g_end && half_in_one_segment(C.seg, p.W, e, y, g_end)) {
+                        direct = true;
+                        direct_row = source_row(C.seg, p.W, e, y);
+                    }
+                }
                 int32_t src[4] = {0, 0, 0, 0};
                 int box_level = 0;
                 if (GATHER && !shared) {
@@ -459,8 +472,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         else if (box_level > 0)
                             tma_2d<PAIR>(a_st + lane * 512, &p.tmA_box[box_level - 1], fb, kb * BK, src[0]);
                     } else if (lane == 0) {
-                        tma_2d<PAIR>(a_st, shared ? &p.tmA_shared : &p.tmA_routed, fb, kb * BK,
-                                     shared ? w.m * TILE_M + static_cast<int>(rank) * BM : y);
+                        if (direct)
+                            tma_2d<PAIR>(a_st, &p.tmA_direct, fb, kb * BK, direct_row);
+                        else
+                            tma_2d<PAIR>(a_st, shared ? &p.tmA_shared : &p.tmA_routed, fb, kb * BK,
+                                         shared ? w.m * TILE_M + static_cast<int>(rank) * BM : y);
                     }
                     if (lane == 0) {
                         if (b4)  // all the stage's weight atoms in one load

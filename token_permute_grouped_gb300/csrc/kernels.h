@@ -18,6 +18,7 @@ struct PermuteLaunch {
     void *dst;            // [A, H1]
     int32_t *status;      // device status word
     int32_t write_status; // 1: this kernel stores the word (first kernel of a call)
+    int32_t only_straddling;  // 1: copy only 128-row halves that straddle a segment boundary
 };
 
 cudaError_t launch_permute(const PermuteLaunch &p, int num_sms, cudaStream_t stream);
@@ -44,6 +45,8 @@ struct GemmLaunch {
     CUtensorMap tmB_routed;   // gmmWeight [e, H1, N1]
     CUtensorMap tmA_shared;   // mmX [BS, H2]
     CUtensorMap tmB_shared;   // mmWeight as [1, H2, N2]
+    CUtensorMap tmA_direct;   // split path: ataOut, 128-row box, for halves read in place
+    int32_t direct_halves;    // 1: halves inside one segment are read from ataOut directly
     CUtensorMap tmB4_routed;  // gmmWeight as 64-column atoms: one load per stage (when b4_routed)
     CUtensorMap tmB4_shared;  // mmWeight likewise (when b4_shared)
     int32_t b4_routed, b4_shared;

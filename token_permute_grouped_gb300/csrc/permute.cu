@@ -25,7 +25,7 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
 __global__ void __launch_bounds__(kPermuteThreads)
     permute_rows_kernel(const int32_t *__restrict__ recvCounts, int W, int e, int A, int H1,
                         const uint4 *__restrict__ src, uint4 *__restrict__ dst, int32_t *status,
-                        int write_status) {
+                        int write_status, int only_straddling) {
     __shared__ SegmentTable table;
     __shared__ int ok;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -45,7 +45,16 @@ __global__ void __launch_bounds__(kPermuteThreads)
     const int vpr = H1 / 8;  // 16-byte vectors per row
     const int nwarps = gridDim.x * kPermuteWarps;
     for (int d = blockIdx.x * kPermuteWarps + warp; d < A; d += nwarps) {
-        const int s = source_row(table, W, e, d);
+        const int seg = segment_of(table, W, e, d);
+        if (only_straddling) {
+            // Copy only the rows of 128-row halves that the GEMM cannot read
+            // in place (see half_in_one_segment).
+            const int j = seg / W;
+            const int g0 = table.dst[j * W], g1 = table.dst[(j + 1) * W];
+            const int first = g0 + (d - g0) / kHalfRows * kHalfRows;
+            if (half_in_one_segment(table, W, e, first, g1)) continue;
+        }
+        const int s = source_row_in(table, W, e, seg, d);
         const uint4 *in = src + static_cast<size_t>(s) * vpr;
         uint4 *out = dst + static_cast<size_t>(d) * vpr;
         int v = lane;
@@ -70,7 +79,7 @@ cudaError_t launch_permute(const PermuteLaunch &p, int num_sms, cudaStream_t str
     if (blocks < 1) blocks = 1;
     permute_rows_kernel<<<blocks, kPermuteThreads, 0, stream>>>(
         p.recvCounts, p.W, p.e, p.A, p.H1, static_cast<const uint4 *>(p.ataOut),
-        static_cast<uint4 *>(p.dst), p.status, p.write_status);
+        static_cast<uint4 *>(p.dst), p.status, p.write_status, p.only_straddling);
     return cudaGetLastError();
 }
 

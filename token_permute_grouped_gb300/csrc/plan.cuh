@@ -95,6 +95,21 @@ __device__ __forceinline__ int32_t source_row_in(const SegmentTable &t, int W, i
     return t.src[w * e + j] + (d - t.dst[seg]);
 }
 
+// Rows a GEMM CTA multiplies come in 128-row halves of its tile, counted from
+// the start of each expert group.  A half whose rows of its own group lie in
+// one segment is a contiguous run of ataOut rows, so the GEMM reads it there
+// directly; only halves that straddle a segment boundary need the
+// expert-major copy.  Rows past the group's end belong to the next group and
+// their products are discarded, so they do not count.  (Both the permute
+// kernel and the GEMM call this, so they agree on which halves are copied.)
+constexpr int kHalfRows = 128;
+
+__device__ __forceinline__ bool half_in_one_segment(const SegmentTable &t, int W, int e, int32_t first,
+                                                    int32_t group_end) {
+    const int32_t last = min(first + kHalfRows, group_end) - 1;
+    return segment_of(t, W, e, first) == segment_of(t, W, e, last);
+}
+
 // ataOut row feeding permuteOut row d (0 <= d < A).
 __device__ __forceinline__ int32_t source_row(const SegmentTable &t, int W, int e, int32_t d) {
     return source_row_in(t, W, e, segment_of(t, W, e, d), d);
