@@ -459,6 +459,52 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_amp(args):
+    """Loss-scale step: the inf/NaN scan over a layer output (HBM-bound) and
+    the scalar update ("aclnnAmpUpdateScale"), timed with CUDA events."""
+    assert torch.cuda.is_available()
+    dev = torch.device("cuda", 0)
+    build.build()
+    binding.load()
+    n = 34502 * 4096  # the DeepSeek-V3-like gmmY: 283 MB of bf16
+    bufs = [torch.randn(n, device=dev, dtype=torch.float32).to(torch.bfloat16) for _ in range(2)]
+    flag = torch.zeros(1, device=dev)
+    scale = torch.tensor([65536.0], device=dev)
+    tracker = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(args.warmup):
+        binding.a2av_found_nonfinite(bufs[i % 2], flag)
+        binding.a2av_amp_update_scale(scale, tracker, flag, 2.0, 0.5, 2000)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    with ClockSampler(0) as clocks:
+        ev[0].record(stream)
+        for i in range(args.steps):
+            binding.a2av_found_nonfinite(bufs[i % 2], flag)
+        ev[1].record(stream)
+        for i in range(args.steps):
+            binding.a2av_amp_update_scale(scale, tracker, flag, 2.0, 0.5, 2000)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+    scan_s = ev[0].elapsed_time(ev[1]) / 1e3 / args.steps
+    upd_us = ev[1].elapsed_time(ev[2]) * 1e3 / args.steps
+    gbs = n * 2 / scan_s / 1e9
+    pk, pk_kind = peaks()
+    print(json.dumps({
+        "metric": "loss-scale step: inf/NaN scan GB/s over a bf16 layer output; us per scale update",
+        "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(scan_s * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic N(0,1)",
+        "config": {"workload": "amp_scan_bf16_34502x4096", "bytes_per_scan": n * 2,
+                   "l2": "two 283 MB buffers alternated (> 129 MiB L2)", "update_us_per_call": round(upd_us, 2)},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": f"{pk_kind} copy bandwidth (read + write); the scan only reads"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -467,14 +513,18 @@ def main(argv=None):
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--permute-out", action="store_true")
     ap.add_argument("--path", default="default", choices=["default", "fused", "split", "split_runs"])
-    ap.add_argument("--tiles", default="default", choices=["default", "single", "pair"])
+    ap.add_argument("--tiles", default="default", choices=["default", "single", "pair", "pair_k64"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--op", default="gemm", choices=["gemm", "amp"],
+                    help="gemm: the hot path (default); amp: the loss-scale step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "amp":
+        run_amp(args)
     else:
         run_gpu(args)
     if torch.distributed.is_initialized():

@@ -78,7 +78,7 @@ typedef enum {
                                   scratch than the library's static array holds */
 } a2av_status;
 
-typedef enum { A2AV_BF16 = 0, A2AV_FP16 = 1 } a2av_dtype;
+typedef enum { A2AV_BF16 = 0, A2AV_FP16 = 1, A2AV_FP32 = 2 /* a2av_found_nonfinite only */ } a2av_dtype;
 
 /* Execution path.  All give bitwise-identical outputs. */
 typedef enum {
@@ -95,7 +95,10 @@ typedef enum {
 typedef enum {
     A2AV_TILES_DEFAULT = 0,    /* the faster shape for this build */
     A2AV_TILES_SINGLE = 1,     /* 128-row tiles, one CTA each */
-    A2AV_TILES_PAIR = 2        /* 256-row tiles on a cluster of two CTAs */
+    A2AV_TILES_PAIR = 2,       /* 256-row tiles on a cluster of two CTAs; pipeline stages
+                                  128 deep in K where H1, H2 are multiples of 128 and the
+                                  weight columns load in whole 64-wide atoms */
+    A2AV_TILES_PAIR_K64 = 3    /* 256-row tiles, stages always 64 deep in K */
 } a2av_tiles;
 
 typedef struct {
@@ -185,6 +188,32 @@ a2av_status a2av_gmm_run_static_scratch(const a2av_gmm_desc *desc, const void *a
                                         const void *mmX, const void *mmWeight,
                                         void *permuteOut, void *gmmY, void *mmY,
                                         a2av_stream_t stream);
+
+/*
+ * Dynamic loss-scale update ("aclnnAmpUpdateScale" page, "Formula" and its
+ * notes), in place on device scalars, enqueued on `stream`:
+ *   *found_inf != 0                  -> *scale *= backoff_factor, *tracker = 0
+ *   else *tracker + 1 == interval    -> grown = *scale * growth_factor;
+ *                                       *scale = grown if finite (else kept);
+ *                                       *tracker = 0
+ *   else                             -> *tracker += 1
+ * scale and found_inf are float32 (the page requires one type for both),
+ * growth_tracker int32.  Products are float32, rounded to nearest.
+ * Returns A2AV_ERR_NULLPTR for a NULL pointer, A2AV_ERR_INVALID for
+ * growth_interval < 1 (the page's range is [1, 2147483647]).
+ */
+a2av_status a2av_amp_update_scale(float *scale, int32_t *growth_tracker, const float *found_inf,
+                                  float growth_factor, float backoff_factor,
+                                  int32_t growth_interval, a2av_stream_t stream);
+
+/*
+ * Sets *found_inf = 1.0f when any of the n elements of x (device, a2av_dtype:
+ * bf16, fp16 or fp32) is inf or NaN, and leaves it unchanged otherwise, so
+ * several tensors can be checked into one flag before a2av_amp_update_scale.
+ * x must be 16-byte aligned.  Enqueued on `stream`.
+ */
+a2av_status a2av_found_nonfinite(const void *x, int64_t n, int32_t dtype, float *found_inf,
+                                 a2av_stream_t stream);
 
 /* A static, human-readable name for a status code. */
 const char *a2av_gmm_status_string(a2av_status status);

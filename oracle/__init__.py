@@ -8,7 +8,8 @@ The arithmetic lives in ``a2av_ref.c`` (plain C, double accumulation, OpenMP
 over output rows); this module builds it with gcc and wraps it with ctypes.
 It follows the "Formula" section of the aclnnAlltoAllvGroupedMatMul page:
 permuteOut = Permute(ataOut), gmmY = permuteOut x gmmWeight (one weight
-matrix per local expert), mmY = mmX x mmWeight.
+matrix per local expert), mmY = mmX x mmWeight; and the "Formula" of the
+aclnnAmpUpdateScale page for the dynamic loss-scale update.
 
 Every function is pinned by tests/test_oracle_pins.py; no function here is
 "parity unpinned".
@@ -53,8 +54,11 @@ def _declare(lib):
     lib.a2av_ref_grouped_matmul.argtypes = [i32, p, i64, i64, i64, i32, p, p, p, i64, p]
     lib.a2av_ref_matmul.argtypes = [i64, i64, i64, i32, p, p, p, i64, p]
     lib.a2av_ref_num_threads.argtypes = []
+    lib.a2av_ref_amp_update_scale.argtypes = [p, p, ctypes.c_float, ctypes.c_float, ctypes.c_float, i32]
+    lib.a2av_ref_any_nonfinite.argtypes = [ctypes.c_int, p, i64, p]
     for f in ("a2av_ref_decode", "a2av_ref_plan", "a2av_ref_permute",
-              "a2av_ref_grouped_matmul", "a2av_ref_matmul", "a2av_ref_num_threads"):
+              "a2av_ref_grouped_matmul", "a2av_ref_matmul", "a2av_ref_num_threads",
+              "a2av_ref_amp_update_scale", "a2av_ref_any_nonfinite"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -151,6 +155,23 @@ class Oracle:
         _check(self.L.a2av_ref_matmul(BS, H2, N2, DTYPE_CODE[mmX.dtype], _ptr(_bits(mmX)),
                                       _ptr(_bits(mmWeight)), _ptr(rl), n, _ptr(out)), "matmul")
         return out
+
+    def amp_update_scale(self, scale: float, growth_tracker: int, found_inf: float, growth_factor: float,
+                         backoff_factor: float, growth_interval: int):
+        """Page "aclnnAmpUpdateScale": returns (updated_scale, updated_tracker), float32 arithmetic."""
+        sc = ctypes.c_float(scale)
+        tr = ctypes.c_int32(growth_tracker)
+        _check(self.L.a2av_ref_amp_update_scale(ctypes.byref(sc), ctypes.byref(tr), found_inf, growth_factor,
+                                                backoff_factor, growth_interval), "amp_update_scale")
+        return sc.value, tr.value
+
+    def any_nonfinite(self, t: torch.Tensor) -> bool:
+        code = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}[t.dtype]
+        b = t.contiguous().reshape(-1)
+        found = ctypes.c_int32(0)
+        _check(self.L.a2av_ref_any_nonfinite(code, b.data_ptr() if b.numel() else None, b.numel(),
+                                             ctypes.byref(found)), "any_nonfinite")
+        return bool(found.value)
 
     def run(self, W: int, e: int, recvCounts, ataOut, gmmWeight, mmX=None, mmWeight=None,
             gmm_rows=None, mm_rows=None):

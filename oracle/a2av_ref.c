@@ -315,3 +315,58 @@ int a2av_ref_num_threads(void)
     return 1;
 #endif
 }
+
+/* ---- AMP dynamic loss scale (page "aclnnAmpUpdateScale") ---------------
+ *
+ * "Formula" of that page, with its four explanatory notes and the
+ * "Inf/NaN priority" and "overflow protection" constraints:
+ *   found_inf != 0                      -> scale * backoff_factor, tracker = 0
+ *   else tracker + 1 == growth_interval -> new = scale * growth_factor;
+ *                                          scale = new if new is finite (else
+ *                                          unchanged); tracker = 0 either way
+ *   else                                -> scale unchanged, tracker + 1
+ * The page requires current_scale and found_inf of one floating type; this
+ * oracle takes float32 for both (the products are float32 products).
+ * Returns REF_BAD_ARG for growth_interval < 1 (page: [1, 2147483647]).
+ */
+int a2av_ref_amp_update_scale(float *scale, int32_t *growth_tracker, float found_inf,
+                              float growth_factor, float backoff_factor, int32_t growth_interval)
+{
+    if (!scale || !growth_tracker || growth_interval < 1)
+        return REF_BAD_ARG;
+    if (found_inf != 0.0f) {            /* NaN != 0 is true: NaN counts as found */
+        *scale = *scale * backoff_factor;
+        *growth_tracker = 0;
+    } else if (*growth_tracker + 1 == growth_interval) {
+        float grown = *scale * growth_factor;
+        if (isfinite(grown))
+            *scale = grown;
+        *growth_tracker = 0;
+    } else {
+        *growth_tracker = *growth_tracker + 1;
+    }
+    return REF_OK;
+}
+
+/* 1 when any of the n values (dtype 0 bf16, 1 fp16, 2 fp32) is inf or NaN. */
+int a2av_ref_any_nonfinite(int dtype, const void *x, int64_t n, int32_t *found)
+{
+    if (!found || n < 0 || (n && !x) || dtype < 0 || dtype > 2)
+        return REF_BAD_ARG;
+    *found = 0;
+    for (int64_t i = 0; i < n && !*found; ++i) {
+        double v;
+        if (dtype == 2) {
+            float f;
+            memcpy(&f, (const char *)x + 4 * i, 4);
+            v = f;
+        } else {
+            uint16_t b;
+            memcpy(&b, (const char *)x + 2 * i, 2);
+            v = dtype == 0 ? bf16_value(b) : fp16_value(b);
+        }
+        if (!isfinite(v))
+            *found = 1;
+    }
+    return REF_OK;
+}

@@ -8,9 +8,10 @@ integer cases, and brute force on tiny inputs.  The same pins run against
 deliberately broken builds of the oracle (test_oracle_mutants.py) to show
 that each plausible mistake is caught.
 
-Page cited throughout: "aclnnAlltoAllvGroupedMatMul", sections "Formula"
+Pages cited: "aclnnAlltoAllvGroupedMatMul", sections "Formula"
 (permuteOut = Permute(ataOut), gmmY = permuteOut x gmmWeight,
-mmY = mmX x mmWeight) and "Shape variables" (A = sum of recvCounts).
+mmY = mmX x mmWeight) and "Shape variables" (A = sum of recvCounts); and
+"aclnnAmpUpdateScale", "Formula" and its notes, for the loss-scale update.
 """
 
 from __future__ import annotations
@@ -299,6 +300,59 @@ def pin_shared_identity_and_integer_exact(orc):
     y = orc.matmul(torch.tensor(xi, dtype=torch.float64).to(torch.float16),
                    torch.tensor(wi, dtype=torch.float64).to(torch.float16))
     assert np.array_equal(y, (xi @ wi).astype(np.float64))
+
+
+# ---- AMP loss-scale update (page "aclnnAmpUpdateScale") ---------------------
+
+def pin_amp_update_golden(orc):
+    g = _golden("amp_update_scale.json")
+    for sc, tr, fi, gr, bo, iv, want_sc, want_tr in g["cases"]:
+        got_sc, got_tr = orc.amp_update_scale(sc, tr, fi, gr, bo, iv)
+        assert got_tr == want_tr, (sc, tr, fi, iv, got_tr)
+        assert np.float32(got_sc) == np.float32(want_sc), (sc, tr, fi, iv, got_sc)
+    c = g["nan_found_inf_case"]
+    got = orc.amp_update_scale(c["scale"], c["tracker"], float("nan"), c["growth"], c["backoff"], c["interval"])
+    assert got == (c["want_scale"], c["want_tracker"])
+
+
+def pin_amp_update_rejects_bad_interval(orc):
+    for iv in (0, -5):
+        try:
+            orc.amp_update_scale(1.0, 0, 0.0, 2.0, 0.5, iv)
+        except OracleError:
+            continue
+        raise AssertionError(f"growth_interval {iv} accepted")
+
+
+def pin_amp_update_matches_torch(orc):
+    # torch's own CPU routine for the same update, as a library check.
+    rng = np.random.default_rng(11)
+    for _ in range(400):
+        iv = int(rng.integers(1, 6))
+        tr = int(rng.integers(0, iv))
+        sc = float(np.float32(rng.choice([1.0, 65536.0, 3.0e38, 1e-30, 2.0 ** rng.integers(-20, 20)])))
+        fi = float(rng.choice([0.0, 0.0, 0.0, 1.0, float("inf"), float("nan")]))
+        gr, bo = float(rng.choice([2.0, 1.5, 1e10])), float(rng.choice([0.5, 0.25]))
+        ts = torch.tensor([sc], dtype=torch.float32)
+        tt = torch.tensor([tr], dtype=torch.int32)
+        torch._amp_update_scale_(ts, tt, torch.tensor([fi], dtype=torch.float32), gr, bo, iv)
+        got_sc, got_tr = orc.amp_update_scale(sc, tr, fi, gr, bo, iv)
+        assert got_tr == int(tt.item()), (sc, tr, fi, gr, bo, iv)
+        assert np.float32(got_sc).tobytes() == ts.numpy().tobytes(), (sc, tr, fi, gr, bo, iv, got_sc, ts)
+
+
+def pin_any_nonfinite(orc):
+    gen = torch.Generator().manual_seed(3)
+    for dtype in (torch.bfloat16, torch.float16, torch.float32):
+        x = torch.randn(1000, generator=gen).to(dtype)
+        assert not orc.any_nonfinite(x)
+        assert not orc.any_nonfinite(x[:0])
+        for bad in (float("inf"), float("-inf"), float("nan")):
+            y = x.clone()
+            y[int(torch.randint(0, 1000, (1,), generator=gen))] = bad
+            assert orc.any_nonfinite(y)
+        big = torch.full((10,), 6.0e4 if dtype == torch.float16 else 3.0e38, dtype=torch.float32).to(dtype)
+        assert not orc.any_nonfinite(big)  # large but finite
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

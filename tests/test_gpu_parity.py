@@ -16,7 +16,7 @@ from token_permute_grouped_gb300.workloads import WORKLOADS, SMALL, Inputs, cust
 pytestmark = pytest.mark.gpu
 
 PATHS = ["fused", "split", "split_runs"]
-TILES = ["single", "pair"]
+TILES = ["single", "pair", "pair_k64"]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -42,6 +42,15 @@ MUTANTS = {
     "sum_rule_not_checked": ("if (total != A)\n        return REF_BAD_COUNTS;", ""),
     "first_group_weight_for_all": (
         "(row_weight_index ? row_weight_index[r] : 0)", "0"),
+    "amp_tracker_kept_on_overflow": (
+        "            *scale = grown;\n        *growth_tracker = 0;",
+        "            *scale = grown;\n        else\n            *growth_tracker = *growth_tracker + 1;"),
+    "amp_growth_one_step_late": (
+        "} else if (*growth_tracker + 1 == growth_interval) {",
+        "} else if (*growth_tracker == growth_interval) {"),
+    "amp_backoff_keeps_tracker": (
+        "        *scale = *scale * backoff_factor;\n        *growth_tracker = 0;",
+        "        *scale = *scale * backoff_factor;"),
 }
 
 

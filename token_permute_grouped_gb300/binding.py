@@ -23,11 +23,12 @@ STATUS_NAMES = {0: "A2AV_OK", 1: "A2AV_ERR_NULLPTR", 2: "A2AV_ERR_INVALID", 3: "
 STATIC_SCRATCH_BYTES = 256 + (8 << 20)  # A2AV_STATIC_SCRATCH_BYTES
 DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 PATHS = {"default": 0, "fused": 1, "split": 2, "split_runs": 3}
-TILES = {"default": 0, "single": 1, "pair": 2}
+TILES = {"default": 0, "single": 1, "pair": 2, "pair_k64": 3}
 
 # Every symbol include/a2av_gmm.h declares.
 EXPORTS = ("a2av_gmm_workspace_size", "a2av_gmm_run", "a2av_gmm_read_device_status",
-           "a2av_gmm_status_string", "a2av_gmm_launch_count", "a2av_gmm_run_static_scratch")
+           "a2av_gmm_status_string", "a2av_gmm_launch_count", "a2av_gmm_run_static_scratch",
+           "a2av_amp_update_scale", "a2av_found_nonfinite")
 
 
 class A2avError(RuntimeError):
@@ -71,6 +72,10 @@ def load():
         L.a2av_gmm_launch_count.restype = i32
         L.a2av_gmm_run_static_scratch.argtypes = [ctypes.POINTER(Desc), p, p, p, p, p, p, p, p, p]
         L.a2av_gmm_run_static_scratch.restype = ctypes.c_int
+        L.a2av_amp_update_scale.argtypes = [p, p, p, ctypes.c_float, ctypes.c_float, i32, p]
+        L.a2av_amp_update_scale.restype = ctypes.c_int
+        L.a2av_found_nonfinite.argtypes = [p, ctypes.c_int64, i32, p, p]
+        L.a2av_found_nonfinite.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -121,6 +126,31 @@ def a2av_gmm_run_static_scratch(desc: Desc, ataOut, recvCounts, gmmWeight, mmX, 
     return int(load().a2av_gmm_run_static_scratch(
         ctypes.byref(desc), _ptr(ataOut), _ptr(recvCounts), _ptr(gmmWeight), _ptr(mmX), _ptr(mmWeight),
         _ptr(permuteOut), _ptr(gmmY), _ptr(mmY), ctypes.c_void_p(s.cuda_stream)))
+
+
+def a2av_amp_update_scale(scale: torch.Tensor, growth_tracker: torch.Tensor, found_inf: torch.Tensor,
+                          growth_factor: float, backoff_factor: float, growth_interval: int, stream=None) -> None:
+    """In place on device scalars: scale (float32 [1]), growth_tracker (int32 [1]), found_inf (float32 [1])."""
+    _check(scale, "scale", torch.float32)
+    _check(growth_tracker, "growth_tracker", torch.int32)
+    _check(found_inf, "found_inf", torch.float32)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = load().a2av_amp_update_scale(_ptr(scale), _ptr(growth_tracker), _ptr(found_inf), growth_factor,
+                                      backoff_factor, growth_interval, ctypes.c_void_p(s.cuda_stream))
+    if st != A2AV_OK:
+        raise A2avError(st, "a2av_amp_update_scale")
+
+
+def a2av_found_nonfinite(x: torch.Tensor, found_inf: torch.Tensor, stream=None) -> None:
+    """found_inf (float32 [1], device) = 1 when x holds an inf or NaN; unchanged otherwise."""
+    code = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}[x.dtype]
+    _check(x, "x")
+    _check(found_inf, "found_inf", torch.float32)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = load().a2av_found_nonfinite(_ptr(x) if x.numel() else None, x.numel(), code, _ptr(found_inf),
+                                     ctypes.c_void_p(s.cuda_stream))
+    if st != A2AV_OK:
+        raise A2avError(st, "a2av_found_nonfinite")
 
 
 def a2av_gmm_read_device_status(workspace: torch.Tensor, stream=None) -> tuple[int, int]:

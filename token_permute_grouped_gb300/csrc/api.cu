@@ -38,7 +38,7 @@ a2av_status validate(const a2av_gmm_desc *d) {
     }
     if (d->dtype != A2AV_BF16 && d->dtype != A2AV_FP16) return A2AV_ERR_INVALID;
     if (d->path < A2AV_PATH_DEFAULT || d->path > A2AV_PATH_SPLIT_RUNS) return A2AV_ERR_INVALID;
-    if (d->tiles < A2AV_TILES_DEFAULT || d->tiles > A2AV_TILES_PAIR) return A2AV_ERR_INVALID;
+    if (d->tiles < A2AV_TILES_DEFAULT || d->tiles > A2AV_TILES_PAIR_K64) return A2AV_ERR_INVALID;
     if (!mult8(d->H1) || !mult8(d->N1)) return A2AV_ERR_UNSUPPORTED;
     if (d->BS > 0 && (!mult8(d->H2) || !mult8(d->N2))) return A2AV_ERR_UNSUPPORTED;
     return A2AV_OK;
@@ -140,18 +140,33 @@ bool make_weight_map(CUtensorMap *m, const void *ptr, int64_t groups, int64_t K,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [rows, cols] seen as 3-D {64 columns, rows, cols / 64 chunks}; box = 64
+// columns x 128 rows x 2 chunks: one load brings 128 of K as two 16 KB
+// K-major swizzled sub-tiles.  Needs cols % 128 == 0.
+bool make_rows_map_chunks(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int32_t dtype) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols * 2), 128};
+    cuuint32_t box[3] = {64, kBM, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, tmap_type(dtype), 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The same weights seen as 4-D: [groups][N / 64 atoms][K][64 columns], box =
-// 64 columns x 64 K rows x `atoms` atoms.  One load then fills a stage's
-// weight columns in the layout of consecutive 64-column atoms (8 KB apart),
-// the same bytes as `atoms` loads of the 3-D map.  Needs N % 64 == 0.
+// 64 columns x kbox K rows x `atoms` atoms.  One load then fills a stage's
+// weight columns in the layout of consecutive 64-column atoms (kbox * 128 B
+// apart), the same bytes as `atoms` loads of the 3-D map.  Needs N % 64 == 0.
 bool make_weight_map_atoms(CUtensorMap *m, const void *ptr, int64_t groups, int64_t K, int64_t N,
-                           int32_t dtype, uint32_t atoms) {
+                           int32_t dtype, uint32_t atoms, uint32_t kbox) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N / 64),
                           static_cast<cuuint64_t>(groups)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(N * 2), 128, static_cast<cuuint64_t>(K * N * 2)};
-    cuuint32_t box[4] = {64, 64, atoms, 1};
+    cuuint32_t box[4] = {64, kbox, atoms, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(m, tmap_type(dtype), 4, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -258,20 +273,32 @@ a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const in
     g.ataOut = ataOut;
     g.permuteOut = split ? nullptr : perm_out;
 
+    // One-load weight stages where the columns come in whole 64-wide atoms;
+    // two-chunk (128-deep) stages on CTA pairs where, in addition, both K's
+    // are multiples of 128 and A is TMA-fed (not row-gathered).
+    const int cta_cols = use_pair(&d) ? 2 : 1;
+    const bool b4r = d.N1 % 64 == 0 && (g.bn1 / cta_cols) % 64 == 0;
+    const bool b4s = has_shared && d.N2 % 64 == 0 && (g.bn2 / cta_cols) % 64 == 0;
+    const bool wide = use_pair(&d) && d.tiles != A2AV_TILES_PAIR_K64 && split && b4r &&
+                      (!has_shared || b4s) && d.H1 % 128 == 0 && (!has_shared || d.H2 % 128 == 0);
+    g.kchunks = wide ? 2 : 1;
+    const uint32_t kbox = wide ? 128 : 64;
+    auto rows_map = [&](CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols) {
+        return wide ? make_rows_map_chunks(m, ptr, rows, cols, d.dtype) : make_rows_map(m, ptr, rows, cols, d.dtype);
+    };
     if (!make_weight_map(&g.tmB_routed, gmmWeight, d.e, d.H1, d.N1, d.dtype)) return A2AV_ERR_CUDA;
     if (has_shared) {
-        if (!make_rows_map(&g.tmA_shared, mmX, d.BS, d.H2, d.dtype)) return A2AV_ERR_CUDA;
+        if (!rows_map(&g.tmA_shared, mmX, d.BS, d.H2)) return A2AV_ERR_CUDA;
         if (!make_weight_map(&g.tmB_shared, mmWeight, 1, d.H2, d.N2, d.dtype)) return A2AV_ERR_CUDA;
     }
-    // One-load weight stages where the columns come in whole 64-wide atoms.
-    const int cta_cols = use_pair(&d) ? 2 : 1;
-    if (d.N1 % 64 == 0 && (g.bn1 / cta_cols) % 64 == 0) {
-        if (!make_weight_map_atoms(&g.tmB4_routed, gmmWeight, d.e, d.H1, d.N1, d.dtype, g.bn1 / cta_cols / 64))
+    if (b4r) {
+        if (!make_weight_map_atoms(&g.tmB4_routed, gmmWeight, d.e, d.H1, d.N1, d.dtype, g.bn1 / cta_cols / 64,
+                                   kbox))
             return A2AV_ERR_CUDA;
         g.b4_routed = 1;
     }
-    if (has_shared && d.N2 % 64 == 0 && (g.bn2 / cta_cols) % 64 == 0) {
-        if (!make_weight_map_atoms(&g.tmB4_shared, mmWeight, 1, d.H2, d.N2, d.dtype, g.bn2 / cta_cols / 64))
+    if (b4s) {
+        if (!make_weight_map_atoms(&g.tmB4_shared, mmWeight, 1, d.H2, d.N2, d.dtype, g.bn2 / cta_cols / 64, kbox))
             return A2AV_ERR_CUDA;
         g.b4_shared = 1;
     }
@@ -289,9 +316,9 @@ a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const in
                                    static_cast<int32_t>(d.H1), ataOut, dst, status, 1, partial};
             if (a2av::launch_permute(pl, sms, stream) != cudaSuccess) return A2AV_ERR_CUDA;
             permute_ran = true;
-            if (!make_rows_map(&g.tmA_routed, dst, d.A, d.H1, d.dtype)) return A2AV_ERR_CUDA;
+            if (!rows_map(&g.tmA_routed, dst, d.A, d.H1)) return A2AV_ERR_CUDA;
             if (partial) {
-                if (!make_rows_map(&g.tmA_direct, ataOut, d.A, d.H1, d.dtype)) return A2AV_ERR_CUDA;
+                if (!rows_map(&g.tmA_direct, ataOut, d.A, d.H1)) return A2AV_ERR_CUDA;
                 g.direct_halves = 1;
             }
         } else {
@@ -332,6 +359,32 @@ a2av_status a2av_gmm_run_static_scratch(const a2av_gmm_desc *desc, const void *a
     if (!scratch) return A2AV_ERR_CUDA;
     return a2av_gmm_run(desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permuteOut, gmmY, mmY, scratch,
                         A2AV_STATIC_SCRATCH_BYTES, stream);
+}
+
+a2av_status a2av_amp_update_scale(float *scale, int32_t *growth_tracker, const float *found_inf,
+                                  float growth_factor, float backoff_factor, int32_t growth_interval,
+                                  a2av_stream_t stream) {
+    if (!scale || !growth_tracker || !found_inf) return A2AV_ERR_NULLPTR;
+    if (growth_interval < 1) return A2AV_ERR_INVALID;
+    if (a2av::launch_amp_update_scale(scale, growth_tracker, found_inf, growth_factor, backoff_factor,
+                                      growth_interval, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return A2AV_ERR_CUDA;
+    return A2AV_OK;
+}
+
+a2av_status a2av_found_nonfinite(const void *x, int64_t n, int32_t dtype, float *found_inf,
+                                 a2av_stream_t stream) {
+    if (!found_inf || (n > 0 && !x)) return A2AV_ERR_NULLPTR;
+    if (n < 0 || dtype < A2AV_BF16 || dtype > A2AV_FP32) return A2AV_ERR_INVALID;
+    if (n == 0) return A2AV_OK;
+    if (!aligned16(x)) return A2AV_ERR_UNSUPPORTED;
+    const int sms = sm_count();
+    if (sms <= 0) return A2AV_ERR_CUDA;
+    const int64_t bytes = n * (dtype == A2AV_FP32 ? 4 : 2);
+    if (a2av::launch_nonfinite_scan(x, bytes, dtype, found_inf, sms, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return A2AV_ERR_CUDA;
+    return A2AV_OK;
 }
 
 a2av_status a2av_gmm_read_device_status(const void *workspace, a2av_stream_t stream, int32_t *code) {

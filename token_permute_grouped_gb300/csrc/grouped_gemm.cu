@@ -44,10 +44,8 @@ namespace a2av {
 
 namespace {
 
-constexpr int BM = 128;  // rows per CTA
-constexpr int BK = 64;
-constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
-constexpr uint32_t B_ATOM_BYTES = BK * 64 * 2;   // 64 K-rows x 64 N: 8 KB
+constexpr int BM = 128;      // rows per CTA
+constexpr int KCHUNK = 64;   // K elements in one 128-byte swizzle row
 constexpr int kProducerWarps = 4;
 constexpr int kMmaWarp = 4;
 constexpr int kThreads = 9 * 32;
@@ -55,13 +53,21 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-template <bool PAIR>
+// CH = 64-wide K chunks per pipeline stage (1 or 2).  With CH = 2 each stage
+// holds 128 of K in the same bytes-in-flight budget as twice as many CH = 1
+// stages, and is still one TMA load per operand: half the TMA instructions
+// per FLOP, the issue rate being what bounds the main loop.
+template <bool PAIR, int CH>
 struct Shape {
     static constexpr int kCtas = PAIR ? 2 : 1;
     static constexpr int TILE_M = BM * kCtas;
+    static constexpr int BK = KCHUNK * CH;                    // K per stage
+    static constexpr uint32_t A_SUB_BYTES = BM * KCHUNK * 2;  // 16 KB: 128 rows x one chunk
+    static constexpr uint32_t A_STAGE_BYTES = A_SUB_BYTES * CH;
+    static constexpr uint32_t B_ATOM_BYTES = BK * 64 * 2;     // BK K-rows x 64 N columns
     // Weight columns one CTA stages: bn (<= 256) or bn / 2 (<= 128).
     static constexpr uint32_t B_STAGE_BYTES = (PAIR ? 2 : 4) * B_ATOM_BYTES;
-    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int STAGES = (PAIR ? 6 : 4) / CH;
 };
 
 struct GroupInfo {
@@ -85,10 +91,10 @@ struct Control {
     SegmentTable seg;
 };
 
-template <bool PAIR>
+template <bool PAIR, int CH>
 constexpr size_t smem_bytes() {
-    return 1024 + Shape<PAIR>::STAGES * (A_STAGE_BYTES + Shape<PAIR>::B_STAGE_BYTES) +
-           sizeof(Control<Shape<PAIR>::STAGES>);
+    using S = Shape<PAIR, CH>;
+    return 1024 + S::STAGES * (S::A_STAGE_BYTES + S::B_STAGE_BYTES) + sizeof(Control<S::STAGES>);
 }
 
 struct Tile {
@@ -297,9 +303,13 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
     }
 }
 
-template <bool BF16, bool GATHER, bool PAIR>
+template <bool BF16, bool GATHER, bool PAIR, int CH>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmLaunch p) {
-    using S = Shape<PAIR>;
+    static_assert(CH == 1 || !GATHER, "row gathers use one-chunk stages");
+    using S = Shape<PAIR, CH>;
+    constexpr int BK = S::BK;
+    constexpr uint32_t A_STAGE_BYTES = S::A_STAGE_BYTES;
+    constexpr uint32_t B_ATOM_BYTES = S::B_ATOM_BYTES;
     constexpr int STAGES = S::STAGES;
     constexpr int TILE_M = S::TILE_M;
     constexpr int kCtas = S::kCtas;
@@ -472,11 +482,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         else if (box_level > 0)
                             tma_2d<PAIR>(a_st + lane * 512, &p.tmA_box[box_level - 1], fb, kb * BK, src[0]);
                     } else if (lane == 0) {
-                        if (direct)
-                            tma_2d<PAIR>(a_st, &p.tmA_direct, fb, kb * BK, direct_row);
-                        else
-                            tma_2d<PAIR>(a_st, shared ? &p.tmA_shared : &p.tmA_routed, fb, kb * BK,
-                                         shared ? w.m * TILE_M + static_cast<int>(rank) * BM : y);
+                        const CUtensorMap *ta = direct ? &p.tmA_direct : shared ? &p.tmA_shared : &p.tmA_routed;
+                        const int ya = direct ? direct_row : shared ? w.m * TILE_M + static_cast<int>(rank) * BM : y;
+                        if constexpr (CH == 1)
+                            tma_2d<PAIR>(a_st, ta, fb, kb * BK, ya);
+                        else  // 3-D view {64 columns, rows, K chunks}: CH chunks in one load
+                            tma_3d<PAIR>(a_st, ta, fb, 0, ya, kb * CH);
                     }
                     if (lane == 0) {
                         if (b4)  // all the stage's weight atoms in one load
@@ -564,8 +575,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     const uint64_t ad0 = a_desc0 + ((s * A_STAGE_BYTES) >> 4);
                     const uint64_t bd0 = b_desc0 + ((s * S::B_STAGE_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        mma<PAIR>(d_tmem, ad0 + 2 * kk, bd0 + 128 * kk, idesc, (kb | kk) != 0);
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // A: chunk kk / 4 (16 KB apart), 32 bytes per K step of 16 within it.
+                        const uint32_t a_off = ((kk >> 2) * S::A_SUB_BYTES + (kk & 3) * 32) >> 4;
+                        mma<PAIR>(d_tmem, ad0 + a_off, bd0 + 128 * kk, idesc, (kb | kk) != 0);
+                    }
                     commit<PAIR>(empty0 + s * sizeof(uint64_t));
                 }
                 if (ok) commit<PAIR>(smem_u32(&C.tfull[acc]));
@@ -630,10 +644,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
 }
 
-template <bool BF16, bool GATHER, bool PAIR>
+template <bool BF16, bool GATHER, bool PAIR, int CH>
 cudaError_t launch_variant(const GemmLaunch &p, cudaStream_t stream) {
-    auto kern = grouped_gemm_kernel<BF16, GATHER, PAIR>;
-    constexpr size_t smem = smem_bytes<PAIR>();
+    auto kern = grouped_gemm_kernel<BF16, GATHER, PAIR, CH>;
+    constexpr size_t smem = smem_bytes<PAIR, CH>();
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
@@ -644,7 +658,7 @@ cudaError_t launch_variant(const GemmLaunch &p, cudaStream_t stream) {
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = Shape<PAIR>::kCtas;
+    attr[0].val.clusterDim.x = Shape<PAIR, CH>::kCtas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -656,8 +670,8 @@ cudaError_t launch_variant(const GemmLaunch &p, cudaStream_t stream) {
 
 template <bool BF16, bool GATHER, bool PAIR>
 int max_units_for() {
-    auto kern = grouped_gemm_kernel<BF16, GATHER, PAIR>;
-    constexpr size_t smem = smem_bytes<PAIR>();
+    auto kern = grouped_gemm_kernel<BF16, GATHER, PAIR, 1>;
+    constexpr size_t smem = smem_bytes<PAIR, 1>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
         return 0;
@@ -667,7 +681,7 @@ int max_units_for() {
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = Shape<PAIR>::kCtas;
+    attr[0].val.clusterDim.x = Shape<PAIR, 1>::kCtas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -679,7 +693,7 @@ int max_units_for() {
 
 }  // namespace
 
-size_t grouped_gemm_smem_bytes(int pair) { return pair ? smem_bytes<true>() : smem_bytes<false>(); }
+size_t grouped_gemm_smem_bytes(int pair) { return pair ? smem_bytes<true, 1>() : smem_bytes<false, 1>(); }
 
 int grouped_gemm_max_coresident(int pair) {
     // Clusters (pair) or CTAs (single) that fit on the device at once.
@@ -688,8 +702,13 @@ int grouped_gemm_max_coresident(int pair) {
 
 cudaError_t launch_grouped_gemm(const GemmLaunch &p, cudaStream_t stream) {
     const bool pair = p.pair != 0;
+    if (p.kchunks == 2) {  // two-chunk stages: CTA pairs, TMA-fed A (no row gathers)
+        if (!pair || p.gather) return cudaErrorInvalidValue;
+        return p.bf16 ? launch_variant<true, false, true, 2>(p, stream)
+                      : launch_variant<false, false, true, 2>(p, stream);
+    }
 #define A2AV_LAUNCH(B, G)                                                                          \
-    (pair ? launch_variant<B, G, true>(p, stream) : launch_variant<B, G, false>(p, stream))
+    (pair ? launch_variant<B, G, true, 1>(p, stream) : launch_variant<B, G, false, 1>(p, stream))
     if (p.bf16) return p.gather ? A2AV_LAUNCH(true, true) : A2AV_LAUNCH(true, false);
     return p.gather ? A2AV_LAUNCH(false, true) : A2AV_LAUNCH(false, false);
 #undef A2AV_LAUNCH

@@ -39,6 +39,7 @@ struct GemmLaunch {
     const void *ataOut;   // for gather
     void *permuteOut;     // for gather: rows copied by warps 1-3 (may be NULL)
     int32_t pair;         // 1: 256-row tiles on CTA pairs (cta_group::2), 0: 128-row tiles
+    int32_t kchunks;      // 64-wide K chunks per stage: 1, or 2 (pair, TMA-fed A, maps below in 3-D/4-D)
     int32_t grid;         // persistent CTAs (pair: an even number, two per cluster)
     CUtensorMap tmA_routed;   // split: expert-major A, 128-row box; fused: ataOut, 1-row box (gather)
     CUtensorMap tmA_box[5];   // fused: ataOut with 8, 16, 32, 64, 128-row boxes (contiguous runs)
@@ -53,6 +54,12 @@ struct GemmLaunch {
 };
 
 cudaError_t launch_grouped_gemm(const GemmLaunch &p, cudaStream_t stream);
+
+// Dynamic loss scaling (amp.cu).
+cudaError_t launch_amp_update_scale(float *scale, int32_t *tracker, const float *found_inf, float growth,
+                                    float backoff, int32_t interval, cudaStream_t stream);
+cudaError_t launch_nonfinite_scan(const void *x, int64_t bytes, int dtype, float *found_inf, int num_sms,
+                                  cudaStream_t stream);
 size_t grouped_gemm_smem_bytes(int pair);
 int grouped_gemm_max_coresident(int pair);  // CTAs (single) or clusters (pair) resident at once
 
