@@ -8,8 +8,10 @@ The arithmetic lives in ``a2av_ref.c`` (plain C, double accumulation, OpenMP
 over output rows); this module builds it with gcc and wraps it with ctypes.
 It follows the "Formula" section of the aclnnAlltoAllvGroupedMatMul page:
 permuteOut = Permute(ataOut), gmmY = permuteOut x gmmWeight (one weight
-matrix per local expert), mmY = mmX x mmWeight; and the "Formula" of the
-aclnnAmpUpdateScale page for the dynamic loss-scale update.
+matrix per local expert), mmY = mmX x mmWeight; the "Formula" of the
+aclnnAmpUpdateScale page for the dynamic loss-scale update; and the
+"Formula" and "Constraints" of the aclnnQuantReduceScatter page for the
+dequantising reduce.
 
 Every function is pinned by tests/test_oracle_pins.py; no function here is
 "parity unpinned".
@@ -56,9 +58,12 @@ def _declare(lib):
     lib.a2av_ref_num_threads.argtypes = []
     lib.a2av_ref_amp_update_scale.argtypes = [p, p, ctypes.c_float, ctypes.c_float, ctypes.c_float, i32]
     lib.a2av_ref_any_nonfinite.argtypes = [ctypes.c_int, p, i64, p]
+    lib.a2av_ref_decode8.argtypes = [ctypes.c_int, p, i64, p]
+    lib.a2av_ref_quant_reduce.argtypes = [i32, i64, i64, i32, i32, p, p, p]
     for f in ("a2av_ref_decode", "a2av_ref_plan", "a2av_ref_permute",
               "a2av_ref_grouped_matmul", "a2av_ref_matmul", "a2av_ref_num_threads",
-              "a2av_ref_amp_update_scale", "a2av_ref_any_nonfinite"):
+              "a2av_ref_amp_update_scale", "a2av_ref_any_nonfinite", "a2av_ref_decode8",
+              "a2av_ref_quant_reduce"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -172,6 +177,24 @@ class Oracle:
         _check(self.L.a2av_ref_any_nonfinite(code, b.data_ptr() if b.numel() else None, b.numel(),
                                              ctypes.byref(found)), "any_nonfinite")
         return bool(found.value)
+
+    def decode8(self, kind: int, bits: np.ndarray) -> np.ndarray:
+        """kind 0 E4M3FN, 1 E5M2, 2 INT8, 3 E8M0 (bytes as uint8)."""
+        b = np.ascontiguousarray(bits, dtype=np.uint8)
+        out = np.empty(b.size, np.float64)
+        _check(self.L.a2av_ref_decode8(kind, _ptr(b) if b.size else None, b.size, _ptr(out)), "decode8")
+        return out.reshape(b.shape)
+
+    def quant_reduce(self, data: np.ndarray, scales: np.ndarray, qtype: int, mode: int) -> np.ndarray:
+        """Page "aclnnQuantReduceScatter": data [W, rows, H] uint8, scales [W, rows, H/32] uint8
+        (mode 0, E8M0) or [W, rows, H/128] float32 (mode 1); returns [rows, H] float64."""
+        W, rows, H = data.shape
+        d = np.ascontiguousarray(data, dtype=np.uint8)
+        sc = np.ascontiguousarray(scales)
+        out = np.empty((rows, H), np.float64)
+        _check(self.L.a2av_ref_quant_reduce(W, rows, H, qtype, mode, _ptr(d), _ptr(sc), _ptr(out)),
+               "quant_reduce")
+        return out
 
     def run(self, W: int, e: int, recvCounts, ataOut, gmmWeight, mmX=None, mmWeight=None,
             gmm_rows=None, mm_rows=None):

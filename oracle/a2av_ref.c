@@ -370,3 +370,107 @@ int a2av_ref_any_nonfinite(int dtype, const void *x, int64_t n, int32_t *found)
     }
     return REF_OK;
 }
+
+/* ---- Quantised reduce (page "aclnnQuantReduceScatter") -----------------
+ *
+ * "Formula": output = Reduce(AllToAllScales * AllToAllData), the Reduce
+ * running over the data received from the different ranks.  On this rank,
+ * after the AllToAll, data[w] and scales[w] are what source rank w sent:
+ *     out[i][h] = sum over w of value(data[w][i][h]) * scale(w, i, h)
+ * "Constraints": mx quantisation = FLOAT8_E4M3FN / FLOAT8_E5M2 data with
+ * FLOAT8_E8M0 scales, one per 32 elements along H (scalesDataSize =
+ * BS * H / 32 bytes); pertoken-pergroup = INT8 / FLOAT8 data with float
+ * scales, one per 128 elements along H (BS * H / 128 * 4 bytes).
+ * Summed in double, w ascending.
+ *
+ * qtype: 0 E4M3FN, 1 E5M2, 2 INT8.  mode: 0 mx (E8M0 per 32), 1 float per 128.
+ */
+
+/* FLOAT8_E4M3FN: 1 sign, 4 exponent (bias 7), 3 fraction bits; no
+ * infinities; S.1111.111 is NaN; exponent 0 encodes zero and subnormals. */
+static double e4m3_value(uint8_t b)
+{
+    int sign = b >> 7, expo = (b >> 3) & 0xf, frac = b & 7;
+    double v;
+    if (expo == 15 && frac == 7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)frac, -9);                   /* frac/8 * 2^(1-7) */
+    else
+        v = ldexp((double)(8 + frac), expo - 10);      /* (1 + frac/8) * 2^(expo-7) */
+    return sign ? -v : v;
+}
+
+/* FLOAT8_E5M2: 1 sign, 5 exponent (bias 15), 2 fraction bits, IEEE rules. */
+static double e5m2_value(uint8_t b)
+{
+    int sign = b >> 7, expo = (b >> 2) & 0x1f, frac = b & 3;
+    double v;
+    if (expo == 31)
+        v = frac ? NAN : INFINITY;
+    else if (expo == 0)
+        v = ldexp((double)frac, -16);                  /* frac/4 * 2^(1-15) */
+    else
+        v = ldexp((double)(4 + frac), expo - 17);      /* (1 + frac/4) * 2^(expo-15) */
+    return sign ? -v : v;
+}
+
+/* FLOAT8_E8M0: an unsigned power of two 2^(e - 127); 0xFF is NaN. */
+static double e8m0_value(uint8_t e)
+{
+    return e == 0xff ? NAN : ldexp(1.0, (int)e - 127);
+}
+
+static double q_value(int qtype, uint8_t b)
+{
+    if (qtype == 0)
+        return e4m3_value(b);
+    if (qtype == 1)
+        return e5m2_value(b);
+    return (double)(int8_t)b;
+}
+
+/* Decode n bytes of one 8-bit format (0 E4M3FN, 1 E5M2, 2 INT8, 3 E8M0). */
+int a2av_ref_decode8(int kind, const uint8_t *bits, int64_t n, double *out)
+{
+    if (kind < 0 || kind > 3 || n < 0 || (n && (!bits || !out)))
+        return REF_BAD_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kind == 3 ? e8m0_value(bits[i]) : q_value(kind, bits[i]);
+    return REF_OK;
+}
+
+int a2av_ref_quant_reduce(int32_t W, int64_t rows, int64_t H, int32_t qtype, int32_t mode,
+                          const uint8_t *data, const void *scales, double *out)
+{
+    if (W < 1 || rows < 0 || H < 1 || qtype < 0 || qtype > 2 || mode < 0 || mode > 1)
+        return REF_BAD_ARG;
+    if (mode == 0 && qtype == 2)
+        return REF_BAD_ARG;                            /* mx takes FLOAT8 data only */
+    const int64_t group = mode == 0 ? 32 : 128;
+    if (H % group)
+        return REF_BAD_ARG;
+    if (rows && (!data || !scales || !out))
+        return REF_BAD_ARG;
+    const int64_t ng = H / group;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < rows; ++i) {
+        for (int64_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int32_t w = 0; w < W; ++w) {
+                const int64_t row = (int64_t)w * rows + i;
+                double s;
+                if (mode == 0) {
+                    s = e8m0_value(((const uint8_t *)scales)[row * ng + h / group]);
+                } else {
+                    float f;
+                    memcpy(&f, (const char *)scales + 4 * (row * ng + h / group), 4);
+                    s = f;
+                }
+                acc += q_value(qtype, data[row * H + h]) * s;
+            }
+            out[i * H + h] = acc;
+        }
+    }
+    return REF_OK;
+}

@@ -355,4 +355,100 @@ def pin_any_nonfinite(orc):
         assert not orc.any_nonfinite(big)  # large but finite
 
 
+# ---- quantised reduce (page "aclnnQuantReduceScatter") -----------------------
+
+def pin_decode8_all_patterns(orc):
+    bits = np.arange(256, dtype=np.uint8)
+    t = torch.from_numpy(bits.copy())
+    for kind, want in ((0, t.view(torch.float8_e4m3fn).to(torch.float64)),
+                       (1, t.view(torch.float8_e5m2).to(torch.float64)),
+                       (2, t.view(torch.int8).to(torch.float64)),
+                       (3, t.view(torch.float8_e8m0fnu).to(torch.float64))):
+        got = orc.decode8(kind, bits)
+        w = want.numpy()
+        nan = np.isnan(w)
+        assert np.array_equal(np.isnan(got), nan), kind
+        assert np.array_equal(got[~nan], w[~nan]), kind
+
+
+def _qr_case(case):
+    W, rows, H = case["W"], case["rows"], case["H"]
+    data = np.zeros((W, rows, H), np.int64)
+    for w in range(W):
+        data[w, 0, :] = case["data_fill"][w]
+        data[w, 0, :4] = case["data_first4"][w]
+    return W, rows, H, data.astype(np.int8).view(np.uint8) if data.min() < 0 else data.astype(np.uint8)
+
+
+def pin_quant_reduce_golden(orc):
+    g = _golden("quant_reduce.json")
+    c = g["mx_e4m3"]
+    W, rows, H, data = _qr_case(c)
+    scales = np.array(c["scales"], np.uint8).reshape(W, rows, H // 32)
+    out = orc.quant_reduce(data, scales, 0, 0)
+    assert out[0, :4].tolist() == c["want_first4"] and (out[0, 4:] == c["want_fill"]).all()
+    c = g["pergroup_int8"]
+    W, rows, H, data = _qr_case(c)
+    scales = np.array(c["scales"], np.float32).reshape(W, rows, H // 128)
+    out = orc.quant_reduce(data, scales, 2, 1)
+    assert out[0, :4].tolist() == c["want_first4"] and (out[0, 4:] == c["want_fill"]).all()
+
+
+def pin_quant_reduce_single_rank_unit_scale(orc):
+    # One rank, scale 1 (E8M0 127, or 1.0f): the reduce is just the decode.
+    rng = np.random.default_rng(12)
+    data = rng.integers(0, 256, (1, 5, 256), dtype=np.uint8)
+    data[(data & 0x7F) == 0x7F] = 0  # no NaN codes
+    for q in (0, 1):
+        data_q = data.copy()
+        if q == 1:
+            data_q[(data_q & 0x7C) == 0x7C] = 0  # no inf/NaN codes
+        out = orc.quant_reduce(data_q, np.full((1, 5, 8), 127, np.uint8), q, 0)
+        assert np.array_equal(out, orc.decode8(q, data_q[0]))
+        out = orc.quant_reduce(data_q, np.ones((1, 5, 2), np.float32), q, 1)
+        assert np.array_equal(out, orc.decode8(q, data_q[0]))
+
+
+def pin_quant_reduce_scale_locality(orc):
+    # Every value 1.0 (E4M3 0x38, INT8 1) and one rank: each output is exactly
+    # the scale of its own (row, group), 2^(e - 127) for E8M0.
+    rng = np.random.default_rng(14)
+    rows, H = 3, 512
+    e = rng.integers(100, 150, (1, rows, H // 32), dtype=np.uint8)
+    out = orc.quant_reduce(np.full((1, rows, H), 0x38, np.uint8), e, 0, 0)
+    assert np.array_equal(out, np.repeat(2.0 ** (e[0].astype(np.float64) - 127), 32, axis=1))
+    f = rng.standard_normal((1, rows, H // 128)).astype(np.float32)
+    out = orc.quant_reduce(np.ones((1, rows, H), np.uint8), f, 2, 1)
+    assert np.array_equal(out, np.repeat(f[0].astype(np.float64), 128, axis=1))
+
+
+def pin_quant_reduce_linear_in_ranks(orc):
+    # Doubling rank w's scales adds exactly rank w's contribution once more;
+    # the rows and groups stay where they are.
+    rng = np.random.default_rng(13)
+    W, rows, H = 4, 6, 256
+    data = rng.integers(0, 127, (W, rows, H), dtype=np.uint8)  # positive E4M3 codes
+    scales = rng.integers(120, 135, (W, rows, H // 32), dtype=np.uint8)
+    base = orc.quant_reduce(data, scales, 0, 0)
+    for w in range(W):
+        s2 = scales.copy()
+        s2[w] += 1
+        one = np.zeros_like(scales)
+        one[w] = scales[w]
+        only_w = orc.quant_reduce(np.where(np.arange(W)[:, None, None] == w, data, 0).astype(np.uint8),
+                                  np.maximum(one, 1), 0, 0)
+        assert np.allclose(orc.quant_reduce(data, s2, 0, 0), base + only_w, rtol=1e-15, atol=0)
+
+
+def pin_quant_reduce_rejects_bad_modes(orc):
+    d = np.zeros((2, 1, 64), np.uint8)
+    for args in ((d, np.zeros((2, 1, 2), np.uint8), 2, 0),       # mx mode takes FLOAT8 only
+                 (d, np.zeros((2, 1, 1), np.float32), 0, 1)):    # H not a multiple of 128
+        try:
+            orc.quant_reduce(*args)
+        except OracleError:
+            continue
+        raise AssertionError("accepted")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -34,7 +34,9 @@ MUTANTS = {
     "fp16_exponent_bias_off_by_one": (
         "ldexp((double)(1024 + frac), expo - 25)",
         "ldexp((double)(1024 + frac), expo - 24)"),
-    "fp16_sign_dropped": ("return sign ? -v : v;", "return v;"),
+    "fp16_sign_dropped": (
+        "expo - 25);  /* (1 + frac/2^10) * 2^(expo-15) */\n    return sign ? -v : v;",
+        "expo - 25);  /* (1 + frac/2^10) * 2^(expo-15) */\n    return v;"),
     "accumulator_not_cleared": ("o[n] = 0.0;", "o[n] = (n == 0);"),
     "counts_read_expert_major": (
         "int32_t c = recvCounts[w * e + j];",
@@ -48,6 +50,13 @@ MUTANTS = {
     "amp_growth_one_step_late": (
         "} else if (*growth_tracker + 1 == growth_interval) {",
         "} else if (*growth_tracker == growth_interval) {"),
+    "e4m3_exponent_bias_off_by_one": (
+        "ldexp((double)(8 + frac), expo - 10)", "ldexp((double)(8 + frac), expo - 9)"),
+    "e8m0_bias_off_by_one": ("ldexp(1.0, (int)e - 127)", "ldexp(1.0, (int)e - 128)"),
+    "scale_group_index_wrong": ("[row * ng + h / group]);", "[row * ng + (h / group) / 2]);"),
+    "quant_reduce_drops_last_rank": (
+        "            for (int32_t w = 0; w < W; ++w) {\n                const int64_t row",
+        "            for (int32_t w = 0; w + 1 < W; ++w) {\n                const int64_t row"),
     "amp_backoff_keeps_tracker": (
         "        *scale = *scale * backoff_factor;\n        *growth_tracker = 0;",
         "        *scale = *scale * backoff_factor;"),
