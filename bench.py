@@ -70,11 +70,15 @@ def algorithmic_bytes(wl, A, permute_out):
     return b
 
 
+# The sources a permute + grouped-GEMM call depends on (kernels and host setup).
+GEMM_SOURCES = ("api.cu", "grouped_gemm.cu", "kernels.h", "permute.cu", "plan.cuh", "ptx.cuh")
+
+
 def source_hash():
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "token_permute_grouped_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + fh.read())
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "token_permute_grouped_gb300", "csrc", name), "rb") as fh:
+            h.update(name.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -505,6 +509,180 @@ def run_amp(args):
     }), flush=True)
 
 
+# ----------------------------------------------------------- quantised reduce
+
+QR_METRIC = "quantised rank reduce: algorithmic GB/s (8-bit codes + scales in, bf16 out)"
+
+
+def qreduce_bytes(wl):
+    """Algorithmic bytes of one call: every code and scale read once, the output written once."""
+    n = wl.W * wl.rows * wl.H
+    scale_bytes = n // 32 if wl.mode == "mx" else n // 128 * 4
+    return n + scale_bytes + wl.rows * wl.H * 2
+
+
+def qreduce_oracle_sample(wl, data, scales, seconds, seed=0):
+    """Oracle on seeded batches of output rows (rows reduce independently); returns
+    (algorithmic bytes covered, seconds, rows, threads, description)."""
+    import oracle
+    orc = oracle.Oracle()
+    rng = np.random.default_rng(seed)
+    qt = {"e4m3fn": 0, "e5m2": 1, "int8": 2}[wl.qtype]
+    mode = 0 if wl.mode == "mx" else 1
+    per_row = qreduce_bytes(wl) / wl.rows
+    chunk = max(orc.num_threads(), 8)
+    rows = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        idx = rng.integers(0, wl.rows, chunk)
+        orc.quant_reduce(np.ascontiguousarray(data[:, idx]), np.ascontiguousarray(scales[:, idx]), qt, mode)
+        rows += chunk
+    el = time.perf_counter() - t0
+    desc = (f"{rows} output rows drawn uniformly, with repeats, from the {wl.rows} rows of {wl.name} "
+            f"(float64 oracle)")
+    return per_row * rows, el, rows, orc.num_threads(), desc
+
+
+def run_qreduce(args):
+    """Dequantising rank reduce ("aclnnQuantReduceScatter" page), one launch per step, HBM-bound.
+    Under torchrun every rank reduces its own received data: weak scaling, no collective."""
+    from token_permute_grouped_gb300.workloads import QREDUCE_WORKLOADS, quant_reduce_inputs
+    world, rank, local = dist_env()
+    wl = QREDUCE_WORKLOADS[args.qworkload]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        data, scales = (t.numpy() for t in quant_reduce_inputs(wl.W, wl.rows, wl.H, wl.qtype, wl.mode, seed=0))
+        per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+        for _ in range(args.warmup):
+            qreduce_oracle_sample(wl, data, scales, per_step / 4)
+        tot_b = tot_s = 0.0
+        threads, desc = 1, ""
+        for i in range(args.steps):
+            b, sec, _, threads, desc = qreduce_oracle_sample(wl, data, scales, per_step, seed=i + 1)
+            tot_b += b
+            tot_s += sec
+        gbs = tot_b / tot_s / 1e9
+        print(json.dumps({
+            "impl": "reference", "metric": QR_METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s * 1e3 / max(1, args.steps), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "W": wl.W, "rows": wl.rows, "H": wl.H, "qtype": wl.qtype,
+                       "mode": wl.mode, "seconds_per_step": per_step},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0,
+        }), flush=True)
+        return
+    assert torch.cuda.is_available(), "bench.py needs a GPU (use --impl reference for the CPU oracle)"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    build.build()
+    binding.load()
+    data, scales = quant_reduce_inputs(wl.W, wl.rows, wl.H, wl.qtype, wl.mode, seed=rank)
+    nbytes = qreduce_bytes(wl)
+    reps = min(64, max(2, -(-3 * L2_BYTES // nbytes)))
+    sets = [(data.to(dev), scales.to(dev), torch.empty(wl.rows, wl.H, dtype=torch.bfloat16, device=dev))
+            for _ in range(reps)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        d, sc, o = sets[i % reps]
+        binding.a2av_quant_reduce(d, sc, wl.qtype, wl.mode, o, stream=stream)
+
+    sync = torch.cuda.synchronize
+    for i in range(args.warmup):
+        step(i)
+    sync()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def timed_step(i):
+        if i == 0:
+            ev[0].record(stream)
+        step(i)
+        if i == args.steps - 1:
+            ev[1].record(stream)
+
+    with ClockSampler(local) as clocks:
+        timed_region(timed_step, args.steps, world, dev, sync)
+    dev_s = ev[0].elapsed_time(ev[1]) / 1e3
+    dev_s_max = reduce_max(dev_s, world, dev)
+    gbs = reduce_sum(nbytes * args.steps, world, dev) / dev_s_max / 1e9
+
+    # End to end through the same call with host buffers: codes and scales in
+    # from pinned memory, the reduced rows back out, on copy streams that
+    # overlap the neighbouring steps' kernels (two device buffer sets).
+    pin_d, pin_s = data.pin_memory(), scales.pin_memory()
+    out_h = torch.empty(wl.rows, wl.H, dtype=torch.bfloat16).pin_memory()
+    h2d_b = pin_d.numel() + pin_s.numel() * pin_s.element_size()
+    d2h_b = out_h.numel() * 2
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    h2d_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    d2h_done = [torch.cuda.Event() for _ in range(2)]
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def issue_h2d(b):
+        with torch.cuda.stream(h2d_stream):
+            h2d_stream.wait_event(comp_done[b])
+            sets[b][0].copy_(pin_d, non_blocking=True)
+            sets[b][1].copy_(pin_s, non_blocking=True)
+            h2d_done[b].record(h2d_stream)
+
+    def e2e_step(i):
+        b = i % 2
+        if i == 0:
+            issue_h2d(0)
+        stream.wait_event(h2d_done[b])
+        stream.wait_event(d2h_done[b])
+        d, sc, o = sets[b]
+        binding.a2av_quant_reduce(d, sc, wl.qtype, wl.mode, o, stream=stream)
+        comp_done[b].record(stream)
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(comp_done[b])
+            out_h.copy_(o, non_blocking=True)
+            d2h_done[b].record(d2h_stream)
+        if i + 1 < e2e_steps:
+            issue_h2d(1 - b)
+
+    _, e2e_max = timed_region(e2e_step, e2e_steps, world, dev, sync)
+    e2e_gbs = reduce_sum(nbytes * e2e_steps, world, dev) / e2e_max / 1e9
+    if rank != 0:
+        barrier(world)
+        return
+    pk, pk_kind = peaks()
+    achieved = nbytes / (dev_s / args.steps) / 1e9
+    line = {
+        "metric": QR_METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dev_s_max * 1e3 / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded uniform finite codes, power-of-two or 2^u scales; no dataset)",
+        "config": {"workload": wl.name, "W": wl.W, "rows": wl.rows, "H": wl.H, "qtype": wl.qtype, "mode": wl.mode,
+                   "out": "bf16", "accumulate": "fp32", "bytes_per_call": nbytes,
+                   "us_per_call": round(dev_s / args.steps * 1e6, 2),
+                   "l2": (f"inputs rotated over {reps} replicas ({reps * nbytes / 2**20:.0f} MiB > 129 MiB L2)"
+                          if reps * nbytes > L2_BYTES else
+                          f"all {reps} replicas ({reps * nbytes / 2**20:.0f} MiB) fit in L2: a latency-bound case")},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None, "kernel": "quant_reduce_kernel",
+                     "peak_source": f"{pk_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if pk_kind == "measured"
+                     else "fallback 6.8 TB/s", "algorithmic_bytes": nbytes},
+        "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d_b),
+                "d2h_bytes_per_step": int(d2h_b), "steps": e2e_steps,
+                "inputs_copied": "codes and scales from pinned host memory; output read back"},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        b, sec, _, threads, desc = qreduce_oracle_sample(wl, data.numpy(), scales.numpy(), args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(b / sec / 1e9, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": desc, "seconds": round(sec, 2)}
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -515,13 +693,17 @@ def main(argv=None):
     ap.add_argument("--path", default="default", choices=["default", "fused", "split", "split_runs"])
     ap.add_argument("--tiles", default="default", choices=["default", "single", "pair", "pair_k64"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="gemm", choices=["gemm", "amp"],
-                    help="gemm: the hot path (default); amp: the loss-scale step")
+    ap.add_argument("--op", default="gemm", choices=["gemm", "amp", "qreduce"],
+                    help="gemm: the hot path (default); amp: the loss-scale step; qreduce: the quantised rank reduce")
+    ap.add_argument("--qworkload", default="qreduce_mx_e4m3_w8_rows1536_h7168",
+                    help="workload of --op qreduce")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
-    if args.impl == "reference":
+    if args.op == "qreduce":
+        run_qreduce(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.op == "amp":
         run_amp(args)

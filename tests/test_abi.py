@@ -4,6 +4,7 @@ No GPU needed: every call here returns before the library touches CUDA.
 """
 
 import ctypes
+import glob
 import os
 import re
 import subprocess
@@ -14,7 +15,7 @@ import torch
 from token_permute_grouped_gb300 import binding, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "a2av_gmm.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 @pytest.fixture(scope="module")
@@ -24,7 +25,7 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(a2av_\w+)\s*\(", text)))
 
@@ -131,6 +132,30 @@ def test_phase2_argument_checks(lib):
     d = binding.make_desc(8, 4, 0, 512, 256, path="split")
     d2 = binding.make_desc(8, 4, 0, 512, 256, 64, 128, 64)
     assert _run(lib, d2, mmY=0) == 1
+
+
+def qr(lib, W=8, rows=16, H=1024, qtype=0, mode=0, out_dtype=0, data=0x10000, scales=0x20000, out=0x30000):
+    return lib.a2av_quant_reduce(W, rows, H, qtype, mode, ctypes.c_void_p(data), ctypes.c_void_p(scales),
+                                 ctypes.c_void_p(out), out_dtype, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"data": 0}, 1),
+    ({"scales": 0}, 1),
+    ({"out": 0}, 1),
+    ({"W": 1}, 2), ({"W": 3}, 2), ({"W": 16}, 2),         # communicator size 2, 4 or 8
+    ({"rows": 0}, 2),                                       # no empty tensors
+    ({"H": 896}, 2), ({"H": 8320}, 2), ({"H": 1088}, 2),  # H in [1024, 8192], 128-aligned
+    ({"qtype": 3}, 2), ({"qtype": -1}, 2),
+    ({"mode": 2}, 2),
+    ({"qtype": 2, "mode": 0}, 2),                           # mx quantisation takes FLOAT8 data only
+    ({"out_dtype": 3}, 2),
+    ({"data": 0x10008}, 3),                                 # data and out 16-byte aligned
+    ({"out": 0x30004}, 3),
+    ({"mode": 1, "scales": 0x20002}, 3),                    # float scales 4-byte aligned
+])
+def test_quant_reduce_argument_checks(lib, kw, status):
+    assert qr(lib, **kw) == status
 
 
 def test_status_strings(lib):

@@ -25,10 +25,14 @@ DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 PATHS = {"default": 0, "fused": 1, "split": 2, "split_runs": 3}
 TILES = {"default": 0, "single": 1, "pair": 2, "pair_k64": 3}
 
-# Every symbol include/a2av_gmm.h declares.
+# Every function the headers under include/ declare.
 EXPORTS = ("a2av_gmm_workspace_size", "a2av_gmm_run", "a2av_gmm_read_device_status",
            "a2av_gmm_status_string", "a2av_gmm_launch_count", "a2av_gmm_run_static_scratch",
-           "a2av_amp_update_scale", "a2av_found_nonfinite")
+           "a2av_amp_update_scale", "a2av_found_nonfinite", "a2av_quant_reduce")
+
+# a2av_qtype / a2av_qmode of include/a2av_quant_reduce.h.
+QTYPES = {"e4m3fn": 0, "e5m2": 1, "int8": 2}
+QMODES = {"mx": 0, "group128": 1}
 
 
 class A2avError(RuntimeError):
@@ -76,6 +80,8 @@ def load():
         L.a2av_amp_update_scale.restype = ctypes.c_int
         L.a2av_found_nonfinite.argtypes = [p, ctypes.c_int64, i32, p, p]
         L.a2av_found_nonfinite.restype = ctypes.c_int
+        L.a2av_quant_reduce.argtypes = [i32, ctypes.c_int64, ctypes.c_int64, i32, i32, p, p, p, i32, p]
+        L.a2av_quant_reduce.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -151,6 +157,27 @@ def a2av_found_nonfinite(x: torch.Tensor, found_inf: torch.Tensor, stream=None) 
                                      ctypes.c_void_p(s.cuda_stream))
     if st != A2AV_OK:
         raise A2avError(st, "a2av_found_nonfinite")
+
+
+def a2av_quant_reduce(data: torch.Tensor, scales: torch.Tensor, qtype: str, mode: str,
+                      out: torch.Tensor, stream=None) -> torch.Tensor:
+    """out [rows, H] = sum over w of decode(data[w]) * scales[w] ("aclnnQuantReduceScatter" page,
+    Formula).  data: uint8 [W, rows, H] codes of qtype ("e4m3fn", "e5m2", "int8"); scales: uint8
+    E8M0 [W, rows, H/32] for mode "mx", float32 [W, rows, H/128] for "group128"; out: bf16, fp16
+    or fp32 [rows, H]."""
+    _check(data, "data", torch.uint8, 3)
+    _check(scales, "scales", torch.uint8 if mode == "mx" else torch.float32, 3)
+    _check(out, "out", None, 2)
+    W, rows, H = data.shape
+    if tuple(out.shape) != (rows, H):
+        raise ValueError(f"out must be [{rows}, {H}], got {tuple(out.shape)}")
+    code = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}[out.dtype]
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = load().a2av_quant_reduce(W, rows, H, QTYPES[qtype], QMODES[mode], _ptr(data), _ptr(scales),
+                                  _ptr(out), code, ctypes.c_void_p(s.cuda_stream))
+    if st != A2AV_OK:
+        raise A2avError(st, "a2av_quant_reduce")
+    return out
 
 
 def a2av_gmm_read_device_status(workspace: torch.Tensor, stream=None) -> tuple[int, int]:

@@ -256,3 +256,77 @@ def random_counts(W: int, e: int, A: int, seed: int, zero_prob: float = 0.0) -> 
     if A:
         rc = rng.multinomial(A, p / p.sum())
     return rc.astype(np.int32)
+
+
+# --- Quantised reduce ("aclnnQuantReduceScatter" page) -----------------------
+#
+# After the AllToAll, a rank holds from each of W source ranks `rows` rows of
+# H 8-bit codes plus their scales.  The page fixes the formats and limits
+# (W in {2, 4, 8}, H a multiple of 128 in [1024, 8192]) but not the values:
+# codes are drawn uniformly from the format's finite codes, and scales are
+# powers of two (E8M0 codes, mx mode) or float32 2^u with u uniform (per-128
+# groups), both over the same exponent range.
+
+STREAM_QDATA = 5
+STREAM_QSCALES = 6
+
+QTYPE_NAMES = ("e4m3fn", "e5m2", "int8")
+QMODE_NAMES = ("mx", "group128")
+
+
+@dataclasses.dataclass(frozen=True)
+class QuantReduceWorkload:
+    name: str
+    W: int
+    rows: int   # rows received from each source rank (BS / W)
+    H: int
+    qtype: str  # "e4m3fn", "e5m2" or "int8"
+    mode: str   # "mx" (E8M0 scales per 32) or "group128" (float32 scales per 128)
+
+
+# BS = 12288 tokens of H = 7168 on W = 8 ranks: x is 88 MB per rank, inside the
+# page's default 200 MB communication buffer (HCCL_BUFFSIZE >= 2 (x + scales + 1) MB).
+QREDUCE_WORKLOADS = {
+    w.name: w
+    for w in (
+        QuantReduceWorkload("qreduce_mx_e4m3_w8_rows1536_h7168", 8, 1536, 7168, "e4m3fn", "mx"),
+        QuantReduceWorkload("qreduce_g128_int8_w8_rows1536_h7168", 8, 1536, 7168, "int8", "group128"),
+        QuantReduceWorkload("qreduce_mx_e5m2_w4_rows2048_h4096", 4, 2048, 4096, "e5m2", "mx"),
+        QuantReduceWorkload("qreduce_mx_e5m2_w2_rows64_h1024", 2, 64, 1024, "e5m2", "mx"),
+    )
+}
+QREDUCE_HEADLINE = "qreduce_mx_e4m3_w8_rows1536_h7168"
+
+
+def finite_codes(qtype: str) -> np.ndarray:
+    """The 8-bit codes of a format that encode finite numbers (by bit pattern only)."""
+    codes = np.arange(256, dtype=np.uint8)
+    if qtype == "e4m3fn":
+        return codes[(codes & 0x7F) != 0x7F]            # S.1111.111 is NaN
+    if qtype == "e5m2":
+        return codes[(codes & 0x7C) != 0x7C]            # exponent field all ones: inf/NaN
+    return codes
+
+
+def quant_reduce_inputs(W: int, rows: int, H: int, qtype: str, mode: str, seed: int = 0,
+                        exp_range=(-10, 6)) -> tuple[torch.Tensor, torch.Tensor]:
+    """(data uint8 [W, rows, H], scales) on the CPU: E8M0 codes uint8 [W, rows, H/32] for
+    mode "mx", float32 [W, rows, H/128] for "group128"; scale exponents in exp_range."""
+    n = W * rows * H
+    allowed = finite_codes(qtype)
+    data = np.empty(n, dtype=np.uint8)
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+
+    def fill(i: int) -> None:
+        s, t = i * _CHUNK, min(n, (i + 1) * _CHUNK)
+        data[s:t] = allowed[_rng(seed, STREAM_QDATA, i).integers(0, len(allowed), t - s)]
+
+    with ThreadPoolExecutor(max(1, min(nchunks, os.cpu_count() or 1))) as ex:
+        list(ex.map(fill, range(nchunks)))
+    lo, hi = exp_range
+    rng = _rng(seed, STREAM_QSCALES)
+    if mode == "mx":
+        sc = (rng.integers(lo, hi + 1, W * rows * (H // 32)) + 127).astype(np.uint8).reshape(W, rows, H // 32)
+    else:
+        sc = np.exp2(rng.uniform(lo, hi, W * rows * (H // 128))).astype(np.float32).reshape(W, rows, H // 128)
+    return torch.from_numpy(data.reshape(W, rows, H)), torch.from_numpy(sc)
