@@ -70,30 +70,33 @@ def algorithmic_bytes(wl, A, permute_out):
     return b
 
 
-# The sources a permute + grouped-GEMM call depends on (kernels and host setup).
+# The sources each measured call depends on (kernels and host setup).
 GEMM_SOURCES = ("api.cu", "grouped_gemm.cu", "kernels.h", "permute.cu", "plan.cuh", "ptx.cuh")
+QREDUCE_SOURCES = ("quant_reduce.cu", "../../include/a2av_quant_reduce.h")
 
 
-def source_hash():
+def source_hash(names=GEMM_SOURCES):
     h = hashlib.sha256()
-    for name in GEMM_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "token_permute_grouped_gb300", "csrc", name), "rb") as fh:
-            h.update(name.encode() + fh.read())
+            h.update(os.path.basename(name).encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload, permute_out, path, tiles):
-    """DRAM bytes per launch of the GEMM kernel from a committed ncu summary,
-    only while the kernel sources are unchanged since the capture."""
+def profiled_traffic(workload, permute_out=False, path="default", tiles="default", kernel="grouped_gemm_kernel"):
+    """DRAM bytes per launch of a kernel from a committed ncu summary, only
+    while the kernel's sources are unchanged since the capture."""
+    names = QREDUCE_SOURCES if kernel == "quant_reduce_kernel" else GEMM_SOURCES
     for f in glob.glob(os.path.join(ROOT, "profiles", "*.json")):
         try:
             with open(f) as fh:
                 s = json.load(fh)
         except (OSError, ValueError):
             continue
-        if (s.get("workload") == workload and s.get("permute_out") == permute_out
-                and s.get("path") == path and s.get("tiles") == tiles
-                and s.get("source_hash") == source_hash()):
+        if (s.get("kernel", "grouped_gemm_kernel") == kernel and s.get("workload") == workload
+                and s.get("permute_out", False) == permute_out
+                and s.get("path", "default") == path and s.get("tiles", "default") == tiles
+                and s.get("source_hash") == source_hash(names)):
             return s.get("dram_bytes_per_launch")
     return None
 
@@ -666,7 +669,9 @@ def run_qreduce(args):
                           if reps * nbytes > L2_BYTES else
                           f"all {reps} replicas ({reps * nbytes / 2**20:.0f} MiB) fit in L2: a latency-bound case")},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None, "kernel": "quant_reduce_kernel",
+                     "frac": round(achieved / pk["hbm_gbs"], 4),
+                     "traffic": profiled_traffic(wl.name, kernel="quant_reduce_kernel"),
+                     "kernel": "quant_reduce_kernel",
                      "peak_source": f"{pk_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if pk_kind == "measured"
                      else "fallback 6.8 TB/s", "algorithmic_bytes": nbytes},
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d_b),

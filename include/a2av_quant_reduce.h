@@ -32,9 +32,9 @@
  *           [W, rows, H / 128]    float32     (GROUP128, 4-byte aligned)
  *   out     [rows, H]             out_dtype: A2AV_BF16, A2AV_FP16 or A2AV_FP32;
  *                                 16-byte aligned
- * Arithmetic: codes and scales are decoded exactly to float32; each product
- * and the running sum over w (in ascending w) are float32, rounded to
- * nearest; the sum is rounded once to out_dtype (nearest even).  NaN codes
+ * Arithmetic: codes and scales are decoded exactly to float32; the sum over w
+ * (ascending w) is formed by float32 fused multiply-adds, rounded to nearest
+ * once per rank; the sum is rounded once to out_dtype (nearest even).  NaN codes
  * (E4M3FN S.1111.111, E5M2 exponent 31 with a non-zero fraction, E8M0 0xFF)
  * give NaN; E5M2 infinities propagate.  Results are deterministic.
  *

@@ -1,16 +1,18 @@
 """Dequantising rank reduce on the GPU against the float64 oracle (needs a GB300).
 
 "aclnnQuantReduceScatter" page, Formula: out = sum over source ranks of
-scales * data.  The kernel decodes exactly to float32, forms each product and
-the running sum over ranks in float32 (round to nearest), and rounds the sum
-once to the output type.  With S = sum_w |value * scale| (float64), u32 =
-2^-24 and u_out the output type's unit roundoff, the error against the exact
-(float64) sum is at most
+scales * data.  The kernel decodes exactly to float32, sums over ranks with
+float32 fused multiply-adds (one rounding to nearest per rank), and rounds the
+sum once to the output type.  With S = sum_w |value * scale| (float64), u32 =
+2^-24 and u_out the output type's unit roundoff (2^-8 bf16, 2^-11 fp16, 2^-24
+fp32), the error against the exact (float64) sum is at most
 
     u_out * |ref| + W * u32 * S * (1 + u_out) + (output subnormal step) + W * 2^-149
 
-(products: u32 each; W - 1 float32 additions: (W - 1) u32 S; one final
-rounding: u_out times the float32 sum; the last two terms cover underflow).
+(W float32 roundings of partial sums, each at most u32 S; one final rounding:
+u_out times the float32 sum; the last two terms cover underflow).  The bound
+also holds for separately rounded products and sums, so it does not depend on
+whether the kernel fuses them.
 Every test uses this bound; NaN and infinity positions must match exactly.
 """
 

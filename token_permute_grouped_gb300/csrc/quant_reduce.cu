@@ -8,10 +8,22 @@
 // FLOAT8_E8M0 scales, one per 32 elements along H; pertoken-pergroup = INT8 /
 // FLOAT8 data with float scales, one per 128 elements along H.
 //
-// One thread makes 16 consecutive outputs of a row: one 16-byte load per
-// rank, one scale per rank (16 elements never straddle a 32-element group),
-// fp32 products and sums with ranks in order, then one rounding to the
-// output type.  HBM-bound: W * 16 + W * (1 or 4) bytes in, 16 * out bytes out.
+// A thread owns units of 16 consecutive outputs of a row: per unit, one
+// 16-byte load per rank and one scale per rank (16 elements never straddle a
+// 32-element group).  Codes are widened exactly to float32 and accumulated by
+// float32 fused multiply-adds, ranks in ascending order (one rounding per
+// rank); the sum is rounded once to the output type.  HBM-bound: per output,
+// W code bytes, W/32 scale bytes (one E8M0 byte per 32 codes, or one float
+// per 128), and 2 output bytes (bf16).
+//
+// Decoding costs a few instructions per code, not a bit-field walk:
+//   E5M2   is the upper byte of an fp16 of the same value (same sign, 5-bit
+//          exponent with bias 15, top two fraction bits), so one byte permute
+//          makes two fp16 lanes, then a half-to-float conversion;
+//   E4M3FN goes through the cvt.rn.f16x2.e4m3x2 conversion (exact: every
+//          E4M3FN value, subnormals and NaN included, is an fp16 value);
+//   INT8   b + 128 (b xor 0x80) is placed in the low byte of the float 2^23,
+//          whose unit in the last place is 1; subtracting 2^23 + 128 is exact.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -25,7 +37,7 @@ namespace a2av {
 namespace {
 
 constexpr int kQrThreads = 256;
-constexpr int kMaxRanks = 8;
+constexpr int kLoadsInFlight = 8;  // 16-byte code loads per thread per step, for any W
 
 struct QuantReduceLaunch {
     int32_t W;
@@ -36,129 +48,182 @@ struct QuantReduceLaunch {
     void *out;                       // [rows, H]
 };
 
-// 8-bit codes to float, from the format definitions.
-__device__ __forceinline__ float e4m3_to_float(uint32_t b) {
-    const uint32_t s = (b >> 7) & 1, e = (b >> 3) & 0xf, f = b & 7;
-    float v;
-    if (e == 15 && f == 7)
-        v = __uint_as_float(0x7FC00000u);                       // the only NaN code
-    else if (e == 0)
-        v = static_cast<float>(f) * 0.001953125f;               // f/8 * 2^-6 = f * 2^-9
-    else
-        v = __uint_as_float(((e + 120u) << 23) | (f << 20));    // (1 + f/8) * 2^(e-7)
-    return s ? -v : v;
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
-__device__ __forceinline__ float e5m2_to_float(uint32_t b) {
-    const uint32_t s = (b >> 7) & 1, e = (b >> 2) & 0x1f, f = b & 3;
-    float v;
-    if (e == 31)
-        v = f ? __uint_as_float(0x7FC00000u) : __uint_as_float(0x7F800000u);
-    else if (e == 0)
-        v = static_cast<float>(f) * 1.52587890625e-05f;         // f/4 * 2^-14 = f * 2^-16
-    else
-        v = __uint_as_float(((e + 112u) << 23) | (f << 21));    // (1 + f/4) * 2^(e-15)
-    return s ? -v : v;
+// Two fp16 lanes of a 32-bit word to float32 (exact).
+__device__ __forceinline__ void f16x2_to_f32(uint32_t h, float &lo, float &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h));
 }
 
+// The four codes of a word (byte k is element k) as float32.
+template <int QT>
+__device__ __forceinline__ void decode_word(uint32_t w, float (&v)[4]) {
+    if constexpr (QT == A2AV_Q_E5M2) {
+        f16x2_to_f32(__byte_perm(w, 0u, 0x1404), v[0], v[1]);  // bytes 0, 1 to the high byte of each lane
+        f16x2_to_f32(__byte_perm(w, 0u, 0x3424), v[2], v[3]);
+    } else if constexpr (QT == A2AV_Q_E4M3FN) {
+        uint32_t lo, hi;
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
+        f16x2_to_f32(lo, v[0], v[1]);
+        f16x2_to_f32(hi, v[2], v[3]);
+    } else {
+        const uint32_t x = w ^ 0x80808080u;  // b + 128 in each byte
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            v[k] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7650 + k)) - 8388736.0f;  // 2^23 + 128
+    }
+}
+
+// E8M0 scale code: 2^(e - 127); 0xFF is NaN.
 __device__ __forceinline__ float e8m0_to_float(uint32_t e) {
     if (e == 255) return __uint_as_float(0x7FC00000u);
-    if (e == 0) return __uint_as_float(0x00400000u);            // 2^-127, a float subnormal
-    return __uint_as_float(e << 23);                            // 2^(e-127)
+    if (e == 0) return __uint_as_float(0x00400000u);  // 2^-127, a float subnormal
+    return __uint_as_float(e << 23);
 }
 
-template <int QT>
-__device__ __forceinline__ float q_to_float(uint32_t b) {
-    if constexpr (QT == 0) return e4m3_to_float(b);
-    else if constexpr (QT == 1) return e5m2_to_float(b);
-    else return static_cast<float>(static_cast<int8_t>(b));
-}
-
-template <int QT, int MODE, int OUT>
+template <int W, int QT, int MODE, int OUT>
 __global__ void __launch_bounds__(kQrThreads)
-    quant_reduce_kernel(int W, int64_t rows, int64_t H, const uint8_t *__restrict__ data,
-                        const void *__restrict__ scales, void *__restrict__ out) {
-    const int64_t vpr = H / 16;  // 16-element units per row
-    const int64_t units = rows * vpr;
-    const int64_t group = MODE == 0 ? 32 : 128;
-    const int64_t ngr = H / group;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units; u += stride) {
-        const int64_t i = u / vpr, h0 = (u % vpr) * 16;
-        uint4 v[kMaxRanks];
-        float sc[kMaxRanks];
+    quant_reduce_kernel(int64_t rows, int64_t H, const uint8_t *__restrict__ data, const void *__restrict__ scales,
+                        void *__restrict__ out) {
+    constexpr int U = kLoadsInFlight / W;  // units per thread per step
+    constexpr int64_t kGroup = MODE == A2AV_QMODE_MX ? 32 : 128;
+    const int64_t vpr = H / 16;      // units per row
+    const int64_t ngr = H / kGroup;  // scale groups per row
+    const int64_t plane = rows * H, splane = rows * ngr;
+    // Unit u = i * vpr + c (row i, 16-column chunk c).  Units of one step are
+    // spaced by the block size, so each load instruction is coalesced; a step
+    // advances every unit by `stride`, kept as (row, chunk) increments.
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kQrThreads * U;
+    const int64_t dq = stride / vpr, dr = stride % vpr;
+    int64_t ri[U], ci[U];
 #pragma unroll
-        for (int w = 0; w < kMaxRanks; ++w) {
-            if (w < W) {
-                const int64_t row = static_cast<int64_t>(w) * rows + i;
-                v[w] = __ldg(reinterpret_cast<const uint4 *>(data + row * H + h0));
-                if constexpr (MODE == 0)
-                    sc[w] = e8m0_to_float(__ldg(static_cast<const uint8_t *>(scales) + row * ngr + h0 / group));
-                else
-                    sc[w] = __ldg(static_cast<const float *>(scales) + row * ngr + h0 / group);
-            }
-        }
-        float acc[16];
+    for (int j = 0; j < U; ++j) {
+        const int64_t u = (static_cast<int64_t>(blockIdx.x) * U + j) * kQrThreads + threadIdx.x;
+        ri[j] = u / vpr;
+        ci[j] = u % vpr;
+    }
+    while (ri[0] < rows) {
+        uint4 q[U][W];
+        float sc[U][W];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+        for (int j = 0; j < U; ++j) {
+            if (ri[j] < rows) {
+                const int64_t off = ri[j] * H + ci[j] * 16;
+                const int64_t soff = ri[j] * ngr + ci[j] * 16 / kGroup;
 #pragma unroll
-        for (int w = 0; w < kMaxRanks; ++w) {
-            if (w < W) {
-                const uint32_t word[4] = {v[w].x, v[w].y, v[w].z, v[w].w};
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    acc[k] = __fadd_rn(acc[k], __fmul_rn(q_to_float<QT>((word[k >> 2] >> (8 * (k & 3))) & 0xFF), sc[w]));
-            }
-        }
-        if constexpr (OUT == 2) {
-            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + i * H + h0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) o[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-        } else {
-            uint32_t packed[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                if constexpr (OUT == 0) {
-                    __nv_bfloat162 t = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-                    packed[q] = *reinterpret_cast<uint32_t *>(&t);
-                } else {
-                    __half2 t = __floats2half2_rn(acc[2 * q], acc[2 * q + 1]);
-                    packed[q] = *reinterpret_cast<uint32_t *>(&t);
+                for (int w = 0; w < W; ++w) {
+                    q[j][w] = ld_stream(data + w * plane + off);
+                    if constexpr (MODE == A2AV_QMODE_MX)
+                        sc[j][w] = e8m0_to_float(__ldg(static_cast<const uint8_t *>(scales) + w * splane + soff));
+                    else
+                        sc[j][w] = __ldg(static_cast<const float *>(scales) + w * splane + soff);
                 }
             }
-            uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + i * H + h0);
-            o[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            o[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            if (ri[j] < rows) {
+                float acc[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+#pragma unroll
+                for (int w = 0; w < W; ++w) {
+                    const uint32_t word[4] = {q[j][w].x, q[j][w].y, q[j][w].z, q[j][w].w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        float v[4];
+                        decode_word<QT>(word[t], v);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) acc[4 * t + k] = __fmaf_rn(v[k], sc[j][w], acc[4 * t + k]);
+                    }
+                }
+                const int64_t off = ri[j] * H + ci[j] * 16;
+                if constexpr (OUT == A2AV_FP32) {
+                    float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + off);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        o[t] = make_float4(acc[4 * t], acc[4 * t + 1], acc[4 * t + 2], acc[4 * t + 3]);
+                } else {
+                    uint32_t packed[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        if constexpr (OUT == A2AV_BF16) {
+                            __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * t], acc[2 * t + 1]);
+                            packed[t] = *reinterpret_cast<uint32_t *>(&b);
+                        } else {
+                            __half2 b = __floats2half2_rn(acc[2 * t], acc[2 * t + 1]);
+                            packed[t] = *reinterpret_cast<uint32_t *>(&b);
+                        }
+                    }
+                    uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + off);
+                    o[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    o[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                }
+            }
+            ci[j] += dr;
+            if (ci[j] >= vpr) {
+                ci[j] -= vpr;
+                ri[j] += 1;
+            }
+            ri[j] += dq;
         }
     }
 }
 
-template <int QT, int MODE, int OUT>
+template <int W, int QT, int MODE, int OUT>
 cudaError_t launch_qr(const QuantReduceLaunch &p, int num_sms, cudaStream_t stream) {
-    const int64_t units = p.rows * (p.H / 16);
-    int64_t blocks = (units + kQrThreads - 1) / kQrThreads;
-    const int64_t cap = static_cast<int64_t>(num_sms) * (2048 / kQrThreads) * 4;
+    constexpr int U = kLoadsInFlight / W;
+    static int resident = 0;  // CTAs per SM, from the occupancy calculator, once per instantiation
+    if (resident == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_reduce_kernel<W, QT, MODE, OUT>, kQrThreads,
+                                                          0) != cudaSuccess || n < 1)
+            n = 1;
+        resident = n;
+    }
+    const int64_t per_block = static_cast<int64_t>(kQrThreads) * U;
+    int64_t blocks = (p.rows * (p.H / 16) + per_block - 1) / per_block;
+    const int64_t cap = static_cast<int64_t>(num_sms) * resident;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    quant_reduce_kernel<QT, MODE, OUT><<<static_cast<int>(blocks), kQrThreads, 0, stream>>>(
-        p.W, p.rows, p.H, static_cast<const uint8_t *>(p.data), p.scales, p.out);
+    quant_reduce_kernel<W, QT, MODE, OUT><<<static_cast<int>(blocks), kQrThreads, 0, stream>>>(
+        p.rows, p.H, static_cast<const uint8_t *>(p.data), p.scales, p.out);
     return cudaGetLastError();
 }
 
-template <int QT, int MODE>
+template <int W, int QT, int MODE>
 cudaError_t launch_qr_out(const QuantReduceLaunch &p, int num_sms, cudaStream_t stream) {
-    if (p.out_dtype == 0) return launch_qr<QT, MODE, 0>(p, num_sms, stream);
-    if (p.out_dtype == 1) return launch_qr<QT, MODE, 1>(p, num_sms, stream);
-    return launch_qr<QT, MODE, 2>(p, num_sms, stream);
+    if (p.out_dtype == A2AV_BF16) return launch_qr<W, QT, MODE, A2AV_BF16>(p, num_sms, stream);
+    if (p.out_dtype == A2AV_FP16) return launch_qr<W, QT, MODE, A2AV_FP16>(p, num_sms, stream);
+    return launch_qr<W, QT, MODE, A2AV_FP32>(p, num_sms, stream);
+}
+
+template <int W>
+cudaError_t launch_qr_w(const QuantReduceLaunch &p, int num_sms, cudaStream_t stream) {
+    if (p.mode == A2AV_QMODE_MX) {  // FLOAT8 data, E8M0 scales per 32
+        return p.qtype == A2AV_Q_E4M3FN ? launch_qr_out<W, A2AV_Q_E4M3FN, A2AV_QMODE_MX>(p, num_sms, stream)
+                                        : launch_qr_out<W, A2AV_Q_E5M2, A2AV_QMODE_MX>(p, num_sms, stream);
+    }
+    if (p.qtype == A2AV_Q_E4M3FN) return launch_qr_out<W, A2AV_Q_E4M3FN, A2AV_QMODE_GROUP128>(p, num_sms, stream);
+    if (p.qtype == A2AV_Q_E5M2) return launch_qr_out<W, A2AV_Q_E5M2, A2AV_QMODE_GROUP128>(p, num_sms, stream);
+    return launch_qr_out<W, A2AV_Q_INT8, A2AV_QMODE_GROUP128>(p, num_sms, stream);
 }
 
 cudaError_t launch_quant_reduce(const QuantReduceLaunch &p, int num_sms, cudaStream_t stream) {
-    if (p.mode == 0) {  // mx: FLOAT8 data, E8M0 scales per 32
-        return p.qtype == 0 ? launch_qr_out<0, 0>(p, num_sms, stream) : launch_qr_out<1, 0>(p, num_sms, stream);
-    }
-    if (p.qtype == 0) return launch_qr_out<0, 1>(p, num_sms, stream);
-    if (p.qtype == 1) return launch_qr_out<1, 1>(p, num_sms, stream);
-    return launch_qr_out<2, 1>(p, num_sms, stream);
+    if (p.W == 2) return launch_qr_w<2>(p, num_sms, stream);
+    if (p.W == 4) return launch_qr_w<4>(p, num_sms, stream);
+    return launch_qr_w<8>(p, num_sms, stream);
 }
 
 int qr_sm_count() {
