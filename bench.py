@@ -15,6 +15,11 @@ Under torchrun (N > 1) every rank runs its own expert-parallel rank's share
 --impl reference times the CPU oracle (float64, OpenMP) on the host cores on a
 bounded sample of the same workload and prints the same line with
 "impl": "reference".
+
+Other measurements (one JSON line each):
+    --op amp       the loss-scale step: inf/NaN scan and scale update
+    --op qreduce   the dequantising rank reduce [--qworkload NAME]
+    --op layer     AlltoAllv (NCCL) + the hot path, per rank [--overlap]
 """
 
 from __future__ import annotations
@@ -688,6 +693,89 @@ def run_qreduce(args):
     barrier(world)
 
 
+# ------------------------------------------------------ the whole operator
+
+def run_layer(args):
+    """AlltoAllv (NCCL) + Permute + GroupedMatMul + shared-expert MatMul per step, through
+    exchange.layer.  Every rank sends its gmmX rows to their expert owners, so with N ranks
+    this is the full expert-parallel exchange (N = 1: rows go to the same rank)."""
+    from token_permute_grouped_gb300 import exchange
+    from token_permute_grouped_gb300.workloads import Workload, make_gmmX
+    world, rank, local = dist_env()
+    assert torch.cuda.is_available(), "bench.py needs a GPU (use --impl reference for the CPU oracle)"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not torch.distributed.is_initialized():
+        if world == 1:
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            os.environ.setdefault("MASTER_PORT", str(29500 + os.getpid() % 1000))
+            torch.distributed.init_process_group("nccl", rank=0, world_size=1)
+        else:
+            torch.distributed.init_process_group("nccl")
+    build.build()
+    binding.load()
+    base = WORKLOADS[args.workload]
+    if base.routing != "normal":
+        raise SystemExit(f"--op layer needs a workload with the normal routing model, not {base.name}")
+    # The expert-parallel domain is the torchrun world: W = N ranks with the workload's e, H, N.
+    # With fewer than K global experts, K is capped at W*e and each source routes
+    # proportionally more tokens, so a rank still expects tokens_per_source * K rows.
+    k = min(base.topk, world * base.e)
+    wl = Workload(f"{base.name}_ep{world}", W=world, e=base.e, H1=base.H1, N1=base.N1, dtype=base.dtype,
+                  routing="normal", tokens_per_source=base.tokens_per_source * base.topk // k, topk=k,
+                  bias_std=base.bias_std, BS=base.BS, H2=base.H2, N2=base.N2)
+    gmmX, sc = make_gmmX(wl, seed=0, rank=rank)
+    inp = make_inputs(base, seed=0, rank=rank)  # weights and mmX of this rank
+    reps = 2
+    sets = [dict(gmmX=gmmX.to(dev), sc=torch.from_numpy(sc).to(dev), gw=inp.gmmWeight.to(dev),
+                 mmX=inp.mmX.to(dev) if wl.BS else None, mmW=inp.mmWeight.to(dev) if wl.BS else None)
+            for _ in range(reps)]
+    out = {}
+
+    def step(i):
+        s = sets[i % reps]
+        out["r"] = exchange.layer(s["gmmX"], s["sc"], s["gw"], s["mmX"], s["mmW"],
+                                  overlap_shared=args.overlap)
+
+    sync = torch.cuda.synchronize
+    for i in range(args.warmup):
+        step(i)
+    sync()
+    A = int(out["r"][3].shape[0])
+    flops = flops_of(wl, A)
+    with ClockSampler(local) as clocks:
+        dt, dt_max = timed_region(step, args.steps, world, dev, sync)
+    total = reduce_sum(flops * args.steps, world, dev)
+    tflops = total / dt_max / 1e12
+    plan = binding.Plan(wl.W, wl.e, A, wl.H1, wl.N1, 0 if args.overlap else wl.BS, wl.H2, wl.N2,
+                        wl.torch_dtype, device=dev)
+    launches = binding.a2av_gmm_launch_count(plan.desc) + (1 if wl.BS and args.overlap else 0)
+    if rank != 0:
+        barrier(world)
+        return
+    pk, pk_kind = peaks()
+    print(json.dumps({
+        "metric": METRIC + " (with the AlltoAllv in the step)", "value": round(tflops, 2), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt_max * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded routing and N(0,1) tensors; no dataset)",
+        "config": {"workload": wl.name, "W": wl.W, "e": wl.e, "A_rank0": A, "H1": wl.H1, "N1": wl.N1,
+                   "tokens_per_source": wl.tokens_per_source, "topk": wl.topk,
+                   "BS": wl.BS, "H2": wl.H2, "N2": wl.N2,
+                   "exchange": f"NCCL all_to_all_single of counts, then of rows, world {world}",
+                   "shared_expert": "beside the row exchange" if args.overlap else "with the routed experts",
+                   "timing": "host wall clock between barriers and syncs (the step syncs once on the counts)",
+                   "l2": f"inputs rotated over {reps} replicas (gmmX alone {gmmX.numel() * 2 / 2**20:.0f} MiB)"},
+        "roofline": {"bound": "tensor", "achieved": round(tflops / world, 2), "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(tflops / world / pk["bf16_tflops"], 4), "traffic": None,
+                     "peak_source": f"{pk_kind} bf16 dense burst", "note": "per GPU, exchange included"},
+        "e2e": None,
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks.summary(),
+    }), flush=True)
+    barrier(world)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -698,8 +786,11 @@ def main(argv=None):
     ap.add_argument("--path", default="default", choices=["default", "fused", "split", "split_runs"])
     ap.add_argument("--tiles", default="default", choices=["default", "single", "pair", "pair_k64"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="gemm", choices=["gemm", "amp", "qreduce"],
-                    help="gemm: the hot path (default); amp: the loss-scale step; qreduce: the quantised rank reduce")
+    ap.add_argument("--op", default="gemm", choices=["gemm", "amp", "qreduce", "layer"],
+                    help="gemm: the hot path (default); amp: the loss-scale step; qreduce: the quantised "
+                         "rank reduce; layer: AlltoAllv + the hot path")
+    ap.add_argument("--overlap", action="store_true",
+                    help="--op layer: run the shared expert beside the row exchange (default: with the routed experts)")
     ap.add_argument("--qworkload", default="qreduce_mx_e4m3_w8_rows1536_h7168",
                     help="workload of --op qreduce")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -708,6 +799,8 @@ def main(argv=None):
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.op == "qreduce":
         run_qreduce(args)
+    elif args.op == "layer":
+        run_layer(args)
     elif args.impl == "reference":
         run_reference(args)
     elif args.op == "amp":

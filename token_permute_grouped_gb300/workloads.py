@@ -39,6 +39,7 @@ STREAM_ATAOUT = 1
 STREAM_GMM_WEIGHT = 2
 STREAM_MMX = 3
 STREAM_MM_WEIGHT = 4
+STREAM_GMMX = 7  # a source rank's rows before the AlltoAllv
 
 
 @dataclasses.dataclass(frozen=True)
@@ -151,11 +152,7 @@ def recv_counts(wl: Workload, seed: int = 0, rank: int = 0) -> np.ndarray:
 
     rc = np.zeros(E, dtype=np.int64)
     if wl.routing == "normal":
-        bias = (rng.standard_normal(E) * wl.bias_std) if wl.bias_std else np.zeros(E)
-        for w in range(W):
-            logits = rng.standard_normal((wl.tokens_per_source, E), dtype=np.float32)
-            logits += bias.astype(np.float32)
-            rc[w * e:(w + 1) * e] = _topk_counts(logits, wl.topk, lo, e)
+        rc[:] = routing_counts(wl, seed)[:, lo:lo + e].reshape(-1)
     elif wl.routing == "zipf":
         # Popularity p_x proportional to rank(x)^-s over a seeded ranking of
         # the E experts; each token samples K distinct experts with
@@ -182,6 +179,37 @@ def recv_counts(wl: Workload, seed: int = 0, rank: int = 0) -> np.ndarray:
     else:
         raise ValueError(wl.routing)
     return rc.astype(np.int32)
+
+
+def routing_counts(wl: Workload, seed: int = 0) -> np.ndarray:
+    """[W, W*e] int64: how many of source rank w's top-K selections hit global
+    expert g, for the "normal" routing model (one draw shared by all ranks)."""
+    if wl.routing != "normal":
+        raise ValueError("routing_counts models the sender side of normal routing only")
+    W, E = wl.W, wl.W * wl.e
+    rng = _rng(seed, STREAM_ROUTING)
+    bias = (rng.standard_normal(E) * wl.bias_std) if wl.bias_std else np.zeros(E)
+    out = np.zeros((W, E), dtype=np.int64)
+    for w in range(W):
+        logits = rng.standard_normal((wl.tokens_per_source, E), dtype=np.float32)
+        logits += bias.astype(np.float32)
+        out[w] = _topk_counts(logits, wl.topk, 0, E)
+    return out
+
+
+def send_counts(wl: Workload, seed: int = 0, rank: int = 0) -> np.ndarray:
+    """sendCounts of source rank `rank`: int32 [W*e], entry g = rows it sends to
+    global expert g (owned by rank g // e as its local expert g % e)."""
+    return routing_counts(wl, seed)[rank].astype(np.int32)
+
+
+def make_gmmX(wl: Workload, seed: int = 0, rank: int = 0) -> tuple[torch.Tensor, np.ndarray]:
+    """(gmmX, sendCounts) of one source rank: [sum(sendCounts), H1] N(0,1) rows,
+    grouped by destination global expert in ascending order, drawn from seed + rank."""
+    sc = send_counts(wl, seed, rank)
+    n = int(sc.astype(np.int64).sum())
+    x = rounded(normal_f32(n * wl.H1, seed + rank, STREAM_GMMX), (n, wl.H1), wl.torch_dtype)
+    return x, sc
 
 
 @dataclasses.dataclass
