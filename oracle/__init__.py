@@ -60,10 +60,11 @@ def _declare(lib):
     lib.a2av_ref_any_nonfinite.argtypes = [ctypes.c_int, p, i64, p]
     lib.a2av_ref_decode8.argtypes = [ctypes.c_int, p, i64, p]
     lib.a2av_ref_quant_reduce.argtypes = [i32, i64, i64, i32, i32, p, p, p]
+    lib.a2av_ref_mx_grouped_matmul.argtypes = [i32, p, i64, i64, i64, i32, i32, p, p, p, p, p, i64, p]
     for f in ("a2av_ref_decode", "a2av_ref_plan", "a2av_ref_permute",
               "a2av_ref_grouped_matmul", "a2av_ref_matmul", "a2av_ref_num_threads",
               "a2av_ref_amp_update_scale", "a2av_ref_any_nonfinite", "a2av_ref_decode8",
-              "a2av_ref_quant_reduce"):
+              "a2av_ref_quant_reduce", "a2av_ref_mx_grouped_matmul"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -194,6 +195,24 @@ class Oracle:
         out = np.empty((rows, H), np.float64)
         _check(self.L.a2av_ref_quant_reduce(W, rows, H, qtype, mode, _ptr(d), _ptr(sc), _ptr(out)),
                "quant_reduce")
+        return out
+
+    def mx_grouped_matmul(self, group_rows, a, sa, w, sw, qa: int, qw: int, rows=None) -> np.ndarray:
+        """Block-scaled FP8 grouped product: a [A, K] codes, sa [A, K/32] E8M0, w [e, N, K]
+        codes, sw [e, N, K/32] E8M0 (all uint8); qa, qw 0 = E4M3FN, 1 = E5M2.  Returns
+        [len(rows) or A, N] float64.  A shared-expert product is the case e = 1."""
+        gr = np.ascontiguousarray(group_rows, dtype=np.int64)
+        a, sa, w, sw = (np.ascontiguousarray(t.numpy() if isinstance(t, torch.Tensor) else t, dtype=np.uint8)
+                        for t in (a, sa, w, sw))
+        A, K = a.shape
+        e, N, K2 = w.shape
+        assert K2 == K and sa.shape == (A, K // 32) and sw.shape == (e, N, K // 32) and len(gr) == e
+        rl = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        n = A if rl is None else len(rl)
+        out = np.empty((n, N), np.float64)
+        _check(self.L.a2av_ref_mx_grouped_matmul(e, _ptr(gr), A, K, N, qa, qw, _ptr(a), _ptr(sa), _ptr(w),
+                                                 _ptr(sw), _ptr(rl), 0 if rl is None else n, _ptr(out)),
+               "mx_grouped_matmul")
         return out
 
     def run(self, W: int, e: int, recvCounts, ataOut, gmmWeight, mmX=None, mmWeight=None,

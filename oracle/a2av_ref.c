@@ -474,3 +474,79 @@ int a2av_ref_quant_reduce(int32_t W, int64_t rows, int64_t H, int32_t qtype, int
     }
     return REF_OK;
 }
+
+/* ---- MX (block-scaled FP8) grouped product ----------------------------
+ *
+ * The GroupedMatMul of "aclnnAlltoAllvGroupedMatMul" ("Formula": gmmY =
+ * permuteOut x gmmWeight) with its operands in the mx quantisation that the
+ * "aclnnQuantReduceScatter" page's "Constraints" define: FLOAT8_E4M3FN or
+ * FLOAT8_E5M2 codes, one FLOAT8_E8M0 scale per 32 consecutive elements of a
+ * row (scalesDataSize = rows * H / 32 bytes).  Both operands are blocked
+ * along the contraction dimension K, so
+ *
+ *   out[i][n] = sum_k  value(a[i][k]) * 2^(sa[i][k/32] - 127)
+ *                    * value(w[n][k]) * 2^(sw[n][k/32] - 127)
+ *
+ * for row i of group j, with w = that group's weight.  Layouts (row-major):
+ *   a   [A, K] codes,  sa [A, K/32] E8M0          (rows expert-major)
+ *   w   [e, N, K] codes (each output column's K codes contiguous),
+ *   sw  [e, N, K/32] E8M0.
+ * Each element is decoded to its exact value, products are formed and summed
+ * in double, k ascending.  `rows` (length nrows) selects output rows as in
+ * a2av_ref_grouped_matmul (NULL: all A rows); out is [nrows, N].
+ * qa, qw: 0 = E4M3FN, 1 = E5M2.
+ */
+int a2av_ref_mx_grouped_matmul(int32_t e, const int64_t *group_rows, int64_t A, int64_t K, int64_t N,
+                               int32_t qa, int32_t qw, const uint8_t *a, const uint8_t *sa,
+                               const uint8_t *w, const uint8_t *sw, const int64_t *rows, int64_t nrows,
+                               double *out)
+{
+    if (e < 1 || !group_rows || A < 0 || K < 32 || K % 32 || N < 1 || qa < 0 || qa > 1 || qw < 0 || qw > 1)
+        return REF_BAD_ARG;
+    int64_t sum = 0;
+    for (int32_t j = 0; j < e; ++j) {
+        if (group_rows[j] < 0)
+            return REF_BAD_COUNTS;
+        sum += group_rows[j];
+    }
+    if (sum != A)
+        return REF_BAD_COUNTS;
+    if (!rows)
+        nrows = A;
+    if (nrows == 0)
+        return REF_OK;
+    if (!a || !sa || !w || !sw || !out || nrows < 0)
+        return REF_BAD_ARG;
+    const int64_t nb = K / 32;
+    int bad = 0;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= A)
+            bad = 1;
+    }
+    if (bad)
+        return REF_BAD_ARG;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        int64_t start = 0;
+        int32_t j = 0;
+        while (i >= start + group_rows[j]) {
+            start += group_rows[j];
+            ++j;
+        }
+        double *x = malloc(sizeof(double) * K);
+        for (int64_t k = 0; k < K; ++k)
+            x[k] = q_value(qa, a[i * K + k]) * e8m0_value(sa[i * nb + k / 32]);
+        const uint8_t *wj = w + (int64_t)j * N * K;
+        const uint8_t *sj = sw + (int64_t)j * N * nb;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += x[k] * (q_value(qw, wj[n * K + k]) * e8m0_value(sj[n * nb + k / 32]));
+            out[r * N + n] = acc;
+        }
+        free(x);
+    }
+    return REF_OK;
+}

@@ -10,8 +10,11 @@ that each plausible mistake is caught.
 
 Pages cited: "aclnnAlltoAllvGroupedMatMul", sections "Formula"
 (permuteOut = Permute(ataOut), gmmY = permuteOut x gmmWeight,
-mmY = mmX x mmWeight) and "Shape variables" (A = sum of recvCounts); and
-"aclnnAmpUpdateScale", "Formula" and its notes, for the loss-scale update.
+mmY = mmX x mmWeight) and "Shape variables" (A = sum of recvCounts);
+"aclnnAmpUpdateScale", "Formula" and its notes, for the loss-scale update;
+"aclnnQuantReduceScatter", "Formula" and "Constraints" (mx quantisation:
+FLOAT8 codes with one FLOAT8_E8M0 scale per 32 elements; float scales per
+128), for the quantised reduce and the block-scaled FP8 grouped product.
 """
 
 from __future__ import annotations
@@ -449,6 +452,110 @@ def pin_quant_reduce_rejects_bad_modes(orc):
         except OracleError:
             continue
         raise AssertionError("accepted")
+
+
+# ---- block-scaled FP8 grouped product (mx operands) ---------------------------
+
+def _mx_decode(codes, scales, qtype):
+    """Exact values of mx-quantised rows by torch's own float8 decoders: codes [..., K],
+    E8M0 scales [..., K/32]."""
+    t = torch.from_numpy(np.ascontiguousarray(codes))
+    v = t.view(torch.float8_e4m3fn if qtype == 0 else torch.float8_e5m2).to(torch.float64)
+    s = torch.from_numpy(np.ascontiguousarray(scales)).view(torch.float8_e8m0fnu).to(torch.float64)
+    return (v * s.repeat_interleave(32, dim=-1)).numpy()
+
+
+def _mx_random(rng, shape, qtype, lo=120, hi=134):
+    """Random finite codes of a format and E8M0 scales in [lo, hi]."""
+    finite = np.array([c for c in range(256) if (qtype == 0 and (c & 0x7F) != 0x7F)
+                       or (qtype == 1 and (c & 0x7C) != 0x7C)], np.uint8)
+    codes = finite[rng.integers(0, len(finite), shape)]
+    scales = rng.integers(lo, hi + 1, shape[:-1] + (shape[-1] // 32,)).astype(np.uint8)
+    return codes, scales
+
+
+def pin_mx_grouped_matmul_golden(orc):
+    g = _golden("mx_grouped_matmul.json")
+    for q, key in ((0, "e4m3"), (1, "e5m2")):
+        c = g[key]
+        K = c["K"]
+        a = np.repeat(np.array(c["a_codes"], np.uint8), 32)[None, :]
+        sa = np.array(c["a_scales"], np.uint8)[None, :]
+        w = np.stack([np.repeat(np.array(col, np.uint8), 32) for col in c["w_codes"]])[None]
+        sw = np.array(c["w_scales"], np.uint8)[None]
+        assert a.shape == (1, K)
+        out = orc.mx_grouped_matmul([1], a, sa, w, sw, q, q)
+        assert out[0].tolist() == c["want"], (key, out)
+
+
+def pin_mx_grouped_matmul_numpy(orc):
+    # Against numpy float64 products of operands decoded by torch.
+    rng = np.random.default_rng(31)
+    for q in (0, 1):
+        e, K, N = 3, 96, 24
+        gr = [5, 0, 9]
+        a, sa = _mx_random(rng, (14, K), q)
+        w, sw = _mx_random(rng, (e, N, K), q)
+        got = orc.mx_grouped_matmul(gr, a, sa, w, sw, q, q)
+        x = _mx_decode(a, sa, q)
+        wv = _mx_decode(w, sw, q)
+        expert = np.repeat(np.arange(e), gr)
+        want = np.stack([x[i] @ wv[expert[i]].T for i in range(14)])
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-300), q
+
+
+def pin_mx_scale_block_locality(orc):
+    # Only block b of the row carries non-zero codes: the other blocks' scales
+    # cannot matter, and one step of block b's scale doubles the result.
+    K, N = 128, 4
+    a = np.zeros((1, K), np.uint8)
+    a[0, 64:96] = 0x38  # 1.0 in block 2
+    sa = np.array([[100, 140, 127, 90]], np.uint8)
+    w = np.full((1, N, K), 0x38, np.uint8)
+    sw = np.full((1, N, K // 32), 127, np.uint8)
+    base = orc.mx_grouped_matmul([1], a, sa, w, sw, 0, 0)
+    assert (base == 32.0).all()
+    sa2 = sa.copy()
+    sa2[0, [0, 1, 3]] = [130, 110, 127]
+    assert np.array_equal(orc.mx_grouped_matmul([1], a, sa2, w, sw, 0, 0), base)
+    sa2[0, 2] = 128
+    assert (orc.mx_grouped_matmul([1], a, sa2, w, sw, 0, 0) == 64.0).all()
+    sw2 = sw.copy()
+    sw2[0, 1, 2] = 125  # column 1, block 2: a quarter
+    out = orc.mx_grouped_matmul([1], a, sa, w, sw2, 0, 0)
+    assert out[0].tolist() == [32.0, 8.0, 32.0, 32.0]
+
+
+def pin_mx_group_boundaries_scaled_identity(orc):
+    # w[j][n][k] = 2^j * [k == n] (E4M3 1.0 with E8M0 scale 127 + j): row i of
+    # group j gives 2^j * x[i][:N], exactly, across an empty group.
+    rng = np.random.default_rng(32)
+    K = N = 64
+    gr = [3, 0, 4, 2]
+    a, sa = _mx_random(rng, (9, K), 0, 124, 130)
+    w = np.zeros((4, N, K), np.uint8)
+    for n in range(N):
+        w[:, n, n] = 0x38
+    sw = np.repeat((127 + np.arange(4, dtype=np.uint8))[:, None, None], N, 1).repeat(K // 32, 2)
+    got = orc.mx_grouped_matmul(gr, a, sa, w, sw, 0, 0)
+    x = _mx_decode(a, sa, 0)
+    expert = np.repeat(np.arange(4), gr)
+    assert np.array_equal(got, x * (2.0 ** expert)[:, None])
+
+
+def pin_mx_rows_subset_and_rejects(orc):
+    rng = np.random.default_rng(33)
+    a, sa = _mx_random(rng, (7, 64), 1)
+    w, sw = _mx_random(rng, (2, 5, 64), 1)
+    full = orc.mx_grouped_matmul([3, 4], a, sa, w, sw, 1, 1)
+    rows = [6, 0, 3, 3]
+    assert np.array_equal(orc.mx_grouped_matmul([3, 4], a, sa, w, sw, 1, 1, rows=rows), full[rows])
+    for args in (([3, 3], a, sa, w, sw, 1, 1), ([3, 4], a, sa, w, sw, 2, 1)):
+        try:
+            orc.mx_grouped_matmul(*args)
+        except OracleError:
+            continue
+        raise AssertionError(f"accepted {args[0]}, qa={args[5]}")
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

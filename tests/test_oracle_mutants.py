@@ -57,6 +57,10 @@ MUTANTS = {
     "quant_reduce_drops_last_rank": (
         "            for (int32_t w = 0; w < W; ++w) {\n                const int64_t row",
         "            for (int32_t w = 0; w + 1 < W; ++w) {\n                const int64_t row"),
+    "mx_weight_scale_ignores_column": ("e8m0_value(sj[n * nb + k / 32])", "e8m0_value(sj[k / 32])"),
+    "mx_weight_read_transposed": ("q_value(qw, wj[n * K + k])", "q_value(qw, wj[k * N + n])"),
+    "mx_activation_scale_block_64": ("e8m0_value(sa[i * nb + k / 32])", "e8m0_value(sa[i * nb + k / 64])"),
+    "mx_first_expert_weight_for_all": ("const uint8_t *wj = w + (int64_t)j * N * K;", "const uint8_t *wj = w;"),
     "amp_backoff_keeps_tracker": (
         "        *scale = *scale * backoff_factor;\n        *growth_tracker = 0;",
         "        *scale = *scale * backoff_factor;"),
