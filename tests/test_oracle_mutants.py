@@ -29,8 +29,15 @@ MUTANTS = {
         "o[n] += a * dec[wk[n]];",
         "o[n] += a * dec[wk[N - 1 - n]];"),
     "row_assigned_to_previous_group": (
-        "while (i >= start + group_rows[j]) {",
-        "while (i > start + group_rows[j] && j + 1 < e) {"),
+        "while (i >= start + group_rows[j]) {\n            start += group_rows[j];\n            ++j;\n"
+        "        }\n        expert[r] = j;",
+        "while (i > start + group_rows[j] && j + 1 < e) {\n            start += group_rows[j];\n            ++j;\n"
+        "        }\n        expert[r] = j;"),
+    "mx_row_assigned_to_previous_group": (
+        "while (i >= start + group_rows[j]) {\n            start += group_rows[j];\n            ++j;\n"
+        "        }\n        double *x",
+        "while (i > start + group_rows[j] && j + 1 < e) {\n            start += group_rows[j];\n            ++j;\n"
+        "        }\n        double *x"),
     "fp16_exponent_bias_off_by_one": (
         "ldexp((double)(1024 + frac), expo - 25)",
         "ldexp((double)(1024 + frac), expo - 24)"),
