@@ -20,6 +20,7 @@ Other measurements (one JSON line each):
     --op amp       the loss-scale step: inf/NaN scan and scale update
     --op qreduce   the dequantising rank reduce [--qworkload NAME]
     --op layer     AlltoAllv (NCCL) + the hot path, per rank [--overlap]
+    --op mx        the hot path with block-scaled FP8 operands [--mx-qtype]
 """
 
 from __future__ import annotations
@@ -776,6 +777,190 @@ def run_layer(args):
     barrier(world)
 
 
+# ------------------------------------------------ block-scaled FP8 (mx) GEMM
+
+MX_METRIC = "mx (block-scaled FP8) permute+grouped-GEMM TFLOP/s, % of GB300 FP8 dense peak; us per call"
+
+
+def mx_bytes(wl, A):
+    """Algorithmic bytes of one mx call: codes and E8M0 scales read once (1 + 1/32 bytes per
+    element), bf16 outputs written once, permuteOut not requested."""
+    ins = A * wl.H1 + wl.e * wl.H1 * wl.N1 + (wl.BS * wl.H2 + wl.H2 * wl.N2 if wl.BS else 0)
+    return int(ins * (1 + 1 / 32) + 2 * (A * wl.N1 + wl.BS * wl.N2))
+
+
+def mx_oracle_sample(wl, inp, seconds, seed=0):
+    """Oracle on seeded output rows of the mx call; returns (FLOPs, seconds, rows, threads, description)."""
+    import oracle
+    orc = oracle.Oracle()
+    q = 0 if inp.qtype == "e4m3fn" else 1
+    pq = orc.permute(wl.W, wl.e, inp.recvCounts, inp.ataOut_q.view(torch.int16)).view(torch.uint8)
+    ps = orc.permute(wl.W, wl.e, inp.recvCounts, inp.ataOut_s.view(torch.int16)).view(torch.uint8)
+    _, _, gr, _ = orc.plan(wl.W, wl.e, inp.recvCounts, inp.A)
+    rng = np.random.default_rng(seed)
+    total_rows = inp.A + wl.BS
+    chunk = max(orc.num_threads(), 8)
+    flops = 0.0
+    rows = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        r = rng.integers(0, total_rows, chunk)
+        routed, shared = r[r < inp.A], r[r >= inp.A] - inp.A
+        if len(routed):
+            orc.mx_grouped_matmul(gr, pq, ps, inp.gmmWeight_q, inp.gmmWeight_s, q, q, routed)
+            flops += 2.0 * wl.H1 * wl.N1 * len(routed)
+        if len(shared):
+            orc.mx_grouped_matmul([wl.BS], inp.mmX_q, inp.mmX_s, inp.mmWeight_q[None], inp.mmWeight_s[None], q, q,
+                                  shared)
+            flops += 2.0 * wl.H2 * wl.N2 * len(shared)
+        rows += chunk
+    el = time.perf_counter() - t0
+    desc = (f"{rows} output rows drawn uniformly, with repeats, from the {total_rows} rows of gmmY and mmY of "
+            f"{wl.name} in mx {inp.qtype} (float64 oracle, full K per row)")
+    return flops, el, rows, orc.num_threads(), desc
+
+
+def run_mx(args):
+    """The hot path with block-scaled FP8 operands (a2av_gmm_mx_run), weak scaling under torchrun."""
+    from token_permute_grouped_gb300.workloads import make_mx_inputs
+    world, rank, local = dist_env()
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = make_mx_inputs(wl, seed=0, qtype=args.mx_qtype)
+        per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+        for _ in range(args.warmup):
+            mx_oracle_sample(wl, inp, per_step / 4)
+        tot_f = tot_s = 0.0
+        threads, desc = 1, ""
+        for i in range(args.steps):
+            f, sec, _, threads, desc = mx_oracle_sample(wl, inp, per_step, seed=i + 1)
+            tot_f += f
+            tot_s += sec
+        tf = tot_f / tot_s / 1e12
+        print(json.dumps({
+            "impl": "reference", "metric": MX_METRIC, "value": round(tf, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s * 1e3 / max(1, args.steps), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name + "_mx_" + args.mx_qtype, "A": inp.A, "seconds_per_step": per_step},
+            "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}), flush=True)
+        return
+    assert torch.cuda.is_available(), "bench.py needs a GPU (use --impl reference for the CPU oracle)"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    build.build()
+    binding.load()
+    inp = make_mx_inputs(wl, seed=0, rank=rank, qtype=args.mx_qtype)
+    A = inp.A
+    plan = binding.MxPlan(wl.W, wl.e, A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, args.mx_qtype, device=dev)
+    nbytes = mx_bytes(wl, A)
+    reps = min(64, max(2, -(-3 * L2_BYTES // nbytes)))
+    names = ("ataOut_q", "ataOut_s", "gmmWeight_q", "gmmWeight_s", "mmX_q", "mmX_s", "mmWeight_q", "mmWeight_s")
+    sets = []
+    for _ in range(reps):
+        st = {k: (getattr(inp, k).to(dev) if getattr(inp, k) is not None else None) for k in names}
+        st["gmmY"] = torch.empty(A, wl.N1, dtype=torch.bfloat16, device=dev)
+        st["mmY"] = torch.empty(wl.BS, wl.N2, dtype=torch.bfloat16, device=dev) if wl.BS else None
+        sets.append(st)
+    rc_dev = torch.from_numpy(inp.recvCounts).to(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        st = sets[i % reps]
+        plan.run(st["ataOut_q"], st["ataOut_s"], rc_dev, st["gmmWeight_q"], st["gmmWeight_s"], st["mmX_q"],
+                 st["mmX_s"], st["mmWeight_q"], st["mmWeight_s"], gmmY=st["gmmY"], mmY=st["mmY"], stream=stream)
+
+    sync = torch.cuda.synchronize
+    for i in range(args.warmup):
+        step(i)
+    sync()
+    code = binding.a2av_gmm_read_device_status(plan.workspace)
+    if code[0] != 0:
+        raise RuntimeError(f"device status {code}")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+
+    def timed_step(i):
+        if i == 0:
+            ev[0].record(stream)
+        step(i)
+        ev[i + 1].record(stream)
+
+    with ClockSampler(local) as clocks:
+        timed_region(timed_step, args.steps, world, dev, sync)
+    per_call_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    dev_s = sum(per_call_ms) / 1e3
+    dev_s_max = reduce_max(dev_s, world, dev)
+    flops = flops_of(wl, A)
+    tflops = reduce_sum(flops * args.steps, world, dev) / dev_s_max / 1e12
+
+    # End to end through the same call: codes and scales of this step's
+    # activations in from pinned memory, the bf16 results back out (weights resident).
+    pin_q, pin_s = inp.ataOut_q.pin_memory(), inp.ataOut_s.pin_memory()
+    pin_xq = inp.mmX_q.pin_memory() if wl.BS else None
+    pin_xs = inp.mmX_s.pin_memory() if wl.BS else None
+    out_y = torch.empty(A, wl.N1, dtype=torch.bfloat16).pin_memory()
+    out_m = torch.empty(wl.BS, wl.N2, dtype=torch.bfloat16).pin_memory() if wl.BS else None
+    h2d = pin_q.numel() + pin_s.numel() + (pin_xq.numel() + pin_xs.numel() if wl.BS else 0) + rc_dev.numel() * 4
+    d2h = out_y.numel() * 2 + (out_m.numel() * 2 if wl.BS else 0)
+    rc_pin = torch.from_numpy(inp.recvCounts).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step(i):
+        st = sets[i % 2]
+        st["ataOut_q"].copy_(pin_q, non_blocking=True)
+        st["ataOut_s"].copy_(pin_s, non_blocking=True)
+        rc_dev.copy_(rc_pin, non_blocking=True)
+        if wl.BS:
+            st["mmX_q"].copy_(pin_xq, non_blocking=True)
+            st["mmX_s"].copy_(pin_xs, non_blocking=True)
+        step(i % 2)
+        out_y.copy_(st["gmmY"], non_blocking=True)
+        if wl.BS:
+            out_m.copy_(st["mmY"], non_blocking=True)
+
+    _, e2e_max = timed_region(e2e_step, e2e_steps, world, dev, sync)
+    e2e_tflops = reduce_sum(flops * e2e_steps, world, dev) / e2e_max / 1e12
+    if rank != 0:
+        barrier(world)
+        return
+    pk, pk_kind = peaks()
+    peak = 2.0 * pk["bf16_tflops"]  # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
+    achieved = flops / (dev_s / args.steps) / 1e12
+    line = {
+        "metric": MX_METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dev_s_max * 1e3 / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": args.mx_qtype,
+        "data": "synthetic (seeded routing and N(0,1) tensors, mx-quantised per 32 along K; no dataset)",
+        "config": {"workload": wl.name + "_mx_" + args.mx_qtype, "W": wl.W, "e": wl.e, "A": A, "H1": wl.H1,
+                   "N1": wl.N1, "BS": wl.BS, "H2": wl.H2, "N2": wl.N2, "accumulate": "fp32", "out": "bf16",
+                   "us_per_call_median": round(statistics.median(per_call_ms) * 1e3, 2),
+                   "pct_of_fp8_peak": round(100 * tflops / world / peak, 2),
+                   "gflop_per_call": round(flops / 1e9, 3),
+                   "l2": f"inputs rotated over {reps} replicas ({reps * nbytes / 2**20:.0f} MiB > 129 MiB L2)",
+                   "launches_per_call": 3 if A else 1},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": "grouped_gemm_mx_kernel",
+                     "peak_source": f"2 x {pk_kind} bf16 dense burst (nominal FP8:bf16 ratio 4.5:2.25)",
+                     "algorithmic_bytes": nbytes},
+        "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
+                "inputs_copied": "activation codes and scales, recvCounts, mmX codes and scales (weights resident)"},
+        "gpu_launches": (3 if A else 1) * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        f, sec, _, threads, desc = mx_oracle_sample(wl, inp, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(f / sec / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle", "sample": desc, "seconds": round(sec, 2)}
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -786,9 +971,10 @@ def main(argv=None):
     ap.add_argument("--path", default="default", choices=["default", "fused", "split", "split_runs"])
     ap.add_argument("--tiles", default="default", choices=["default", "single", "pair", "pair_k64"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="gemm", choices=["gemm", "amp", "qreduce", "layer"],
+    ap.add_argument("--mx-qtype", default="e4m3fn", choices=["e4m3fn", "e5m2"], help="--op mx: code format")
+    ap.add_argument("--op", default="gemm", choices=["gemm", "amp", "qreduce", "layer", "mx"],
                     help="gemm: the hot path (default); amp: the loss-scale step; qreduce: the quantised "
-                         "rank reduce; layer: AlltoAllv + the hot path")
+                         "rank reduce; layer: AlltoAllv + the hot path; mx: the hot path in block-scaled FP8")
     ap.add_argument("--overlap", action="store_true",
                     help="--op layer: run the shared expert beside the row exchange (default: with the routed experts)")
     ap.add_argument("--qworkload", default="qreduce_mx_e4m3_w8_rows1536_h7168",
@@ -801,6 +987,8 @@ def main(argv=None):
         run_qreduce(args)
     elif args.op == "layer":
         run_layer(args)
+    elif args.op == "mx":
+        run_mx(args)
     elif args.impl == "reference":
         run_reference(args)
     elif args.op == "amp":

@@ -158,6 +158,40 @@ def test_quant_reduce_argument_checks(lib, kw, status):
     assert qr(lib, **kw) == status
 
 
+def mx_ws(**kw):
+    base = dict(W=8, e=4, A=16000, H1=4096, N1=1024, BS=2048, H2=4096, N2=1024, qtype=0, want_permute_out=0)
+    base.update(kw)
+    d = binding.MxDesc(*(base[k] for k in ("W", "e", "A", "H1", "N1", "BS", "H2", "N2", "qtype",
+                                            "want_permute_out")))
+    n = ctypes.c_size_t(0)
+    return binding.load().a2av_gmm_mx_workspace_size(ctypes.byref(d), ctypes.byref(n)), n.value
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, 0),
+    ({"qtype": 1}, 0),
+    ({"qtype": 2}, 2),                  # E4M3FN or E5M2 codes only
+    ({"e": 33}, 2),
+    ({"W": 9, "e": 32}, 2),
+    ({"H1": 65536}, 2),
+    ({"H2": 12800}, 2),
+    ({"A": -1}, 2),
+    ({"H1": 4096 + 128}, 3),            # scale rows of H/32 bytes must be 16-byte multiples
+    ({"H2": 1024 + 256}, 3),
+    ({"N1": 1020}, 3),
+    ({"BS": 0, "H2": 0, "N2": 0}, 0),
+])
+def test_mx_phase1_validation(lib, kw, status):
+    assert mx_ws(**kw)[0] == status
+
+
+def test_mx_workspace_sizes(lib):
+    st, n = mx_ws(A=1000, H1=512)
+    assert st == 0 and n == 256 + 512000 + 16128  # status + codes + scales, each padded to 256 B
+    assert mx_ws(A=1000, H1=512, want_permute_out=1)[1] == 256
+    assert mx_ws(A=0)[1] == 256
+
+
 def test_status_strings(lib):
     for code in range(7):
         assert binding.a2av_gmm_status_string(code)

@@ -1,0 +1,161 @@
+"""Block-scaled FP8 (mx) grouped GEMM on the GPU against the float64 oracle (needs a GB300).
+
+include/a2av_gmm_mx.h: gmmY = permuteOut x gmmWeight and mmY = mmX x mmWeight
+with E4M3FN/E5M2 codes and one E8M0 scale per 32 elements along K
+("aclnnQuantReduceScatter" page, Constraints, for the format).  permuteOut
+(codes and scales) must be bit-exact; gmmY and mmY must satisfy the path's
+tolerance |gpu - ref| <= 2e-2 * max(1, |ref|) against the oracle's float64
+sum.  Where every partial sum is a small integer the fp32 accumulator is
+exact in any order, so the output must be the bf16 rounding of the oracle's
+value, bit for bit; the scale-layout cases are built that way.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_close
+from token_permute_grouped_gb300 import binding, build
+from token_permute_grouped_gb300.workloads import (HEADLINE, WORKLOADS, make_mx_inputs, mx_quantize,
+                                                   random_counts, MxInputs, Workload)
+
+pytestmark = pytest.mark.gpu
+QCODE = {"e4m3fn": 0, "e5m2": 1}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build.build()
+
+
+def run_mx(inp: MxInputs, want_perm=False):
+    dev = torch.device("cuda:0")
+    wl = inp.wl
+    plan = binding.MxPlan(wl.W, wl.e, inp.A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, inp.qtype, want_perm, dev)
+    d = lambda t: None if t is None else t.to(dev)
+    out = plan.run(d(inp.ataOut_q), d(inp.ataOut_s), torch.from_numpy(inp.recvCounts).to(dev),
+                   d(inp.gmmWeight_q), d(inp.gmmWeight_s), d(inp.mmX_q), d(inp.mmX_s), d(inp.mmWeight_q),
+                   d(inp.mmWeight_s))
+    torch.cuda.synchronize()
+    st = binding.a2av_gmm_read_device_status(plan.workspace)
+    return [None if t is None else t.cpu() for t in out], st
+
+
+def reference(orc, inp: MxInputs, rows=None, shared_rows=None):
+    """(expert-major codes, scales, gmmY rows, mmY rows) from the oracle."""
+    wl = inp.wl
+    q = QCODE[inp.qtype]
+    perm_q = orc.permute(wl.W, wl.e, inp.recvCounts, inp.ataOut_q.view(torch.int16)).view(torch.uint8)
+    perm_s = orc.permute(wl.W, wl.e, inp.recvCounts, inp.ataOut_s.view(torch.int16)).view(torch.uint8)
+    _, _, groups, _ = orc.plan(wl.W, wl.e, inp.recvCounts, inp.A)
+    y = orc.mx_grouped_matmul(groups, perm_q, perm_s, inp.gmmWeight_q, inp.gmmWeight_s, q, q, rows) if inp.A else None
+    m = None
+    if wl.BS:
+        m = orc.mx_grouped_matmul([wl.BS], inp.mmX_q, inp.mmX_s, inp.mmWeight_q[None], inp.mmWeight_s[None], q, q,
+                                  shared_rows)
+    return perm_q, perm_s, y, m
+
+
+def _custom(W, e, H1, N1, rc, qtype="e4m3fn", BS=0, H2=0, N2=0, seed=0):
+    wl = Workload(f"mx_w{W}e{e}", W=W, e=e, H1=H1, N1=N1, dtype="bf16", routing="uniform",
+                  BS=BS, H2=H2, N2=N2)
+    return make_mx_inputs(wl, seed=seed, qtype=qtype, recvCounts=np.asarray(rc, np.int32))
+
+
+def _ones_case(sa, sw, A=128, H1=512, N1=128):
+    """Every code E4M3 1.0 with the given scale codes: out[m][n] = 32 sum_b 2^(sa[m,b]+sw[n,b]-254)."""
+    wl = Workload("mx_ones", W=1, e=1, H1=H1, N1=N1, dtype="bf16", routing="uniform")
+    return MxInputs(wl, "e4m3fn", np.array([A], np.int32), torch.full((A, H1), 0x38, dtype=torch.uint8),
+                    sa, torch.full((1, N1, H1), 0x38, dtype=torch.uint8), sw)
+
+
+def _layout_cases():
+    A, N1, kb = 128, 128, 16
+    one_a = torch.full((A, kb), 127, dtype=torch.uint8)
+    one_w = torch.full((1, N1, kb), 127, dtype=torch.uint8)
+    rows = (127 + torch.arange(A) % 5)[:, None].repeat(1, kb).to(torch.uint8)
+    cols = (127 + torch.arange(N1) % 5)[None, :, None].repeat(1, 1, kb).to(torch.uint8)
+    blocks_a = (127 + torch.arange(kb) % 4)[None, :].repeat(A, 1).to(torch.uint8)
+    blocks_w = (127 + torch.arange(kb) % 4)[None, None, :].repeat(1, N1, 1).to(torch.uint8)
+    mixed = (120 + (torch.arange(A)[:, None] + 3 * torch.arange(kb)[None, :]) % 11).to(torch.uint8)
+    return {"unit": (one_a, one_w), "per_row": (rows, one_w), "per_column": (one_a, cols),
+            "per_block_a": (blocks_a, one_w), "per_block_b": (one_a, blocks_w), "row_and_block": (mixed, blocks_w)}
+
+
+@pytest.mark.parametrize("case", list(_layout_cases()))
+def test_scale_placement_exact(orc, case):
+    # Which E8M0 byte scales which row, column and K-block: every output is
+    # an exact small power-of-two sum, so the bf16 result must be bit-exact.
+    sa, sw = _layout_cases()[case]
+    inp = _ones_case(sa, sw, H1=512)
+    (y, _, _, _), st = run_mx(inp)
+    assert st[0] == 0, st
+    _, _, ref, _ = reference(orc, inp)
+    want = torch.from_numpy(ref).to(torch.bfloat16)
+    assert torch.equal(y.view(torch.int16), want.view(torch.int16)), (y[:2, :4], want[:2, :4])
+
+
+@pytest.mark.parametrize("qtype", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("W,e,H1,N1,A,zero,BS,H2,N2", [
+    (2, 2, 512, 128, 300, 0.0, 0, 0, 0),
+    (4, 3, 1024, 200, 700, 0.3, 100, 512, 136),
+    (8, 4, 2048, 256, 1500, 0.1, 257, 1024, 384),
+])
+def test_matches_oracle(orc, qtype, W, e, H1, N1, A, zero, BS, H2, N2):
+    rc = random_counts(W, e, A, seed=A + W, zero_prob=zero)
+    inp = _custom(W, e, H1, N1, rc, qtype, BS, H2, N2, seed=W)
+    (y, m, _, _), st = run_mx(inp)
+    assert st[0] == 0, st
+    _, _, ref_y, ref_m = reference(orc, inp)
+    assert_close(y, ref_y, "gmmY")
+    if BS:
+        assert_close(m, ref_m, "mmY")
+
+
+def test_permute_out_bit_exact_and_same_products(orc):
+    rc = random_counts(4, 2, 600, seed=5, zero_prob=0.25)
+    inp = _custom(4, 2, 1024, 128, rc, "e4m3fn", seed=5)
+    (y, _, pq, ps), st = run_mx(inp, want_perm=True)
+    assert st[0] == 0, st
+    ref_q, ref_s, _, _ = reference(orc, inp)
+    assert torch.equal(pq, ref_q) and torch.equal(ps, ref_s)
+    (y2, _, _, _), st = run_mx(inp, want_perm=False)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+def test_integer_products_bit_exact(orc):
+    # Codes of small integers (E4M3 1, 2, 3, 4 and negatives) at unit scale:
+    # every partial sum is an integer below 2^24, exact in fp32 in any order.
+    rng = np.random.default_rng(4)
+    vals = np.array([0x38, 0x40, 0x44, 0x48, 0xB8, 0xC0, 0x00], np.uint8)
+    rc = np.array([40, 0, 90, 30], np.int32)  # W = 2, e = 2
+    wl = Workload("mx_int", W=2, e=2, H1=512, N1=64, dtype="bf16", routing="uniform")
+    A = int(rc.sum())
+    inp = MxInputs(wl, "e4m3fn", rc, torch.from_numpy(vals[rng.integers(0, 7, (A, 512))]),
+                   torch.full((A, 16), 127, dtype=torch.uint8),
+                   torch.from_numpy(vals[rng.integers(0, 7, (2, 64, 512))]), torch.full((2, 64, 16), 127, dtype=torch.uint8))
+    (y, _, _, _), st = run_mx(inp)
+    assert st[0] == 0, st
+    _, _, ref, _ = reference(orc, inp)
+    assert torch.equal(y.view(torch.int16), torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16))
+
+
+def test_bad_counts_are_reported(orc):
+    inp = _custom(2, 2, 512, 128, [10, 20, 30, 40], seed=1)
+    inp.recvCounts = np.array([10, 20, 30, 41], np.int32)  # sums to A + 1
+    _, st = run_mx(inp)
+    assert st[0] == 6 and st[1] & 1, st  # A2AV_ERR_DEVICE_CHECK, bad-counts bit in the status word
+
+
+def test_full_size_headline(orc):
+    # The 8-rank x 4-expert workload in mx form, compared on sampled rows.
+    inp = make_mx_inputs(WORKLOADS[HEADLINE], seed=0, qtype="e4m3fn")
+    (y, m, _, _), st = run_mx(inp)
+    assert st[0] == 0, st
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, inp.A - 1], rng.integers(0, inp.A, 48)]))
+    srows = np.unique(np.concatenate([[0, inp.wl.BS - 1], rng.integers(0, inp.wl.BS, 16)]))
+    _, _, ref_y, ref_m = reference(orc, inp, rows=rows, shared_rows=srows)
+    assert_close(y[rows], ref_y, "gmmY")
+    assert_close(m[srows], ref_m, "mmY")

@@ -28,7 +28,8 @@ TILES = {"default": 0, "single": 1, "pair": 2, "pair_k64": 3}
 # Every function the headers under include/ declare.
 EXPORTS = ("a2av_gmm_workspace_size", "a2av_gmm_run", "a2av_gmm_read_device_status",
            "a2av_gmm_status_string", "a2av_gmm_launch_count", "a2av_gmm_run_static_scratch",
-           "a2av_amp_update_scale", "a2av_found_nonfinite", "a2av_quant_reduce")
+           "a2av_amp_update_scale", "a2av_found_nonfinite", "a2av_quant_reduce",
+           "a2av_gmm_mx_workspace_size", "a2av_gmm_mx_run")
 
 # a2av_qtype / a2av_qmode of include/a2av_quant_reduce.h.
 QTYPES = {"e4m3fn": 0, "e5m2": 1, "int8": 2}
@@ -47,6 +48,14 @@ class Desc(ctypes.Structure):
                 ("BS", ctypes.c_int64), ("H2", ctypes.c_int64), ("N2", ctypes.c_int64),
                 ("dtype", ctypes.c_int32), ("want_permute_out", ctypes.c_int32),
                 ("path", ctypes.c_int32), ("tiles", ctypes.c_int32)]
+
+
+class MxDesc(ctypes.Structure):
+    """a2av_gmm_mx_desc of include/a2av_gmm_mx.h."""
+    _fields_ = [("W", ctypes.c_int32), ("e", ctypes.c_int32),
+                ("A", ctypes.c_int64), ("H1", ctypes.c_int64), ("N1", ctypes.c_int64),
+                ("BS", ctypes.c_int64), ("H2", ctypes.c_int64), ("N2", ctypes.c_int64),
+                ("qtype", ctypes.c_int32), ("want_permute_out", ctypes.c_int32)]
 
 
 _lib = None
@@ -82,6 +91,10 @@ def load():
         L.a2av_found_nonfinite.restype = ctypes.c_int
         L.a2av_quant_reduce.argtypes = [i32, ctypes.c_int64, ctypes.c_int64, i32, i32, p, p, p, i32, p]
         L.a2av_quant_reduce.restype = ctypes.c_int
+        L.a2av_gmm_mx_workspace_size.argtypes = [ctypes.POINTER(MxDesc), ctypes.POINTER(sz)]
+        L.a2av_gmm_mx_workspace_size.restype = ctypes.c_int
+        L.a2av_gmm_mx_run.argtypes = [ctypes.POINTER(MxDesc)] + [p] * 14 + [sz, p]
+        L.a2av_gmm_mx_run.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -252,3 +265,58 @@ def a2av_gmm(ataOut, recvCounts, gmmWeight, mmX=None, mmWeight=None, return_perm
     plan = Plan(W, e, ataOut.shape[0], H1, N1, BS, H2, N2, gmmWeight.dtype, return_permute, path,
                 device=gmmWeight.device, tiles=tiles)
     return plan.run(ataOut, recvCounts, gmmWeight, mmX, mmWeight)
+
+
+class MxPlan:
+    """Descriptor + workspace of the block-scaled FP8 (mx) call for one shape
+    (include/a2av_gmm_mx.h): codes as uint8 tensors, E8M0 scales as uint8
+    tensors with one byte per 32 codes along K, weights [e, N1, H1]."""
+
+    def __init__(self, W, e, A, H1, N1, BS=0, H2=0, N2=0, qtype="e4m3fn", want_permute_out=False, device=None):
+        self.desc = MxDesc(W, e, A, H1, N1, BS, H2, N2, QTYPES[qtype], int(bool(want_permute_out)))
+        self.device = torch.device(device) if device is not None else torch.device("cuda")
+        n = ctypes.c_size_t(0)
+        st = load().a2av_gmm_mx_workspace_size(ctypes.byref(self.desc), ctypes.byref(n))
+        if st != A2AV_OK:
+            raise A2avError(st, "a2av_gmm_mx_workspace_size")
+        self.workspace = torch.empty(n.value, dtype=torch.uint8, device=self.device)
+
+    def run(self, ataOut_q, ataOut_s, recvCounts, gmmWeight_q, gmmWeight_s, mmX_q=None, mmX_s=None,
+            mmWeight_q=None, mmWeight_s=None, gmmY=None, mmY=None, permuteOut_q=None, permuteOut_s=None,
+            stream=None):
+        """Returns (gmmY, mmY, permuteOut_q, permuteOut_s); outputs are bf16."""
+        d = self.desc
+        for t, name in ((ataOut_q, "ataOut_q"), (ataOut_s, "ataOut_s")):
+            if d.A:
+                _check(t, name, torch.uint8, 2)
+        _check(recvCounts, "recvCounts", torch.int32, 1)
+        _check(gmmWeight_q, "gmmWeight_q", torch.uint8, 3)
+        _check(gmmWeight_s, "gmmWeight_s", torch.uint8, 3)
+        if tuple(gmmWeight_q.shape) != (d.e, d.N1, d.H1) or tuple(gmmWeight_s.shape) != (d.e, d.N1, d.H1 // 32):
+            raise ValueError("gmmWeight_q must be [e, N1, H1] and gmmWeight_s [e, N1, H1/32]")
+        if d.A and (tuple(ataOut_q.shape) != (d.A, d.H1) or tuple(ataOut_s.shape) != (d.A, d.H1 // 32)):
+            raise ValueError("ataOut_q must be [A, H1] and ataOut_s [A, H1/32]")
+        if gmmY is None:
+            gmmY = torch.empty(d.A, d.N1, dtype=torch.bfloat16, device=self.device)
+        if d.want_permute_out:
+            if permuteOut_q is None:
+                permuteOut_q = torch.empty(d.A, d.H1, dtype=torch.uint8, device=self.device)
+            if permuteOut_s is None:
+                permuteOut_s = torch.empty(d.A, d.H1 // 32, dtype=torch.uint8, device=self.device)
+        if d.BS:
+            for t, name in ((mmX_q, "mmX_q"), (mmX_s, "mmX_s"), (mmWeight_q, "mmWeight_q"),
+                            (mmWeight_s, "mmWeight_s")):
+                _check(t, name, torch.uint8, 2)
+            if mmY is None:
+                mmY = torch.empty(d.BS, d.N2, dtype=torch.bfloat16, device=self.device)
+        s = stream if stream is not None else torch.cuda.current_stream()
+        st = load().a2av_gmm_mx_run(
+            ctypes.byref(d), _ptr(ataOut_q) if d.A else None, _ptr(ataOut_s) if d.A else None, _ptr(recvCounts),
+            _ptr(gmmWeight_q), _ptr(gmmWeight_s), _ptr(mmX_q) if d.BS else None, _ptr(mmX_s) if d.BS else None,
+            _ptr(mmWeight_q) if d.BS else None, _ptr(mmWeight_s) if d.BS else None,
+            _ptr(permuteOut_q) if d.want_permute_out else None, _ptr(permuteOut_s) if d.want_permute_out else None,
+            _ptr(gmmY) if d.A else None, _ptr(mmY) if d.BS else None, _ptr(self.workspace), self.workspace.numel(),
+            ctypes.c_void_p(s.cuda_stream))
+        if st != A2AV_OK:
+            raise A2avError(st, "a2av_gmm_mx_run")
+        return gmmY, mmY, permuteOut_q, permuteOut_s

@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liba2av_gmm.so")
-SOURCES = ["api.cu", "permute.cu", "grouped_gemm.cu", "amp.cu", "quant_reduce.cu"]
+SOURCES = ["api.cu", "permute.cu", "grouped_gemm.cu", "grouped_gemm_mx.cu", "amp.cu", "quant_reduce.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -358,3 +358,64 @@ def quant_reduce_inputs(W: int, rows: int, H: int, qtype: str, mode: str, seed: 
     else:
         sc = np.exp2(rng.uniform(lo, hi, W * rows * (H // 128))).astype(np.float32).reshape(W, rows, H // 128)
     return torch.from_numpy(data.reshape(W, rows, H)), torch.from_numpy(sc)
+
+
+# --- Block-scaled FP8 (mx) operands --------------------------------------------
+#
+# The mx variant of a workload draws the same float32 tensors as make_inputs
+# and quantises each 32-element block along K the OCP MX way: the block's
+# E8M0 scale is 2^(floor(log2 amax) - emax) with emax the format's largest
+# exponent (8 for E4M3FN, 15 for E5M2); the codes are the scaled values
+# rounded to the format by torch's own float8 cast (saturating at the largest
+# finite value).  Weights are stored K-contiguous per output column: [e, N1, H1].
+
+_F8 = {"e4m3fn": (torch.float8_e4m3fn, 8, 448.0), "e5m2": (torch.float8_e5m2, 15, 57344.0)}
+
+
+def mx_quantize(x: torch.Tensor, qtype: str) -> tuple[torch.Tensor, torch.Tensor]:
+    """float32 [..., K] (K % 32 == 0) -> (uint8 codes [..., K], uint8 E8M0 scales [..., K/32])."""
+    f8, emax, fmax = _F8[qtype]
+    xb = x.reshape(*x.shape[:-1], x.shape[-1] // 32, 32)
+    amax = xb.abs().amax(-1)
+    e = torch.where(amax > 0, torch.floor(torch.log2(amax)), torch.full_like(amax, -127.0)) - emax
+    e = e.clamp(-127, 127)
+    codes = (xb / torch.exp2(e)[..., None]).clamp(-fmax, fmax).to(f8).view(torch.uint8)
+    return codes.reshape(x.shape), (e + 127).to(torch.uint8)
+
+
+@dataclasses.dataclass
+class MxInputs:
+    wl: Workload
+    qtype: str
+    recvCounts: np.ndarray           # int32 [W*e]
+    ataOut_q: torch.Tensor           # [A, H1] codes
+    ataOut_s: torch.Tensor           # [A, H1/32] E8M0
+    gmmWeight_q: torch.Tensor        # [e, N1, H1]
+    gmmWeight_s: torch.Tensor        # [e, N1, H1/32]
+    mmX_q: torch.Tensor | None = None
+    mmX_s: torch.Tensor | None = None
+    mmWeight_q: torch.Tensor | None = None  # [N2, H2]
+    mmWeight_s: torch.Tensor | None = None
+
+    @property
+    def A(self) -> int:
+        return int(self.ataOut_q.shape[0])
+
+
+def make_mx_inputs(wl: Workload, seed: int = 0, rank: int = 0, qtype: str = "e4m3fn",
+                   recvCounts=None) -> MxInputs:
+    """The mx operands of one rank (CPU tensors): the float32 draws of make_inputs, quantised."""
+    rc = recv_counts(wl, seed, rank) if recvCounts is None else np.asarray(recvCounts, np.int32)
+    seed = seed + rank
+    A = int(rc.astype(np.int64).sum())
+    act = torch.from_numpy(normal_f32(A * wl.H1, seed, STREAM_ATAOUT)).reshape(A, wl.H1)
+    aq, as_ = mx_quantize(act, qtype)
+    wt = torch.from_numpy(normal_f32(wl.e * wl.H1 * wl.N1, seed, STREAM_GMM_WEIGHT)).reshape(wl.e, wl.H1, wl.N1)
+    wq, ws = mx_quantize(wt.transpose(1, 2).contiguous() * (1.0 / math.sqrt(wl.H1)), qtype)
+    out = MxInputs(wl, qtype, rc, aq, as_, wq, ws)
+    if wl.BS:
+        x = torch.from_numpy(normal_f32(wl.BS * wl.H2, seed, STREAM_MMX)).reshape(wl.BS, wl.H2)
+        out.mmX_q, out.mmX_s = mx_quantize(x, qtype)
+        wm = torch.from_numpy(normal_f32(wl.H2 * wl.N2, seed, STREAM_MM_WEIGHT)).reshape(wl.H2, wl.N2)
+        out.mmWeight_q, out.mmWeight_s = mx_quantize(wm.t().contiguous() * (1.0 / math.sqrt(wl.H2)), qtype)
+    return out
