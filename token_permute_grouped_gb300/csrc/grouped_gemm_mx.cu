@@ -8,22 +8,23 @@
 // apply the scales themselves (tcgen05.mma kind::mxf8f6f4 with block_scale):
 // an MMA of K = 32 takes one E8M0 scale per A row and per B column from TMEM.
 //
-// Tiles: 128 rows x 128 columns per CTA (cta_group::1); K in stages of 128
-// codes (128 bytes: one 128-byte swizzle row, four MMAs).  Per CTA:
+// Tiles: 128 rows x 128 columns per CTA (cta_group::1); K in stages of 256
+// codes: two 128-byte swizzle rows per operand row (two 16 KB sub-tiles),
+// eight MMAs.  Per CTA:
 //   warp 0     one thread issues a stage's TMA loads: 128 expert-major A rows
 //              (staged by the permute kernel) and 128 K-major weight columns,
-//              16 KB each.
+//              one 4-D load of both sub-tiles per operand.
 //   warp 1     one thread issues the MMAs.
 //   warps 2-5  scales: lane l loads the E8M0 scales of tile rows and tile
-//              columns l, 32 + l, 64 + l, 96 + l, 16 bytes (four stages) at a
-//              time, and writes each stage's 32-bit words (byte i for MMA i)
-//              into TMEM with tcgen05.st: 32 lanes x 4 columns per operand,
-//              the layout the MMA reads, in the warp's own lane quarter (each
-//              quarter holds a copy).
+//              columns l, 32 + l, 64 + l, 96 + l, 16 bytes (two stages) at a
+//              time, and writes each stage's two 32-bit words per row (byte i
+//              of word j for MMA 4j + i) into TMEM with tcgen05.st: per word,
+//              32 lanes x 4 columns, the layout the MMA reads, in the warp's
+//              own lane quarter (each quarter holds a copy).
 //   warps 6-9  epilogue: TMEM -> registers -> bf16 (nearest even) -> global,
 //              rows past the group's end and columns past N masked.
 // TMEM: two 128-column fp32 accumulators (the epilogue of one tile overlaps
-// the main loop of the next), then per stage four A-scale and four B-scale
+// the main loop of the next), then per stage eight A-scale and eight B-scale
 // columns.  Every wait is bounded: on timeout the CTA sets kStatusTimeout and
 // winds down.
 #include <cuda_bf16.h>
@@ -44,21 +45,25 @@ namespace {
 
 constexpr int MX_BM = 128;  // rows per tile
 constexpr int MX_BN = 128;  // columns per tile
-constexpr int MX_BK = 128;  // K (codes = bytes) per stage
-constexpr int MX_STAGES = 6;
+constexpr int MX_KCHUNK = 128;  // codes (bytes) in one 128-byte swizzle row
+constexpr int MX_CH = 2;         // K chunks per stage
+constexpr int MX_BK = MX_KCHUNK * MX_CH;
+constexpr int MX_STAGES = 3;
 constexpr int MX_THREADS = 10 * 32;
 constexpr int kMxMmaWarp = 1;
 constexpr int kMxScaleWarp0 = 2;
 constexpr int kMxEpiWarp0 = 6;
-constexpr uint32_t MX_TILE_BYTES = MX_BM * MX_BK;  // 16 KB; a B stage is the same
+constexpr uint32_t MX_SUB_BYTES = MX_BM * MX_KCHUNK;   // 16 KB: 128 rows x one chunk
+constexpr uint32_t MX_TILE_BYTES = MX_SUB_BYTES * MX_CH;  // one operand's stage; B is the same size
 constexpr uint32_t kMxTmemCols = 512;
 constexpr uint32_t kMxAccCols = 128;
 constexpr uint32_t kMxSfCol0 = 2 * kMxAccCols;
 constexpr uint64_t kMxWaitLimitNs = 2000000000ull;
 
-__host__ __device__ constexpr uint32_t sfa_col(int s) { return kMxSfCol0 + 8u * s; }
-__host__ __device__ constexpr uint32_t sfb_col(int s) { return kMxSfCol0 + 8u * s + 4u; }
-static_assert(sfb_col(MX_STAGES - 1) + 4 <= kMxTmemCols, "scale columns must fit the TMEM allocation");
+// Per stage: A scales in 4 columns per word (2 words), then B scales likewise.
+__host__ __device__ constexpr uint32_t sfa_col(int s) { return kMxSfCol0 + 16u * s; }
+__host__ __device__ constexpr uint32_t sfb_col(int s) { return kMxSfCol0 + 16u * s + 8u; }
+static_assert(sfb_col(MX_STAGES - 1) + 8 <= kMxTmemCols, "scale columns must fit the TMEM allocation");
 
 struct MxLaunch {
     const int32_t *recvCounts;
@@ -74,10 +79,12 @@ struct MxLaunch {
     int32_t write_status;
     int32_t qtype;  // 0 E4M3FN, 1 E5M2 (both operands)
     int32_t grid;
-    CUtensorMap tmA;   // expert-major codes [A, H1], box 128 x 128
-    CUtensorMap tmB;   // weight codes {H1, N1, e}, box 128 x 128 x 1
+    // Code maps, all 4-D {128 codes, rows, K / 128 chunks, groups}, box
+    // 128 x 128 x 2 x 1: one load is a stage's two 16 KB sub-tiles.
+    CUtensorMap tmA;   // expert-major codes [A, H1]
+    CUtensorMap tmB;   // weight codes [e, N1, H1]
     CUtensorMap tmX;   // mmX codes [BS, H2]
-    CUtensorMap tmMW;  // mmWeight codes {H2, N2, 1}
+    CUtensorMap tmMW;  // mmWeight codes [N2, H2]
 };
 
 struct MxGroup {
@@ -150,13 +157,21 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
-// Thread i of the warp writes four 32-bit words to lane (quarter base + i),
-// columns [col, col + 4).
-__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2,
-                                                  uint32_t v3) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
-                 "r"(v2), "r"(v3)
+// Thread i of the warp writes eight 32-bit words to lane (quarter base + i),
+// columns [col, col + 8).
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                  : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_mx(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y,
+                                               int32_t z, int32_t w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -274,9 +289,9 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     }
                     const uint32_t fb = smem_u32(&C.full[s]);
                     mbar_arrive_expect_tx(fb, 2 * MX_TILE_BYTES);
-                    // Every code map is 3-D {K, rows, groups}; A maps have one group.
-                    tma_load_3d(a_smem + s * MX_TILE_BYTES, ta, fb, kb * MX_BK, ya, 0);
-                    tma_load_3d(b_smem + s * MX_TILE_BYTES, tb, fb, kb * MX_BK, xn, z);
+                    // {chunk column, row, chunk, group}: both chunks of the stage.
+                    tma_load_4d_mx(a_smem + s * MX_TILE_BYTES, ta, fb, 0, ya, kb * MX_CH, 0);
+                    tma_load_4d_mx(b_smem + s * MX_TILE_BYTES, tb, fb, 0, xn, kb * MX_CH, z);
                 }
             }
             // Wait until the MMAs released every stage that was filled.
@@ -289,7 +304,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
             const uint32_t idesc0 = mx_idesc(static_cast<uint32_t>(p.qtype), MX_BM, MX_BN);
             // Both operands K-major with a 128-byte swizzle: 128-byte rows,
             // 8-row groups 1024 B apart; an MMA's K step of 32 codes is 32
-            // bytes along the row (2 in the 16-byte address field).
+            // bytes along the row (2 in the 16-byte address field), and the
+            // second chunk of a stage starts 16 KB further on.
             const uint64_t a_desc0 = smem_desc(a_smem, 16, 1024, kSwizzle128B);
             const uint64_t b_desc0 = smem_desc(b_smem, 16, 1024, kSwizzle128B);
             uint32_t it = 0, tl = 0;
@@ -315,8 +331,12 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     const uint32_t sfa = C.tmem_base + sfa_col(s);
                     const uint32_t sfb = C.tmem_base + sfb_col(s);
 #pragma unroll
-                    for (int kk = 0; kk < MX_BK / 32; ++kk)
-                        mma_mx(d_tmem, ad + 2 * kk, bd + 2 * kk, idesc0 | mx_sf_ids(kk), sfa, sfb, (kb | kk) != 0);
+                    for (int kk = 0; kk < MX_BK / 32; ++kk) {
+                        const uint32_t off = ((kk >> 2) * MX_SUB_BYTES + (kk & 3) * 32) >> 4;
+                        const uint32_t word = (kk >> 2) * 4;  // scale column group of this MMA
+                        mma_mx(d_tmem, ad + off, bd + off, idesc0 | mx_sf_ids(kk & 3), sfa + word, sfb + word,
+                               (kb | kk) != 0);
+                    }
                     mma_commit(smem_u32(&C.empty[s]));
                 }
                 if (ok) mma_commit(smem_u32(&C.tfull[acc]));
@@ -350,7 +370,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 sb[c] = bcol < N ? (shared ? p.mw_s + bcol * srow : p.w_s + (static_cast<int64_t>(w.g) * N + bcol) * srow)
                                  : nullptr;
             }
-            // Scales of four stages (16 bytes per row) at a time, one chunk ahead.
+            // Scales of two stages (16 bytes per row) at a time, one chunk ahead.
             const uint4 zero = make_uint4(0, 0, 0, 0);
             uint4 ca[4], cb[4], na[4], nb[4];
 #pragma unroll
@@ -360,16 +380,16 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 na[c] = nb[c] = zero;
             }
             for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                if ((kb & 3) == 0) {
+                if ((kb & 1) == 0) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         if (kb > 0) {
                             ca[c] = na[c];
                             cb[c] = nb[c];
                         }
-                        if (kb + 4 < kblocks) {
-                            na[c] = sa[c] ? __ldg(reinterpret_cast<const uint4 *>(sa[c] + (kb + 4) * 4)) : zero;
-                            nb[c] = sb[c] ? __ldg(reinterpret_cast<const uint4 *>(sb[c] + (kb + 4) * 4)) : zero;
+                        if (kb + 2 < kblocks) {  // a stage's 8 scale bytes per row; 16 bytes cover two
+                            na[c] = sa[c] ? __ldg(reinterpret_cast<const uint4 *>(sa[c] + (kb + 2) * 8)) : zero;
+                            nb[c] = sb[c] ? __ldg(reinterpret_cast<const uint4 *>(sb[c] + (kb + 2) * 8)) : zero;
                         }
                     }
                 }
@@ -381,11 +401,18 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     break;
                 }
                 tc_fence_after_sync();
-                const int j = kb & 3;
-                tmem_st_32x32b_x4(C.tmem_base + lane_base + sfa_col(s), word_of(ca[0], j), word_of(ca[1], j),
-                                  word_of(ca[2], j), word_of(ca[3], j));
-                tmem_st_32x32b_x4(C.tmem_base + lane_base + sfb_col(s), word_of(cb[0], j), word_of(cb[1], j),
-                                  word_of(cb[2], j), word_of(cb[3], j));
+                // Column 4j + c: word j of this stage for row (column) 32c + lane.
+                const int j0 = (kb & 1) * 2;
+                uint32_t wa[8], wb[8];
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        wa[4 * j + c] = word_of(ca[c], j0 + j);
+                        wb[4 * j + c] = word_of(cb[c], j0 + j);
+                    }
+                tmem_st_32x32b_x8(C.tmem_base + lane_base + sfa_col(s), wa);
+                tmem_st_32x32b_x8(C.tmem_base + lane_base + sfb_col(s), wb);
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
@@ -481,16 +508,18 @@ PFN_cuTensorMapEncodeTiled_v12000 mx_encode_fn() {
     return fn;
 }
 
-// Byte codes {K, rows, groups} (K contiguous); box 128 x 128 x 1, 128-byte swizzle.
+// Byte codes [groups][rows][K] seen as 4-D {128 codes, rows, K / 128 chunks,
+// groups}; box 128 x 128 x MX_CH x 1, 128-byte swizzle: one load lands a
+// stage's K chunks as consecutive 16 KB K-major sub-tiles.  Needs K % 256 == 0.
 bool mx_codes_map(CUtensorMap *m, const void *ptr, int64_t groups, int64_t rows, int64_t K) {
     auto fn = mx_encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
+    cuuint64_t dims[4] = {MX_KCHUNK, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K / MX_KCHUNK),
                           static_cast<cuuint64_t>(groups)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(K * rows)};
-    cuuint32_t box[3] = {MX_BK, MX_BM, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(K), MX_KCHUNK, static_cast<cuuint64_t>(K * rows)};
+    cuuint32_t box[4] = {MX_KCHUNK, MX_BM, MX_CH, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
