@@ -79,6 +79,7 @@ def algorithmic_bytes(wl, A, permute_out):
 # The sources each measured call depends on (kernels and host setup).
 GEMM_SOURCES = ("api.cu", "grouped_gemm.cu", "kernels.h", "permute.cu", "plan.cuh", "ptx.cuh")
 QREDUCE_SOURCES = ("quant_reduce.cu", "../../include/a2av_quant_reduce.h")
+MX_SOURCES = ("grouped_gemm_mx.cu", "permute.cu", "plan.cuh", "ptx.cuh", "kernels.h", "../../include/a2av_gmm_mx.h")
 
 
 def source_hash(names=GEMM_SOURCES):
@@ -92,7 +93,7 @@ def source_hash(names=GEMM_SOURCES):
 def profiled_traffic(workload, permute_out=False, path="default", tiles="default", kernel="grouped_gemm_kernel"):
     """DRAM bytes per launch of a kernel from a committed ncu summary, only
     while the kernel's sources are unchanged since the capture."""
-    names = QREDUCE_SOURCES if kernel == "quant_reduce_kernel" else GEMM_SOURCES
+    names = {"quant_reduce_kernel": QREDUCE_SOURCES, "grouped_gemm_mx_kernel": MX_SOURCES}.get(kernel, GEMM_SOURCES)
     for f in glob.glob(os.path.join(ROOT, "profiles", "*.json")):
         try:
             with open(f) as fh:
@@ -857,7 +858,8 @@ def run_mx(args):
     binding.load()
     inp = make_mx_inputs(wl, seed=0, rank=rank, qtype=args.mx_qtype)
     A = inp.A
-    plan = binding.MxPlan(wl.W, wl.e, A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, args.mx_qtype, device=dev)
+    mx_tiles = args.tiles if args.tiles in ("default", "single", "pair") else "default"
+    plan = binding.MxPlan(wl.W, wl.e, A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, args.mx_qtype, device=dev, tiles=mx_tiles)
     nbytes = mx_bytes(wl, A)
     reps = min(64, max(2, -(-3 * L2_BYTES // nbytes)))
     names = ("ataOut_q", "ataOut_s", "gmmWeight_q", "gmmWeight_s", "mmX_q", "mmX_s", "mmWeight_q", "mmWeight_s")
@@ -936,7 +938,8 @@ def run_mx(args):
         "warmup": args.warmup, "ms_per_step": round(dev_s_max * 1e3 / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": args.mx_qtype,
         "data": "synthetic (seeded routing and N(0,1) tensors, mx-quantised per 32 along K; no dataset)",
-        "config": {"workload": wl.name + "_mx_" + args.mx_qtype, "W": wl.W, "e": wl.e, "A": A, "H1": wl.H1,
+        "config": {"workload": wl.name + "_mx_" + args.mx_qtype, "tiles": mx_tiles, "W": wl.W, "e": wl.e, "A": A,
+                   "H1": wl.H1,
                    "N1": wl.N1, "BS": wl.BS, "H2": wl.H2, "N2": wl.N2, "accumulate": "fp32", "out": "bf16",
                    "us_per_call_median": round(statistics.median(per_call_ms) * 1e3, 2),
                    "pct_of_fp8_peak": round(100 * tflops / world / peak, 2),
@@ -944,7 +947,10 @@ def run_mx(args):
                    "l2": f"inputs rotated over {reps} replicas ({reps * nbytes / 2**20:.0f} MiB > 129 MiB L2)",
                    "launches_per_call": 3 if A else 1},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": "grouped_gemm_mx_kernel",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(wl.name + "_mx_" + args.mx_qtype, tiles=mx_tiles,
+                                                 kernel="grouped_gemm_mx_kernel"),
+                     "kernel": "grouped_gemm_mx_kernel",
                      "peak_source": f"2 x {pk_kind} bf16 dense burst (nominal FP8:bf16 ratio 4.5:2.25)",
                      "algorithmic_bytes": nbytes},
         "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),

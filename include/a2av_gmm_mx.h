@@ -60,6 +60,8 @@ typedef struct {
     int64_t BS, H2, N2;
     int32_t qtype;            /* code format of every operand: 0 E4M3FN, 1 E5M2 */
     int32_t want_permute_out; /* 1: write permuteOut_q / permuteOut_s */
+    int32_t tiles;            /* a2av_tiles: DEFAULT (= PAIR), SINGLE (128 x 128 tiles on one CTA),
+                                 PAIR (256 x 256 tiles on a cluster of two CTAs, cta_group::2) */
 } a2av_gmm_mx_desc;
 
 a2av_status a2av_gmm_mx_workspace_size(const a2av_gmm_mx_desc *desc, size_t *bytes);

@@ -159,10 +159,11 @@ def test_quant_reduce_argument_checks(lib, kw, status):
 
 
 def mx_ws(**kw):
-    base = dict(W=8, e=4, A=16000, H1=4096, N1=1024, BS=2048, H2=4096, N2=1024, qtype=0, want_permute_out=0)
+    base = dict(W=8, e=4, A=16000, H1=4096, N1=1024, BS=2048, H2=4096, N2=1024, qtype=0, want_permute_out=0,
+                tiles=0)
     base.update(kw)
     d = binding.MxDesc(*(base[k] for k in ("W", "e", "A", "H1", "N1", "BS", "H2", "N2", "qtype",
-                                            "want_permute_out")))
+                                            "want_permute_out", "tiles")))
     n = ctypes.c_size_t(0)
     return binding.load().a2av_gmm_mx_workspace_size(ctypes.byref(d), ctypes.byref(n)), n.value
 
@@ -180,6 +181,8 @@ def mx_ws(**kw):
     ({"H2": 1024 + 256}, 3),
     ({"N1": 1020}, 3),
     ({"BS": 0, "H2": 0, "N2": 0}, 0),
+    ({"tiles": 1}, 0), ({"tiles": 2}, 0),
+    ({"tiles": 3}, 2), ({"tiles": -1}, 2),  # default, single or pair
 ])
 def test_mx_phase1_validation(lib, kw, status):
     assert mx_ws(**kw)[0] == status

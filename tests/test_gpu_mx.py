@@ -29,10 +29,13 @@ def _lib():
     build.build()
 
 
-def run_mx(inp: MxInputs, want_perm=False):
+TILES = ["single", "pair"]
+
+
+def run_mx(inp: MxInputs, want_perm=False, tiles="default"):
     dev = torch.device("cuda:0")
     wl = inp.wl
-    plan = binding.MxPlan(wl.W, wl.e, inp.A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, inp.qtype, want_perm, dev)
+    plan = binding.MxPlan(wl.W, wl.e, inp.A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, inp.qtype, want_perm, dev, tiles)
     d = lambda t: None if t is None else t.to(dev)
     out = plan.run(d(inp.ataOut_q), d(inp.ataOut_s), torch.from_numpy(inp.recvCounts).to(dev),
                    d(inp.gmmWeight_q), d(inp.gmmWeight_s), d(inp.mmX_q), d(inp.mmX_s), d(inp.mmWeight_q),
@@ -63,7 +66,7 @@ def _custom(W, e, H1, N1, rc, qtype="e4m3fn", BS=0, H2=0, N2=0, seed=0):
     return make_mx_inputs(wl, seed=seed, qtype=qtype, recvCounts=np.asarray(rc, np.int32))
 
 
-def _ones_case(sa, sw, A=128, H1=512, N1=128):
+def _ones_case(sa, sw, A=256, H1=512, N1=256):
     """Every code E4M3 1.0 with the given scale codes: out[m][n] = 32 sum_b 2^(sa[m,b]+sw[n,b]-254)."""
     wl = Workload("mx_ones", W=1, e=1, H1=H1, N1=N1, dtype="bf16", routing="uniform")
     return MxInputs(wl, "e4m3fn", np.array([A], np.int32), torch.full((A, H1), 0x38, dtype=torch.uint8),
@@ -71,7 +74,7 @@ def _ones_case(sa, sw, A=128, H1=512, N1=128):
 
 
 def _layout_cases():
-    A, N1, kb = 128, 128, 16
+    A, N1, kb = 256, 256, 16
     one_a = torch.full((A, kb), 127, dtype=torch.uint8)
     one_w = torch.full((1, N1, kb), 127, dtype=torch.uint8)
     rows = (127 + torch.arange(A) % 5)[:, None].repeat(1, kb).to(torch.uint8)
@@ -83,29 +86,31 @@ def _layout_cases():
             "per_block_a": (blocks_a, one_w), "per_block_b": (one_a, blocks_w), "row_and_block": (mixed, blocks_w)}
 
 
+@pytest.mark.parametrize("tiles", TILES)
 @pytest.mark.parametrize("case", list(_layout_cases()))
-def test_scale_placement_exact(orc, case):
+def test_scale_placement_exact(orc, case, tiles):
     # Which E8M0 byte scales which row, column and K-block: every output is
     # an exact small power-of-two sum, so the bf16 result must be bit-exact.
     sa, sw = _layout_cases()[case]
     inp = _ones_case(sa, sw, H1=512)
-    (y, _, _, _), st = run_mx(inp)
+    (y, _, _, _), st = run_mx(inp, tiles=tiles)
     assert st[0] == 0, st
     _, _, ref, _ = reference(orc, inp)
     want = torch.from_numpy(ref).to(torch.bfloat16)
     assert torch.equal(y.view(torch.int16), want.view(torch.int16)), (y[:2, :4], want[:2, :4])
 
 
+@pytest.mark.parametrize("tiles", TILES)
 @pytest.mark.parametrize("qtype", ["e4m3fn", "e5m2"])
 @pytest.mark.parametrize("W,e,H1,N1,A,zero,BS,H2,N2", [
     (2, 2, 512, 128, 300, 0.0, 0, 0, 0),
     (4, 3, 1024, 200, 700, 0.3, 100, 512, 136),
     (8, 4, 2048, 256, 1500, 0.1, 257, 1024, 384),
 ])
-def test_matches_oracle(orc, qtype, W, e, H1, N1, A, zero, BS, H2, N2):
+def test_matches_oracle(orc, qtype, W, e, H1, N1, A, zero, BS, H2, N2, tiles):
     rc = random_counts(W, e, A, seed=A + W, zero_prob=zero)
     inp = _custom(W, e, H1, N1, rc, qtype, BS, H2, N2, seed=W)
-    (y, m, _, _), st = run_mx(inp)
+    (y, m, _, _), st = run_mx(inp, tiles=tiles)
     assert st[0] == 0, st
     _, _, ref_y, ref_m = reference(orc, inp)
     assert_close(y, ref_y, "gmmY")
@@ -122,6 +127,10 @@ def test_permute_out_bit_exact_and_same_products(orc):
     assert torch.equal(pq, ref_q) and torch.equal(ps, ref_s)
     (y2, _, _, _), st = run_mx(inp, want_perm=False)
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    # The other tile shape gives the same products (fp32 sums of the same
+    # K blocks in the same order).
+    (y3, _, _, _), st = run_mx(inp, tiles="single")
+    assert st[0] == 0 and torch.allclose(y3.float(), y.float(), rtol=1e-2, atol=1e-2)
 
 
 def test_integer_products_bit_exact(orc):
@@ -135,10 +144,11 @@ def test_integer_products_bit_exact(orc):
     inp = MxInputs(wl, "e4m3fn", rc, torch.from_numpy(vals[rng.integers(0, 7, (A, 512))]),
                    torch.full((A, 16), 127, dtype=torch.uint8),
                    torch.from_numpy(vals[rng.integers(0, 7, (2, 64, 512))]), torch.full((2, 64, 16), 127, dtype=torch.uint8))
-    (y, _, _, _), st = run_mx(inp)
-    assert st[0] == 0, st
-    _, _, ref, _ = reference(orc, inp)
-    assert torch.equal(y.view(torch.int16), torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16))
+    for tiles in TILES:
+        (y, _, _, _), st = run_mx(inp, tiles=tiles)
+        assert st[0] == 0, st
+        _, _, ref, _ = reference(orc, inp)
+        assert torch.equal(y.view(torch.int16), torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16)), tiles
 
 
 def test_bad_counts_are_reported(orc):

@@ -55,7 +55,7 @@ class MxDesc(ctypes.Structure):
     _fields_ = [("W", ctypes.c_int32), ("e", ctypes.c_int32),
                 ("A", ctypes.c_int64), ("H1", ctypes.c_int64), ("N1", ctypes.c_int64),
                 ("BS", ctypes.c_int64), ("H2", ctypes.c_int64), ("N2", ctypes.c_int64),
-                ("qtype", ctypes.c_int32), ("want_permute_out", ctypes.c_int32)]
+                ("qtype", ctypes.c_int32), ("want_permute_out", ctypes.c_int32), ("tiles", ctypes.c_int32)]
 
 
 _lib = None
@@ -272,8 +272,9 @@ class MxPlan:
     (include/a2av_gmm_mx.h): codes as uint8 tensors, E8M0 scales as uint8
     tensors with one byte per 32 codes along K, weights [e, N1, H1]."""
 
-    def __init__(self, W, e, A, H1, N1, BS=0, H2=0, N2=0, qtype="e4m3fn", want_permute_out=False, device=None):
-        self.desc = MxDesc(W, e, A, H1, N1, BS, H2, N2, QTYPES[qtype], int(bool(want_permute_out)))
+    def __init__(self, W, e, A, H1, N1, BS=0, H2=0, N2=0, qtype="e4m3fn", want_permute_out=False, device=None,
+                 tiles="default"):
+        self.desc = MxDesc(W, e, A, H1, N1, BS, H2, N2, QTYPES[qtype], int(bool(want_permute_out)), TILES[tiles])
         self.device = torch.device(device) if device is not None else torch.device("cuda")
         n = ctypes.c_size_t(0)
         st = load().a2av_gmm_mx_workspace_size(ctypes.byref(self.desc), ctypes.byref(n))

@@ -15,14 +15,18 @@
 //              (staged by the permute kernel) and 128 K-major weight columns,
 //              one 4-D load of both sub-tiles per operand.
 //   warp 1     one thread issues the MMAs.
-//   warps 2-5  scales: lane l loads the E8M0 scales of tile rows and tile
-//              columns l, 32 + l, 64 + l, 96 + l, 16 bytes (two stages) at a
-//              time, and writes each stage's two 32-bit words per row (byte i
-//              of word j for MMA 4j + i) into TMEM with tcgen05.st: per word,
-//              32 lanes x 4 columns, the layout the MMA reads, in the warp's
-//              own lane quarter (each quarter holds a copy).
-//   warps 6-9  epilogue: TMEM -> registers -> bf16 (nearest even) -> global,
-//              rows past the group's end and columns past N masked.
+//   warps 2-5  scales: lane l loads the E8M0 scales of the tile rows and
+//              columns 32c + l, 8 bytes per row per stage (one stage ahead),
+//              and writes each stage's two 32-bit words per row (byte i of
+//              word j for MMA 4j + i) into TMEM with tcgen05.st: per word, 32
+//              lanes x (rows / 32) columns, the layout the MMA reads, in the
+//              warp's own lane quarter (each quarter holds a copy).
+//   warps 6-13 epilogue, two warps per TMEM lane quarter, each draining half
+//              of the columns: TMEM -> registers -> bf16 (nearest even) ->
+//              global, rows past the group's end and columns past N masked.
+//              The load of the next 32 columns overlaps the stores of the
+//              previous ones, and the accumulator is released as soon as the
+//              last load has landed.
 // TMEM: two 128-column fp32 accumulators (the epilogue of one tile overlaps
 // the main loop of the next), then per stage eight A-scale and eight B-scale
 // columns.  Every wait is bounded: on timeout the CTA sets kStatusTimeout and
@@ -43,41 +47,62 @@ namespace a2av {
 
 namespace {
 
-constexpr int MX_BM = 128;  // rows per tile
-constexpr int MX_BN = 128;  // columns per tile
-constexpr int MX_KCHUNK = 128;  // codes (bytes) in one 128-byte swizzle row
+constexpr int MX_BM = 128;       // A rows per CTA
+constexpr int MX_BNC = 128;      // weight columns per CTA
+constexpr int MX_KCHUNK = 128;   // codes (bytes) in one 128-byte swizzle row
 constexpr int MX_CH = 2;         // K chunks per stage
 constexpr int MX_BK = MX_KCHUNK * MX_CH;
 constexpr int MX_STAGES = 3;
-constexpr int MX_THREADS = 10 * 32;
+constexpr int kMxEpiWarps = 8;  // two per TMEM lane quarter, each draining half of the columns
+constexpr int kMxScaleLoadWarp = 6 + kMxEpiWarps;  // issues the scale TMA loads
+constexpr int MX_THREADS = (7 + kMxEpiWarps) * 32;
+constexpr int MX_SC_SLOTS = 4;  // scale ring: each slot holds two stages' scales (16 bytes per row)
 constexpr int kMxMmaWarp = 1;
 constexpr int kMxScaleWarp0 = 2;
 constexpr int kMxEpiWarp0 = 6;
-constexpr uint32_t MX_SUB_BYTES = MX_BM * MX_KCHUNK;   // 16 KB: 128 rows x one chunk
+constexpr uint32_t MX_SUB_BYTES = MX_BM * MX_KCHUNK;      // 16 KB: 128 rows x one chunk
 constexpr uint32_t MX_TILE_BYTES = MX_SUB_BYTES * MX_CH;  // one operand's stage; B is the same size
 constexpr uint32_t kMxTmemCols = 512;
-constexpr uint32_t kMxAccCols = 128;
-constexpr uint32_t kMxSfCol0 = 2 * kMxAccCols;
+constexpr uint32_t kMxSfCol0 = 256;  // after the accumulators (2 x 128 single, 1 x 256 pair)
 constexpr uint64_t kMxWaitLimitNs = 2000000000ull;
 
-// Per stage: A scales in 4 columns per word (2 words), then B scales likewise.
-__host__ __device__ constexpr uint32_t sfa_col(int s) { return kMxSfCol0 + 16u * s; }
-__host__ __device__ constexpr uint32_t sfb_col(int s) { return kMxSfCol0 + 16u * s + 8u; }
-static_assert(sfb_col(MX_STAGES - 1) + 8 <= kMxTmemCols, "scale columns must fit the TMEM allocation");
+// Tile shapes.  Single: one CTA, 128 x 128 tiles, two accumulators.  Pair:
+// a cluster of two CTAs, 256 x 256 tiles (cta_group::2); each CTA stages its
+// own 128 A rows and 128 of the weight columns and holds its 128 rows of the
+// accumulator, one buffer of 256 columns (two would fill TMEM).
+template <bool PAIR>
+struct MxShape {
+    static constexpr int kCtas = PAIR ? 2 : 1;
+    static constexpr int TILE_M = MX_BM * kCtas;
+    static constexpr int TILE_N = MX_BNC * kCtas;
+    static constexpr int kAccBufs = PAIR ? 1 : 2;
+    static constexpr uint32_t kAccCols = TILE_N;
+    // Scale words per stage: 2 (eight MMAs, four per word); each word is 32
+    // lanes x (rows / 32) columns.  A: this CTA's 128 rows; B: all TILE_N columns.
+    static constexpr uint32_t kSfaCols = 2 * 4;
+    static constexpr uint32_t kSfbCols = 2 * (TILE_N / 32);
+    static constexpr uint32_t kSfStride = kSfaCols + kSfbCols;
+};
+
+template <bool PAIR>
+__host__ __device__ constexpr uint32_t sfa_col(int s) { return kMxSfCol0 + MxShape<PAIR>::kSfStride * s; }
+template <bool PAIR>
+__host__ __device__ constexpr uint32_t sfb_col(int s) { return sfa_col<PAIR>(s) + MxShape<PAIR>::kSfaCols; }
+static_assert(MxShape<false>::kAccBufs * MxShape<false>::kAccCols <= kMxSfCol0, "accumulators below the scales");
+static_assert(MxShape<true>::kAccBufs * MxShape<true>::kAccCols <= kMxSfCol0, "accumulators below the scales");
+static_assert(sfb_col<true>(MX_STAGES - 1) + MxShape<true>::kSfbCols <= kMxTmemCols, "scales fit TMEM");
+static_assert(sfb_col<false>(MX_STAGES - 1) + MxShape<false>::kSfbCols <= kMxTmemCols, "scales fit TMEM");
 
 struct MxLaunch {
     const int32_t *recvCounts;
     int32_t W, e, A;
     int32_t H1, N1, BS, H2, N2;
-    const uint8_t *a_s;   // [A, H1/32] expert-major scales (staged, or permuteOut_s)
-    const uint8_t *w_s;   // [e, N1, H1/32]
-    const uint8_t *x_s;   // [BS, H2/32]
-    const uint8_t *mw_s;  // [N2, H2/32]
     void *gmmY;
     void *mmY;
     int32_t *status;
     int32_t write_status;
     int32_t qtype;  // 0 E4M3FN, 1 E5M2 (both operands)
+    int32_t pair;
     int32_t grid;
     // Code maps, all 4-D {128 codes, rows, K / 128 chunks, groups}, box
     // 128 x 128 x 2 x 1: one load is a stage's two 16 KB sub-tiles.
@@ -85,7 +110,30 @@ struct MxLaunch {
     CUtensorMap tmB;   // weight codes [e, N1, H1]
     CUtensorMap tmX;   // mmX codes [BS, H2]
     CUtensorMap tmMW;  // mmWeight codes [N2, H2]
+    // E8M0 scale maps, 3-D {K/32 bytes, rows, groups}, box 16 bytes (two
+    // stages) x 128 rows (A) or x TILE_N rows (B) x 1, no swizzle.
+    CUtensorMap tmSA;   // expert-major scales [A, H1/32]
+    CUtensorMap tmSB;   // weight scales [e, N1, H1/32]
+    CUtensorMap tmSX;   // mmX scales [BS, H2/32]
+    CUtensorMap tmSMW;  // mmWeight scales [N2, H2/32]
+    // Halves of a tile (this CTA's 128 rows) whose rows of the group lie in
+    // one (source, expert) segment are read in place from ataOut; the permute
+    // kernel staged only the others (see half_in_one_segment).
+    int32_t direct_halves;
+    CUtensorMap tmA_direct;   // ataOut codes [A, H1]
+    CUtensorMap tmSA_direct;  // ataOut scales [A, H1/32]
 };
+
+// Where this CTA's 128 A rows of a routed tile come from: in place from
+// ataOut (a run of one segment), or from the expert-major staging copy.
+__device__ __forceinline__ bool mx_direct_row(const MxLaunch &p, const SegmentTable &seg, int row0, int rows, int y,
+                                              int32_t *src) {
+    if (!p.direct_halves) return false;
+    const int g_end = row0 + rows;
+    if (y >= g_end || !half_in_one_segment(seg, p.W, p.e, y, g_end)) return false;
+    *src = source_row(seg, p.W, p.e, y);
+    return true;
+}
 
 struct MxGroup {
     int32_t row0;  // first A row (routed: expert-major row)
@@ -95,11 +143,13 @@ struct MxGroup {
 };
 
 struct MxControl {
-    uint64_t full[MX_STAGES];     // a stage's codes landed
+    uint64_t full[MX_STAGES];     // a stage's codes landed (pair: both CTAs'; in the even CTA)
     uint64_t empty[MX_STAGES];    // the MMAs reading a stage (codes and scale columns) completed
-    uint64_t sf_full[MX_STAGES];  // the stage's scale words are in TMEM (one arrival per scale warp)
+    uint64_t sf_full[MX_STAGES];  // the stage's scale words are in TMEM (scale warps; pair: of both CTAs)
+    uint64_t sc_full[MX_SC_SLOTS];   // a slot's scale rows (two stages) landed in this CTA
+    uint64_t sc_empty[MX_SC_SLOTS];  // the scale warps have read both stages of a slot
     uint64_t tfull[2];
-    uint64_t tempty[2];
+    uint64_t tempty[2];           // epilogue drained the accumulator (pair: both CTAs; in the even CTA)
     uint32_t tmem_base;
     int32_t abort;
     int32_t total_tiles;
@@ -107,7 +157,17 @@ struct MxControl {
     SegmentTable seg;
 };
 
-constexpr size_t mx_smem_bytes() { return 1024 + MX_STAGES * 2 * MX_TILE_BYTES + sizeof(MxControl); }
+// A scale slot: 16 bytes (the two stages sharing a 16-byte chunk of each
+// scale row) for each of the CTA's 128 A rows and each of TILE_N columns.
+constexpr uint32_t MX_SA_BYTES = MX_BM * 16;
+template <bool PAIR>
+__host__ __device__ constexpr uint32_t mx_sb_bytes() { return MxShape<PAIR>::TILE_N * 16; }
+template <bool PAIR>
+constexpr size_t mx_smem_bytes() {
+    return 1024 + MX_STAGES * 2 * MX_TILE_BYTES + MX_SC_SLOTS * (MX_SA_BYTES + mx_sb_bytes<PAIR>()) +
+           sizeof(MxControl);
+}
+static_assert(mx_smem_bytes<true>() <= 232448, "shared memory per CTA");
 
 struct MxTile {
     int g, m, n;
@@ -121,14 +181,31 @@ __device__ __forceinline__ MxTile mx_decode_tile(const MxControl &c, int t) {
 }
 
 // Bounded wait on an mbarrier phase; false when it gave up (or another role
-// did), with the abort flag and the status word set.
+// did), with the abort flag and the status word set.  CLUSTER: acquire at
+// cluster scope (arrivals come from the peer CTA too).
+template <bool CLUSTER = false>
 __device__ __noinline__ bool mx_wait(int32_t *abort_flag, uint64_t *bar, uint32_t parity, int32_t *status) {
     const uint32_t b = smem_u32(bar);
-    if (mbar_try_wait(b, parity)) return true;
+    auto try_once = [&]() -> bool {
+        if constexpr (CLUSTER) {
+            uint32_t ok;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(ok)
+                : "r"(b), "r"(parity)
+                : "memory");
+            return ok != 0;
+        } else {
+            return mbar_try_wait(b, parity);
+        }
+    };
+    if (try_once()) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(b, parity)) return true;
+            if (try_once()) return true;
         if (*reinterpret_cast<volatile int32_t *>(abort_flag)) return false;
         if (global_timer_ns() - t0 > kMxWaitLimitNs) {
             *reinterpret_cast<volatile int32_t *>(abort_flag) = 1;
@@ -147,66 +224,167 @@ __host__ __device__ constexpr uint32_t mx_idesc(uint32_t qtype, uint32_t M, uint
 
 __device__ __forceinline__ uint32_t mx_sf_ids(uint32_t i) { return (i << 29) | (i << 4); }
 
+template <bool PAIR>
 __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
+    if constexpr (PAIR) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    }
 }
 
-// Thread i of the warp writes eight 32-bit words to lane (quarter base + i),
-// columns [col, col + 8).
-__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+// One arrival on `bar` (pair: on the barrier at that offset in both CTAs)
+// when this thread's earlier tcgen05 operations have completed.
+template <bool PAIR>
+__device__ __forceinline__ void mx_commit(uint32_t bar) {
+    if constexpr (PAIR) {
+        const uint16_t both = 3;
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+            " [%0], %1;" ::"r"(bar),
+            "h"(both)
+            : "memory");
+    } else {
+        mma_commit(bar);
+    }
+}
+
+__device__ __forceinline__ uint32_t mx_cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mx_map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void mx_cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// An arrival on a barrier of the even CTA (own CTA when single).
+template <bool PAIR>
+__device__ __forceinline__ void mx_arrive_leader(uint32_t own_addr) {
+    if constexpr (PAIR)
+        asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                         mx_map_to_rank(own_addr, 0))
+                     : "memory");
+    else
+        mbar_arrive(own_addr);
+}
+
+// Thread i of the warp writes N consecutive 32-bit words to lane (quarter
+// base + i), columns [col, col + N).
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t *v) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
                  "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                  : "memory");
 }
 
-__device__ __forceinline__ void tma_load_4d_mx(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y,
-                                               int32_t z, int32_t w) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
-        : "memory");
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void ld_shared_v2(uint32_t addr, uint32_t &a, uint32_t &b) {
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr) : "memory");
 }
 
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// TMA 4-D load; PAIR: the barrier is the even CTA's (cta_group::2).
+template <bool PAIR>
+__device__ __forceinline__ void tma_load_4d_mx(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y,
+                                               int32_t z, int32_t w) {
+    if constexpr (PAIR) {
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+            " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+            : "memory");
+    } else {
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+            : "memory");
+    }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void mx_tmem_alloc(uint32_t dst_smem) {
+    if constexpr (PAIR) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                     "r"(kMxTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+        tmem_alloc(dst_smem, kMxTmemCols);
+        tmem_relinquish();
+    }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void mx_tmem_free(uint32_t taddr) {
+    if constexpr (PAIR)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kMxTmemCols)
+                     : "memory");
+    else
+        tmem_dealloc(taddr, kMxTmemCols);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(uint32_t lo, uint32_t hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
-    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
+template <bool PAIR>
 __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __grid_constant__ MxLaunch p) {
+    using S = MxShape<PAIR>;
+    constexpr int TILE_M = S::TILE_M;
+    constexpr int TILE_N = S::TILE_N;
+    constexpr int kCtas = S::kCtas;
+    constexpr int NB = TILE_N / 32;  // B scale columns per word
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *base_ptr = smem_raw + (base - raw);
     const uint32_t a_smem = base;
     const uint32_t b_smem = base + MX_STAGES * MX_TILE_BYTES;
-    MxControl &C = *reinterpret_cast<MxControl *>(base_ptr + 2 * MX_STAGES * MX_TILE_BYTES);
+    constexpr uint32_t SB_BYTES = mx_sb_bytes<PAIR>();
+    const uint32_t sa_smem = base + 2 * MX_STAGES * MX_TILE_BYTES;
+    const uint32_t sb_smem = sa_smem + MX_SC_SLOTS * MX_SA_BYTES;
+    MxControl &C = *reinterpret_cast<MxControl *>(base_ptr + 2 * MX_STAGES * MX_TILE_BYTES +
+                                                  MX_SC_SLOTS * (MX_SA_BYTES + SB_BYTES));
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int e = p.e;
+    const uint32_t rank = PAIR ? mx_cluster_rank() : 0;  // 0: this CTA issues the MMAs
+    const int unit = blockIdx.x / kCtas;
+    const int nunits = gridDim.x / kCtas;
 
     // ---- prologue: plan (warp 0), barriers + TMEM (MMA warp), map prefetch (warp 2)
     if (warp == 0) {
         const bool good = build_segment_table(p.recvCounts, p.W, e, p.A, C.seg, lane);
-        const int tn1 = (p.N1 + MX_BN - 1) / MX_BN;
+        const int tn1 = (p.N1 + TILE_N - 1) / TILE_N;
         int row0 = 0, rows = 0, tiles = 0;
         if (lane < e) {
             row0 = C.seg.dst[lane * p.W];
             rows = C.seg.dst[(lane + 1) * p.W] - row0;
-            tiles = good ? ((rows + MX_BM - 1) / MX_BM) * tn1 : 0;
+            tiles = good ? ((rows + TILE_M - 1) / TILE_M) * tn1 : 0;
         }
         int inc = tiles;
 #pragma unroll
@@ -219,9 +397,9 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
         if (lane == 0) {
             int ng = e, total = routed_total;
             if (p.BS > 0) {
-                const int tn2 = (p.N2 + MX_BN - 1) / MX_BN;
+                const int tn2 = (p.N2 + TILE_N - 1) / TILE_N;
                 C.g[e] = MxGroup{0, p.BS, tn2, total};
-                total += good ? ((p.BS + MX_BM - 1) / MX_BM) * tn2 : 0;
+                total += good ? ((p.BS + TILE_M - 1) / TILE_M) * tn2 : 0;
                 ng = e + 1;
             }
             C.g[ng] = MxGroup{0, 0, 1, total};
@@ -237,49 +415,65 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
             for (int s = 0; s < MX_STAGES; ++s) {
                 mbar_init(smem_u32(&C.full[s]), 1);
                 mbar_init(smem_u32(&C.empty[s]), 1);
-                mbar_init(smem_u32(&C.sf_full[s]), 4);
+                mbar_init(smem_u32(&C.sf_full[s]), 4 * kCtas);
+            }
+            for (int c = 0; c < MX_SC_SLOTS; ++c) {
+                mbar_init(smem_u32(&C.sc_full[c]), 1);
+                mbar_init(smem_u32(&C.sc_empty[c]), 4);
             }
             for (int a = 0; a < 2; ++a) {
                 mbar_init(smem_u32(&C.tfull[a]), 1);
-                mbar_init(smem_u32(&C.tempty[a]), 4);
+                mbar_init(smem_u32(&C.tempty[a]), kMxEpiWarps * kCtas);
             }
             fence_barrier_init();
         }
         __syncwarp();
-        tmem_alloc(smem_u32(&C.tmem_base), kMxTmemCols);
-        tmem_relinquish();
+        mx_tmem_alloc<PAIR>(smem_u32(&C.tmem_base));
     } else if (warp == 2) {
         if (lane == 0) {
             if (p.A > 0) {
                 prefetch_tensormap(&p.tmA);
                 prefetch_tensormap(&p.tmB);
+                prefetch_tensormap(&p.tmSA);
+                prefetch_tensormap(&p.tmSB);
+                if (p.direct_halves) {
+                    prefetch_tensormap(&p.tmA_direct);
+                    prefetch_tensormap(&p.tmSA_direct);
+                }
             }
             if (p.BS > 0) {
                 prefetch_tensormap(&p.tmX);
                 prefetch_tensormap(&p.tmMW);
+                prefetch_tensormap(&p.tmSX);
+                prefetch_tensormap(&p.tmSMW);
             }
         }
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (PAIR) mx_cluster_sync();
+    else __syncthreads();
     tc_fence_after_sync();
 
     const int total = C.total_tiles;
-    const int stride = gridDim.x;
 
     if (warp == 0) {
         // =========================================================== TMA producer
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += stride) {
+            for (int t = unit; t < total && ok; t += nunits) {
                 const MxTile w = mx_decode_tile(C, t);
                 const bool shared = w.g >= e;
                 const int K = shared ? p.H2 : p.H1;
                 const CUtensorMap *ta = shared ? &p.tmX : &p.tmA;
                 const CUtensorMap *tb = shared ? &p.tmMW : &p.tmB;
-                const int ya = C.g[w.g].row0 + w.m * MX_BM;
-                const int xn = w.n * MX_BN;
+                int ya = C.g[w.g].row0 + w.m * TILE_M + static_cast<int>(rank) * MX_BM;
+                int32_t src = 0;
+                if (!shared && mx_direct_row(p, C.seg, C.g[w.g].row0, C.g[w.g].rows, ya, &src)) {
+                    ta = &p.tmA_direct;
+                    ya = src;
+                }
+                const int xn = w.n * TILE_N + static_cast<int>(rank) * MX_BNC;
                 const int z = shared ? 0 : w.g;
                 for (int kb = 0; kb < K / MX_BK; ++kb, ++it) {
                     const int s = it % MX_STAGES;
@@ -287,11 +481,12 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_u32(&C.full[s]);
-                    mbar_arrive_expect_tx(fb, 2 * MX_TILE_BYTES);
+                    const uint32_t fb_own = smem_u32(&C.full[s]);
+                    const uint32_t fb = PAIR ? mx_map_to_rank(fb_own, 0) : fb_own;  // the MMA CTA's barrier
+                    if (rank == 0) mbar_arrive_expect_tx(fb_own, kCtas * 2 * MX_TILE_BYTES);
                     // {chunk column, row, chunk, group}: both chunks of the stage.
-                    tma_load_4d_mx(a_smem + s * MX_TILE_BYTES, ta, fb, 0, ya, kb * MX_CH, 0);
-                    tma_load_4d_mx(b_smem + s * MX_TILE_BYTES, tb, fb, 0, xn, kb * MX_CH, z);
+                    tma_load_4d_mx<PAIR>(a_smem + s * MX_TILE_BYTES, ta, fb, 0, ya, kb * MX_CH, 0);
+                    tma_load_4d_mx<PAIR>(b_smem + s * MX_TILE_BYTES, tb, fb, 0, xn, kb * MX_CH, z);
                 }
             }
             // Wait until the MMAs released every stage that was filled.
@@ -300,99 +495,67 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
         }
     } else if (warp == kMxMmaWarp) {
         // =========================================================== MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc0 = mx_idesc(static_cast<uint32_t>(p.qtype), MX_BM, MX_BN);
+        if (lane == 0 && rank == 0) {
+            const uint32_t idesc0 = mx_idesc(static_cast<uint32_t>(p.qtype), TILE_M, TILE_N);
             // Both operands K-major with a 128-byte swizzle: 128-byte rows,
             // 8-row groups 1024 B apart; an MMA's K step of 32 codes is 32
             // bytes along the row (2 in the 16-byte address field), and the
-            // second chunk of a stage starts 16 KB further on.
+            // second chunk of a stage starts 16 KB further on.  Pair: both
+            // CTAs hold their halves of A and B at the same offsets.
             const uint64_t a_desc0 = smem_desc(a_smem, 16, 1024, kSwizzle128B);
             const uint64_t b_desc0 = smem_desc(b_smem, 16, 1024, kSwizzle128B);
             uint32_t it = 0, tl = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += stride, ++tl) {
+            for (int t = unit; t < total && ok; t += nunits, ++tl) {
                 const MxTile w = mx_decode_tile(C, t);
                 const int K = w.g >= e ? p.H2 : p.H1;
-                const int acc = tl & 1;
-                if (!mx_wait(&C.abort, &C.tempty[acc], ((tl >> 1) & 1) ^ 1, p.status)) break;
+                const int acc = S::kAccBufs == 2 ? (tl & 1) : 0;
+                const uint32_t use = S::kAccBufs == 2 ? (tl >> 1) : tl;  // uses of this buffer so far
+                if (!mx_wait<PAIR>(&C.abort, &C.tempty[acc], (use & 1) ^ 1, p.status)) break;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = C.tmem_base + acc * kMxAccCols;
+                const uint32_t d_tmem = C.tmem_base + acc * S::kAccCols;
                 for (int kb = 0; kb < K / MX_BK; ++kb, ++it) {
                     const int s = it % MX_STAGES;
                     const uint32_t par = (it / MX_STAGES) & 1;
                     if (!mx_wait(&C.abort, &C.full[s], par, p.status) ||
-                        !mx_wait(&C.abort, &C.sf_full[s], par, p.status)) {
+                        !mx_wait<PAIR>(&C.abort, &C.sf_full[s], par, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();  // the scale words came by tcgen05.st from other threads
                     const uint64_t ad = a_desc0 + ((s * MX_TILE_BYTES) >> 4);
                     const uint64_t bd = b_desc0 + ((s * MX_TILE_BYTES) >> 4);
-                    const uint32_t sfa = C.tmem_base + sfa_col(s);
-                    const uint32_t sfb = C.tmem_base + sfb_col(s);
+                    const uint32_t sfa = C.tmem_base + sfa_col<PAIR>(s);
+                    const uint32_t sfb = C.tmem_base + sfb_col<PAIR>(s);
 #pragma unroll
                     for (int kk = 0; kk < MX_BK / 32; ++kk) {
                         const uint32_t off = ((kk >> 2) * MX_SUB_BYTES + (kk & 3) * 32) >> 4;
-                        const uint32_t word = (kk >> 2) * 4;  // scale column group of this MMA
-                        mma_mx(d_tmem, ad + off, bd + off, idesc0 | mx_sf_ids(kk & 3), sfa + word, sfb + word,
-                               (kb | kk) != 0);
+                        const uint32_t j = kk >> 2;  // scale word of this MMA
+                        mma_mx<PAIR>(d_tmem, ad + off, bd + off, idesc0 | mx_sf_ids(kk & 3), sfa + 4 * j,
+                                     sfb + NB * j, (kb | kk) != 0);
                     }
-                    mma_commit(smem_u32(&C.empty[s]));
+                    mx_commit<PAIR>(smem_u32(&C.empty[s]));
                 }
-                if (ok) mma_commit(smem_u32(&C.tfull[acc]));
+                if (ok) mx_commit<PAIR>(smem_u32(&C.tfull[acc]));
             }
         }
     } else if (warp >= kMxScaleWarp0 && warp < kMxEpiWarp0) {
         // =========================================================== scale writers
-        // The MMA reads the 128 scale bytes of a K block as 32 lanes x 4
-        // columns: row (B: column) 32c + l at lane l, column base + c, and
-        // each 32-lane quarter of TMEM holds the same copy.  A warp reaches
-        // only its own quarter, so every scale warp writes the whole tile.
+        // The MMA reads a K block's scale bytes for 128 rows (columns) as 32
+        // lanes x 4 columns: row 32c + l at lane l, column base + c, and each
+        // 32-lane quarter of TMEM holds the same copy.  A warp reaches only
+        // its own quarter, so every scale warp writes the whole set: A for
+        // this CTA's 128 rows, B for all TILE_N columns of the tile.
         const int q = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += stride) {
+        for (int t = unit; t < total && ok; t += nunits) {
             const MxTile w = mx_decode_tile(C, t);
             const bool shared = w.g >= e;
             const int K = shared ? p.H2 : p.H1;
-            const int N = shared ? p.N2 : p.N1;
             const int kblocks = K / MX_BK;
-            const int64_t srow = K / 32;  // scale bytes per row
-            const uint8_t *sa[4];
-            const uint8_t *sb[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int r = 32 * c + lane;
-                const int64_t arow = static_cast<int64_t>(C.g[w.g].row0) + w.m * MX_BM + r;
-                const int64_t bcol = static_cast<int64_t>(w.n) * MX_BN + r;
-                sa[c] = arow < (shared ? p.BS : p.A) ? (shared ? p.x_s : p.a_s) + arow * srow : nullptr;
-                sb[c] = bcol < N ? (shared ? p.mw_s + bcol * srow : p.w_s + (static_cast<int64_t>(w.g) * N + bcol) * srow)
-                                 : nullptr;
-            }
-            // Scales of two stages (16 bytes per row) at a time, one chunk ahead.
-            const uint4 zero = make_uint4(0, 0, 0, 0);
-            uint4 ca[4], cb[4], na[4], nb[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                ca[c] = sa[c] ? __ldg(reinterpret_cast<const uint4 *>(sa[c])) : zero;
-                cb[c] = sb[c] ? __ldg(reinterpret_cast<const uint4 *>(sb[c])) : zero;
-                na[c] = nb[c] = zero;
-            }
             for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                if ((kb & 1) == 0) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (kb > 0) {
-                            ca[c] = na[c];
-                            cb[c] = nb[c];
-                        }
-                        if (kb + 2 < kblocks) {  // a stage's 8 scale bytes per row; 16 bytes cover two
-                            na[c] = sa[c] ? __ldg(reinterpret_cast<const uint4 *>(sa[c] + (kb + 2) * 8)) : zero;
-                            nb[c] = sb[c] ? __ldg(reinterpret_cast<const uint4 *>(sb[c] + (kb + 2) * 8)) : zero;
-                        }
-                    }
-                }
                 const int s = it % MX_STAGES;
                 bool free_slot = true;
                 if (lane == 0) free_slot = mx_wait(&C.abort, &C.empty[s], ((it / MX_STAGES) & 1) ^ 1, p.status);
@@ -400,73 +563,138 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     ok = false;
                     break;
                 }
-                tc_fence_after_sync();
-                // Column 4j + c: word j of this stage for row (column) 32c + lane.
-                const int j0 = (kb & 1) * 2;
-                uint32_t wa[8], wb[8];
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        wa[4 * j + c] = word_of(ca[c], j0 + j);
-                        wb[4 * j + c] = word_of(cb[c], j0 + j);
+                // Scale slot of this stage: stages 2i and 2i + 1 (tiles have an
+                // even number of stages) share slot i % MX_SC_SLOTS.
+                const uint32_t chunk = it >> 1;
+                const int slot = chunk % MX_SC_SLOTS;
+                if ((it & 1) == 0) {
+                    if (lane == 0)
+                        free_slot = mx_wait(&C.abort, &C.sc_full[slot], (chunk / MX_SC_SLOTS) & 1, p.status);
+                    if (!__shfl_sync(0xffffffffu, free_slot, 0)) {
+                        ok = false;
+                        break;
                     }
-                tmem_st_32x32b_x8(C.tmem_base + lane_base + sfa_col(s), wa);
-                tmem_st_32x32b_x8(C.tmem_base + lane_base + sfb_col(s), wb);
+                }
+                tc_fence_after_sync();
+                // Staged scale row r is 16 bytes at 16 r; this stage's two words
+                // are its half (it & 1).  Word j for row (column) 32c + lane goes
+                // to column (columns per word) * j + c.
+                uint32_t wa[8], wb[2 * NB];
+                const uint32_t half = (it & 1) * 8 + static_cast<uint32_t>(lane) * 16;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    ld_shared_v2(sa_smem + slot * MX_SA_BYTES + c * 512 + half, wa[c], wa[4 + c]);
+#pragma unroll
+                for (int c = 0; c < NB; ++c)
+                    ld_shared_v2(sb_smem + slot * SB_BYTES + c * 512 + half, wb[c], wb[NB + c]);
+                if (it & 1) {  // both stages of the slot read: free it for the loader
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&C.sc_empty[slot]));
+                }
+                tmem_st_x8(C.tmem_base + lane_base + sfa_col<PAIR>(s), wa);
+#pragma unroll
+                for (int h = 0; h < 2 * NB; h += 8) tmem_st_x8(C.tmem_base + lane_base + sfb_col<PAIR>(s) + h, wb + h);
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&C.sf_full[s]));
+                if (lane == 0) mx_arrive_leader<PAIR>(smem_u32(&C.sf_full[s]));
             }
+        }
+    } else if (warp == kMxScaleLoadWarp) {
+        // =========================================================== scale loader
+        // Walks the same stages two at a time and keeps the scale ring full,
+        // up to MX_SC_SLOTS slots ahead of the scale writers.
+        if (lane == 0) {
+            uint32_t chunk = 0;
+            bool ok = true;
+            for (int t = unit; t < total && ok; t += nunits) {
+                const MxTile w = mx_decode_tile(C, t);
+                const bool shared = w.g >= e;
+                const int K = shared ? p.H2 : p.H1;
+                const CUtensorMap *tsa = shared ? &p.tmSX : &p.tmSA;
+                const CUtensorMap *tsb = shared ? &p.tmSMW : &p.tmSB;
+                int ya = C.g[w.g].row0 + w.m * TILE_M + static_cast<int>(rank) * MX_BM;
+                int32_t src = 0;
+                if (!shared && mx_direct_row(p, C.seg, C.g[w.g].row0, C.g[w.g].rows, ya, &src)) {
+                    tsa = &p.tmSA_direct;
+                    ya = src;
+                }
+                const int z = shared ? 0 : w.g;
+                for (int kb = 0; kb < K / MX_BK; kb += 2, ++chunk) {
+                    const int slot = chunk % MX_SC_SLOTS;
+                    if (!mx_wait(&C.abort, &C.sc_empty[slot], ((chunk / MX_SC_SLOTS) & 1) ^ 1, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t lb = smem_u32(&C.sc_full[slot]);
+                    mbar_arrive_expect_tx(lb, MX_SA_BYTES + SB_BYTES);
+                    // The 16-byte chunk of each scale row holding stages kb and kb + 1.
+                    tma_load_3d(sa_smem + slot * MX_SA_BYTES, tsa, lb, (kb >> 1) * 16, ya, 0);
+                    tma_load_3d(sb_smem + slot * SB_BYTES, tsb, lb, (kb >> 1) * 16, w.n * TILE_N, z);
+                }
+            }
+            // Wait until the scale writers have read every slot that was filled.
+            for (int i = 0; i < MX_SC_SLOTS && ok; ++i, ++chunk)
+                ok = mx_wait(&C.abort, &C.sc_empty[chunk % MX_SC_SLOTS], ((chunk / MX_SC_SLOTS) & 1) ^ 1, p.status);
         }
     } else {
         // =========================================================== epilogue
         const int q = warp & 3;
+        constexpr int kChunks = TILE_N / 32 / 2;              // 32-column chunks per warp
+        const int c0 = ((warp - kMxEpiWarp0) / 4) * kChunks;  // first chunk of this warp's half
         uint32_t tl = 0;
-        for (int t = blockIdx.x; t < total; t += stride, ++tl) {
+        for (int t = unit; t < total; t += nunits, ++tl) {
             const MxTile w = mx_decode_tile(C, t);
             const bool shared = w.g >= e;
-            const int acc = tl & 1;
-            if (!mx_wait(&C.abort, &C.tfull[acc], (tl >> 1) & 1, p.status)) break;
+            const int acc = S::kAccBufs == 2 ? (tl & 1) : 0;
+            const uint32_t use = S::kAccBufs == 2 ? (tl >> 1) : tl;
+            if (!mx_wait(&C.abort, &C.tfull[acc], use & 1, p.status)) break;
             __syncwarp();  // lanes leave the wait independently; tcgen05.ld needs the whole warp
             tc_fence_after_sync();
             const int N = shared ? p.N2 : p.N1;
-            const int row = w.m * MX_BM + q * 32 + lane;
+            const int row = w.m * TILE_M + static_cast<int>(rank) * MX_BM + q * 32 + lane;
             const bool valid = row < C.g[w.g].rows;
-            const int n0 = w.n * MX_BN;
+            const int n0 = w.n * TILE_N;
             const size_t out_row = static_cast<size_t>(shared ? row : C.g[w.g].row0 + row);
             uint16_t *out = static_cast<uint16_t *>(shared ? p.mmY : p.gmmY) + out_row * N + n0;
-            const uint32_t t_base = C.tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kMxAccCols;
-            for (int c = 0; c < MX_BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(t_base + c * 32, v);
+            const uint32_t t_base = C.tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::kAccCols;
+            uint32_t v[2][32];
+            tmem_ld_32x32b_x32(t_base + c0 * 32, v[0]);
+#pragma unroll
+            for (int i = 0; i < kChunks; ++i) {
                 tmem_ld_wait();
+                if (i + 1 < kChunks) {
+                    tmem_ld_32x32b_x32(t_base + (c0 + i + 1) * 32, v[(i + 1) & 1]);
+                } else {  // every load of this tile has landed: release the accumulator
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mx_arrive_leader<PAIR>(smem_u32(&C.tempty[acc]));
+                }
                 if (valid) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const int col = c * 32 + j * 8;
+                        const int col = (c0 + i) * 32 + j * 8;
                         if (n0 + col < N) {
+                            const uint32_t *r = v[i & 1] + j * 8;
                             uint4 pk;
-                            pk.x = pack_bf16(v[j * 8 + 0], v[j * 8 + 1]);
-                            pk.y = pack_bf16(v[j * 8 + 2], v[j * 8 + 3]);
-                            pk.z = pack_bf16(v[j * 8 + 4], v[j * 8 + 5]);
-                            pk.w = pack_bf16(v[j * 8 + 6], v[j * 8 + 7]);
+                            pk.x = pack_bf16(r[0], r[1]);
+                            pk.y = pack_bf16(r[2], r[3]);
+                            pk.z = pack_bf16(r[4], r[5]);
+                            pk.w = pack_bf16(r[6], r[7]);
                             *reinterpret_cast<uint4 *>(out + col) = pk;
                         }
                     }
                 }
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&C.tempty[acc]));
         }
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (PAIR) mx_cluster_sync();
+    else __syncthreads();
     if (warp == kMxMmaWarp) {
         tc_fence_after_sync();
-        tmem_dealloc(C.tmem_base, kMxTmemCols);
+        mx_tmem_free<PAIR>(C.tmem_base);
     }
 }
 
@@ -484,6 +712,8 @@ a2av_status mx_validate(const a2av_gmm_mx_desc *d) {
     if (d->A < 0 || d->A > INT32_MAX || d->BS < 0 || d->BS > INT32_MAX) return A2AV_ERR_INVALID;
     if (d->BS > 0 && (d->H2 <= 0 || d->H2 > 12288 || d->N2 <= 0 || d->N2 >= 65536)) return A2AV_ERR_INVALID;
     if (d->qtype != 0 && d->qtype != 1) return A2AV_ERR_INVALID;  // E4M3FN or E5M2
+    if (d->tiles != A2AV_TILES_DEFAULT && d->tiles != A2AV_TILES_SINGLE && d->tiles != A2AV_TILES_PAIR)
+        return A2AV_ERR_INVALID;
     if (d->H1 % 512 != 0 || d->N1 % 8 != 0) return A2AV_ERR_UNSUPPORTED;
     if (d->BS > 0 && (d->H2 % 512 != 0 || d->N2 % 8 != 0)) return A2AV_ERR_UNSUPPORTED;
     return A2AV_OK;
@@ -521,6 +751,21 @@ bool mx_codes_map(CUtensorMap *m, const void *ptr, int64_t groups, int64_t rows,
     cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// E8M0 scales [groups][rows][K/32 bytes] as 3-D {K/32, rows, groups}; box
+// 16 bytes x box_rows x 1, no swizzle (row strides are multiples of 16 B).
+bool mx_scales_map(CUtensorMap *m, const void *ptr, int64_t groups, int64_t rows, int64_t K, uint32_t box_rows) {
+    auto fn = mx_encode_fn();
+    if (!fn) return false;
+    const int64_t kb = K / 32;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kb), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(groups)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kb), static_cast<cuuint64_t>(kb * rows)};
+    cuuint32_t box[3] = {16, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -587,17 +832,19 @@ a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, 
     g.BS = shared ? static_cast<int32_t>(d.BS) : 0;
     g.H2 = shared ? static_cast<int32_t>(d.H2) : 0;
     g.N2 = shared ? static_cast<int32_t>(d.N2) : 0;
-    g.w_s = static_cast<const uint8_t *>(gmmWeight_s);
-    g.x_s = static_cast<const uint8_t *>(mmX_s);
-    g.mw_s = static_cast<const uint8_t *>(mmWeight_s);
     g.gmmY = gmmY;
     g.mmY = mmY;
     g.status = status;
     g.qtype = d.qtype;
+    const bool pair = d.tiles != A2AV_TILES_SINGLE;
+    const uint32_t tile_n = pair ? 2 * MX_BNC : MX_BNC;
     if (!mx_codes_map(&g.tmB, gmmWeight_q, d.e, d.N1, d.H1)) return A2AV_ERR_CUDA;
+    if (!mx_scales_map(&g.tmSB, gmmWeight_s, d.e, d.N1, d.H1, tile_n)) return A2AV_ERR_CUDA;
     if (shared) {
         if (!mx_codes_map(&g.tmX, mmX_q, 1, d.BS, d.H2)) return A2AV_ERR_CUDA;
         if (!mx_codes_map(&g.tmMW, mmWeight_q, 1, d.N2, d.H2)) return A2AV_ERR_CUDA;
+        if (!mx_scales_map(&g.tmSX, mmX_s, 1, d.BS, d.H2, MX_BM)) return A2AV_ERR_CUDA;
+        if (!mx_scales_map(&g.tmSMW, mmWeight_s, 1, d.N2, d.H2, tile_n)) return A2AV_ERR_CUDA;
     }
     bool permute_ran = false;
     if (routed) {
@@ -610,26 +857,52 @@ a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, 
         }
         // The row permute moves 16-byte vectors of rows given in 2-byte
         // elements: a code row is H1 / 2 of them, a scale row H1 / 64.
+        // Without permuteOut only the 128-row halves that straddle a segment
+        // boundary are staged; the kernel reads the others from ataOut.
+        const int32_t partial = d.want_permute_out ? 0 : 1;
         PermuteLaunch pq{recvCounts, d.W, d.e, static_cast<int32_t>(d.A), static_cast<int32_t>(d.H1 / 2),
-                         ataOut_q, dq, status, 1, 0};
+                         ataOut_q, dq, status, 1, partial};
         PermuteLaunch ps{recvCounts, d.W, d.e, static_cast<int32_t>(d.A), static_cast<int32_t>(d.H1 / 64),
-                         ataOut_s, ds, status, 0, 0};
+                         ataOut_s, ds, status, 0, partial};
+        if (partial) {
+            if (!mx_codes_map(&g.tmA_direct, ataOut_q, 1, d.A, d.H1)) return A2AV_ERR_CUDA;
+            if (!mx_scales_map(&g.tmSA_direct, ataOut_s, 1, d.A, d.H1, MX_BM)) return A2AV_ERR_CUDA;
+            g.direct_halves = 1;
+        }
         if (launch_permute(pq, sms, stream) != cudaSuccess) return A2AV_ERR_CUDA;
         if (launch_permute(ps, sms, stream) != cudaSuccess) return A2AV_ERR_CUDA;
         permute_ran = true;
         if (!mx_codes_map(&g.tmA, dq, 1, d.A, d.H1)) return A2AV_ERR_CUDA;
-        g.a_s = ds;
+        if (!mx_scales_map(&g.tmSA, ds, 1, d.A, d.H1, MX_BM)) return A2AV_ERR_CUDA;
     }
     g.write_status = permute_ran ? 0 : 1;
 
-    const int64_t tiles = ((d.A + MX_BM - 1) / MX_BM + d.e) * ((d.N1 + MX_BN - 1) / MX_BN) +
-                          (shared ? ((d.BS + MX_BM - 1) / MX_BM) * ((d.N2 + MX_BN - 1) / MX_BN) : 0);
-    g.grid = static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(sms, tiles)));
-    constexpr size_t smem = mx_smem_bytes();
-    if (cudaFuncSetAttribute(grouped_gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
+    // Persistent grid: one CTA (pair: cluster of two) per SM (pair), never
+    // more than there can be tiles.
+    g.pair = pair ? 1 : 0;
+    const int64_t tm = pair ? 2 * MX_BM : MX_BM, tn = pair ? 2 * MX_BNC : MX_BNC;
+    const int64_t tiles = ((d.A + tm - 1) / tm + d.e) * ((d.N1 + tn - 1) / tn) +
+                          (shared ? ((d.BS + tm - 1) / tm) * ((d.N2 + tn - 1) / tn) : 0);
+    const int64_t units = std::max<int64_t>(1, std::min<int64_t>(pair ? sms / 2 : sms, tiles));
+    g.grid = static_cast<int32_t>(units * (pair ? 2 : 1));
+    const size_t smem = pair ? mx_smem_bytes<true>() : mx_smem_bytes<false>();
+    auto kern = pair ? grouped_gemm_mx_kernel<true> : grouped_gemm_mx_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
         return A2AV_ERR_CUDA;
-    grouped_gemm_mx_kernel<<<g.grid, MX_THREADS, smem, stream>>>(g);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g.grid, 1, 1);
+    cfg.blockDim = dim3(MX_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pair ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pair ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, g) != cudaSuccess) return A2AV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? A2AV_OK : A2AV_ERR_CUDA;
 }
 
