@@ -402,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if (warp == 0) {
             uint32_t it = 0;  // stages issued
             bool ok = true;
+            bool staged_ready = !p.after_permute;  // the permute kernel's rows are visible
             for (int t = unit; t < total && ok; t += nunits) {
                 const Tile w = decode_tile(C, t);
                 const bool shared = w.g >= e;
@@ -460,6 +461,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         if (sf == sl && sf < nseg) best = k;
                     }
                     box_level = best == 0 ? 0 : ((lane & ((1 << best) - 1)) == 0 ? best : -1);
+                }
+                if (!GATHER && !shared && !direct && !staged_ready) {
+                    // This tile reads rows the permute kernel stages: wait for
+                    // that grid (the tiles before needed none of its output).
+                    asm volatile("griddepcontrol.wait;" ::: "memory");
+                    staged_ready = true;
                 }
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % STAGES;
@@ -656,13 +663,22 @@ cudaError_t launch_variant(const GemmLaunch &p, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = Shape<PAIR, CH>::kCtas;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (PAIR) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = Shape<PAIR, CH>::kCtas;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (p.after_permute) {  // start beside the permute kernel; the producer waits where it must
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = PAIR ? 1 : 0;
+    cfg.numAttrs = n;
     err = cudaLaunchKernelEx(&cfg, kern, p);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();

@@ -19,6 +19,8 @@ struct PermuteLaunch {
     int32_t *status;      // device status word
     int32_t write_status; // 1: this kernel stores the word (first kernel of a call)
     int32_t only_straddling;  // 1: copy only 128-row halves that straddle a segment boundary
+    int32_t blocks_per_sm;    // grid cap per SM (0: 8, one full SM of threads); a GEMM that
+                              // starts while this kernel runs needs room beside it
 };
 
 cudaError_t launch_permute(const PermuteLaunch &p, int num_sms, cudaStream_t stream);
@@ -51,6 +53,8 @@ struct GemmLaunch {
     CUtensorMap tmB4_routed;  // gmmWeight as 64-column atoms: one load per stage (when b4_routed)
     CUtensorMap tmB4_shared;  // mmWeight likewise (when b4_shared)
     int32_t b4_routed, b4_shared;
+    int32_t after_permute;    // 1: launched to overlap the permute kernel before it (programmatic
+                              // dependent launch); the producer waits for it before staged loads
 };
 
 cudaError_t launch_grouped_gemm(const GemmLaunch &p, cudaStream_t stream);

@@ -28,6 +28,10 @@ __global__ void __launch_bounds__(kPermuteThreads)
                         int write_status, int only_straddling) {
     __shared__ SegmentTable table;
     __shared__ int ok;
+    // A GEMM launched after this kernel with programmatic dependent launch
+    // may start now: it waits for this grid's completion before it reads
+    // any row this kernel writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0) {
         bool good = build_segment_table(recvCounts, W, e, A, table, lane);
@@ -74,7 +78,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
 
 cudaError_t launch_permute(const PermuteLaunch &p, int num_sms, cudaStream_t stream) {
     int blocks = (p.A + kPermuteWarps - 1) / kPermuteWarps;
-    const int cap = num_sms * (2048 / kPermuteThreads);
+    const int cap = num_sms * (p.blocks_per_sm > 0 ? p.blocks_per_sm : 2048 / kPermuteThreads);
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     permute_rows_kernel<<<blocks, kPermuteThreads, 0, stream>>>(
