@@ -82,7 +82,10 @@ def assert_reduce_close(orc, got, data, scales, qtype, mode):
 
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16, torch.float32])
 @pytest.mark.parametrize("qtype,mode", COMBOS)
-@pytest.mark.parametrize("W,rows,H", [(2, 1, 1024), (4, 37, 1152), (8, 5, 8192)])
+# Shapes: below one 256-unit chunk (direct loads only); scale planes that do
+# not start on 16 bytes (direct loads only); whole chunks staged through shared
+# memory; staged chunks plus a direct-load tail.
+@pytest.mark.parametrize("W,rows,H", [(2, 1, 1024), (4, 37, 1152), (8, 5, 8192), (2, 45, 1024)])
 def test_matches_oracle(orc, qtype, mode, out_dtype, W, rows, H):
     # fp16 output: keep |sum| <= 8 * 57344 * 2^-4 < 65504, so no output overflows.
     er = (-12, -4) if out_dtype == torch.float16 else (-10, 6)
@@ -141,6 +144,23 @@ def test_output_overflow(orc):
     assert torch.isinf(got16.float()).all() and (got16.float() > 0).all()
     for dt in (torch.bfloat16, torch.float32):
         assert_reduce_close(orc, gpu_reduce(data, scales, "e4m3fn", "mx", dt), data, scales, "e4m3fn", "mx")
+
+
+def test_unaligned_scales_take_the_direct_path(orc):
+    # Float scales 4-byte but not 16-byte aligned: the bulk copies need 16, so
+    # every unit is loaded directly; the results must not change.
+    data, scales = quant_reduce_inputs(4, 64, 2048, "int8", "group128", seed=6)
+    dev = torch.device("cuda:0")
+    flat = torch.empty(scales.numel() + 1, dtype=torch.float32, device=dev)
+    odd = flat[1:].view(scales.shape)
+    odd.copy_(scales.to(dev))
+    assert odd.data_ptr() % 16 != 0
+    out = torch.empty(64, 2048, dtype=torch.bfloat16, device=dev)
+    binding.a2av_quant_reduce(data.to(dev), odd, "int8", "group128", out)
+    aligned = gpu_reduce(data, scales, "int8", "group128", torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu().view(torch.int16), aligned.view(torch.int16))
+    assert_reduce_close(orc, aligned, data, scales, "int8", "group128")
 
 
 def test_side_stream_and_determinism(orc):

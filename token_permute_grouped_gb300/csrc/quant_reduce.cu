@@ -28,9 +28,11 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "a2av_quant_reduce.h"
+#include "ptx.cuh"
 
 namespace a2av {
 
@@ -92,10 +94,52 @@ __device__ __forceinline__ float e8m0_to_float(uint32_t e) {
     return __uint_as_float(e << 23);
 }
 
+// One unit: sum over the W ranks of 16 decoded codes times their scales, then
+// the 16 results (rounded to the output type) stored at out + off.
+template <int W, int QT, int OUT>
+__device__ __forceinline__ void reduce_unit(const uint4 (&q)[W], const float (&sc)[W], void *out, int64_t off) {
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+        const uint32_t word[4] = {q[w].x, q[w].y, q[w].z, q[w].w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            float v[4];
+            decode_word<QT>(word[t], v);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[4 * t + k] = __fmaf_rn(v[k], sc[w], acc[4 * t + k]);
+        }
+    }
+    if constexpr (OUT == A2AV_FP32) {
+        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + off);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) o[t] = make_float4(acc[4 * t], acc[4 * t + 1], acc[4 * t + 2], acc[4 * t + 3]);
+    } else {
+        uint32_t packed[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if constexpr (OUT == A2AV_BF16) {
+                __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * t], acc[2 * t + 1]);
+                packed[t] = *reinterpret_cast<uint32_t *>(&b);
+            } else {
+                __half2 b = __floats2half2_rn(acc[2 * t], acc[2 * t + 1]);
+                packed[t] = *reinterpret_cast<uint32_t *>(&b);
+            }
+        }
+        uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + off);
+        o[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        o[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    }
+}
+
+// Units from u_begin on, loaded straight from global memory (any alignment
+// of the scale planes; also the tail the staged kernel leaves).
 template <int W, int QT, int MODE, int OUT>
 __global__ void __launch_bounds__(kQrThreads)
     quant_reduce_kernel(int64_t rows, int64_t H, const uint8_t *__restrict__ data, const void *__restrict__ scales,
-                        void *__restrict__ out) {
+                        void *__restrict__ out, int64_t u_begin) {
     constexpr int U = kLoadsInFlight / W;  // units per thread per step
     constexpr int64_t kGroup = MODE == A2AV_QMODE_MX ? 32 : 128;
     const int64_t vpr = H / 16;      // units per row
@@ -109,7 +153,7 @@ __global__ void __launch_bounds__(kQrThreads)
     int64_t ri[U], ci[U];
 #pragma unroll
     for (int j = 0; j < U; ++j) {
-        const int64_t u = (static_cast<int64_t>(blockIdx.x) * U + j) * kQrThreads + threadIdx.x;
+        const int64_t u = u_begin + (static_cast<int64_t>(blockIdx.x) * U + j) * kQrThreads + threadIdx.x;
         ri[j] = u / vpr;
         ci[j] = u % vpr;
     }
@@ -133,44 +177,7 @@ __global__ void __launch_bounds__(kQrThreads)
         }
 #pragma unroll
         for (int j = 0; j < U; ++j) {
-            if (ri[j] < rows) {
-                float acc[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
-#pragma unroll
-                for (int w = 0; w < W; ++w) {
-                    const uint32_t word[4] = {q[j][w].x, q[j][w].y, q[j][w].z, q[j][w].w};
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        float v[4];
-                        decode_word<QT>(word[t], v);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) acc[4 * t + k] = __fmaf_rn(v[k], sc[j][w], acc[4 * t + k]);
-                    }
-                }
-                const int64_t off = ri[j] * H + ci[j] * 16;
-                if constexpr (OUT == A2AV_FP32) {
-                    float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + off);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        o[t] = make_float4(acc[4 * t], acc[4 * t + 1], acc[4 * t + 2], acc[4 * t + 3]);
-                } else {
-                    uint32_t packed[8];
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        if constexpr (OUT == A2AV_BF16) {
-                            __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * t], acc[2 * t + 1]);
-                            packed[t] = *reinterpret_cast<uint32_t *>(&b);
-                        } else {
-                            __half2 b = __floats2half2_rn(acc[2 * t], acc[2 * t + 1]);
-                            packed[t] = *reinterpret_cast<uint32_t *>(&b);
-                        }
-                    }
-                    uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + off);
-                    o[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                    o[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                }
-            }
+            if (ri[j] < rows) reduce_unit<W, QT, OUT>(q[j], sc[j], out, ri[j] * H + ci[j] * 16);
             ci[j] += dr;
             if (ci[j] >= vpr) {
                 ci[j] -= vpr;
@@ -181,9 +188,147 @@ __global__ void __launch_bounds__(kQrThreads)
     }
 }
 
+// ---- staged kernel: chunks of 256 units (4096 outputs), brought into shared
+// memory by one-dimensional bulk copies (cp.async.bulk): per rank one copy of
+// 4096 codes and one of the chunk's 128 scale bytes (E8M0 per 32, or float
+// per 128: 4096 / 32 bytes either way).  A producer warp keeps a ring of
+// stages full; 256 consumer threads each reduce one unit per chunk from shared
+// memory.  All three arrays are contiguous, so unit u of the flattened
+// [rows, H] output is codes u*16.. of each rank and scale byte (u*16 / group
+// in elements) of each rank's scale plane.
+constexpr int kQbConsumers = 256;
+constexpr int kQbThreads = kQbConsumers + 32;
+constexpr int kQbChunk = kQbConsumers;  // units per chunk
+constexpr uint32_t kQbCodeBytes = kQbChunk * 16;
+constexpr uint32_t kQbScaleBytes = kQbChunk * 16 / 32;
+constexpr uint64_t kQbWaitLimitNs = 2000000000ull;
+constexpr uint32_t kQbHeader = 256;  // barriers and the abort flag, before the ring
+
+template <int W>
+struct Qb {
+    static constexpr uint32_t kStageBytes = W * (kQbCodeBytes + kQbScaleBytes);
+    static constexpr int kStages = W == 8 ? 3 : W == 4 ? 6 : 12;  // about 100 KB per CTA, two CTAs per SM
+    static constexpr size_t kSmem = kQbHeader + kStages * kStageBytes;
+};
+
+// Set when a staged-kernel wait gave up (it then stops early); it cannot be
+// reached by correct code, since every wait is on this CTA's own copies.
+__device__ int32_t g_qr_wait_timeouts = 0;
+
+__device__ __forceinline__ bool qb_wait(uint32_t bar, uint32_t parity, volatile int32_t *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kQbWaitLimitNs) {
+            *abort_flag = 1;
+            atomicAdd(&g_qr_wait_timeouts, 1);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+template <int W, int QT, int MODE, int OUT>
+__global__ void __launch_bounds__(kQbThreads)
+    quant_reduce_staged_kernel(int64_t chunks, int64_t plane, int64_t splane_bytes, const uint8_t *__restrict__ data,
+                               const uint8_t *__restrict__ scales, void *__restrict__ out) {
+    using L = Qb<W>;
+    extern __shared__ __align__(128) uint8_t qb_smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(qb_smem);  // [kStages], then empty[kStages]
+    uint64_t *empty = full + L::kStages;
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(empty + L::kStages);
+    const uint32_t ring = smem_u32(qb_smem) + kQbHeader;
+    static_assert(2 * L::kStages * 8 + 4 <= kQbHeader, "barriers fit in front of the ring");
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < L::kStages; ++st) {
+            mbar_init(smem_u32(&full[st]), 1);
+            mbar_init(smem_u32(&empty[st]), kQbConsumers / 32);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (warp == kQbConsumers / 32) {
+        // ---- producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x, ++it) {
+                const int st = it % L::kStages;
+                if (!qb_wait(smem_u32(&empty[st]), ((it / L::kStages) & 1) ^ 1, abort_flag)) break;
+                const uint32_t fb = smem_u32(&full[st]);
+                mbar_arrive_expect_tx(fb, L::kStageBytes);
+                const uint32_t dst = ring + st * L::kStageBytes;
+#pragma unroll
+                for (int w = 0; w < W; ++w) {
+                    bulk_copy(dst + w * kQbCodeBytes, data + w * plane + c * kQbCodeBytes, kQbCodeBytes, fb);
+                    bulk_copy(dst + W * kQbCodeBytes + w * kQbScaleBytes, scales + w * splane_bytes + c * kQbScaleBytes,
+                              kQbScaleBytes, fb);
+                }
+            }
+        }
+        return;
+    }
+    // ---- consumers: thread t reduces unit t of each chunk
+    const int t = threadIdx.x;
+    uint32_t it = 0;
+    for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x, ++it) {
+        const int st = it % L::kStages;
+        bool ready = true;
+        if (lane == 0) ready = qb_wait(smem_u32(&full[st]), (it / L::kStages) & 1, abort_flag);
+        if (!__shfl_sync(0xffffffffu, ready, 0)) break;
+        const uint8_t *stage = qb_smem + kQbHeader + st * L::kStageBytes;
+        uint4 q[W];
+        float sc[W];
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            q[w] = *reinterpret_cast<const uint4 *>(stage + w * kQbCodeBytes + t * 16);
+            const uint8_t *sp = stage + W * kQbCodeBytes + w * kQbScaleBytes;
+            if constexpr (MODE == A2AV_QMODE_MX) sc[w] = e8m0_to_float(sp[t / 2]);  // 16 codes share a byte per 32
+            else sc[w] = reinterpret_cast<const float *>(sp)[t / 8];              // one float per 128
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[st]));  // the stage's bytes are in registers now
+        reduce_unit<W, QT, OUT>(q, sc, out, (c * kQbChunk + t) * 16);
+    }
+}
+
 template <int W, int QT, int MODE, int OUT>
 cudaError_t launch_qr(const QuantReduceLaunch &p, int num_sms, cudaStream_t stream) {
     constexpr int U = kLoadsInFlight / W;
+    const int64_t units = p.rows * (p.H / 16);
+    const int64_t splane_bytes = p.rows * (p.H / 32);  // E8M0 per 32 or float per 128: H / 32 bytes per row
+    // Bulk copies need 16-byte aligned sources: the staged kernel takes the
+    // full chunks when every rank's scale plane starts on a 16-byte boundary.
+    int64_t u_begin = 0;
+    if ((reinterpret_cast<uintptr_t>(p.scales) & 15u) == 0 && splane_bytes % 16 == 0 && units >= kQbChunk) {
+        using L = Qb<W>;
+        auto kern = quant_reduce_staged_kernel<W, QT, MODE, OUT>;
+        static bool attr_set = false;  // once per instantiation
+        if (!attr_set) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kSmem)) !=
+                cudaSuccess)
+                return cudaErrorInvalidValue;
+            attr_set = true;
+        }
+        const int64_t chunks = units / kQbChunk;
+        const int64_t blocks = std::min<int64_t>(chunks, 2 * static_cast<int64_t>(num_sms));
+        kern<<<static_cast<int>(blocks), kQbThreads, L::kSmem, stream>>>(
+            chunks, p.rows * p.H, splane_bytes, static_cast<const uint8_t *>(p.data),
+            static_cast<const uint8_t *>(p.scales), p.out);
+        cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+        u_begin = chunks * kQbChunk;
+        if (u_begin == units) return cudaSuccess;
+    }
     static int resident = 0;  // CTAs per SM, from the occupancy calculator, once per instantiation
     if (resident == 0) {
         int n = 0;
@@ -193,12 +338,12 @@ cudaError_t launch_qr(const QuantReduceLaunch &p, int num_sms, cudaStream_t stre
         resident = n;
     }
     const int64_t per_block = static_cast<int64_t>(kQrThreads) * U;
-    int64_t blocks = (p.rows * (p.H / 16) + per_block - 1) / per_block;
+    int64_t blocks = (units - u_begin + per_block - 1) / per_block;
     const int64_t cap = static_cast<int64_t>(num_sms) * resident;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     quant_reduce_kernel<W, QT, MODE, OUT><<<static_cast<int>(blocks), kQrThreads, 0, stream>>>(
-        p.rows, p.H, static_cast<const uint8_t *>(p.data), p.scales, p.out);
+        p.rows, p.H, static_cast<const uint8_t *>(p.data), p.scales, p.out, u_begin);
     return cudaGetLastError();
 }
 
