@@ -901,29 +901,51 @@ def run_mx(args):
     tflops = reduce_sum(flops * args.steps, world, dev) / dev_s_max / 1e12
 
     # End to end through the same call: codes and scales of this step's
-    # activations in from pinned memory, the bf16 results back out (weights resident).
-    pin_q, pin_s = inp.ataOut_q.pin_memory(), inp.ataOut_s.pin_memory()
-    pin_xq = inp.mmX_q.pin_memory() if wl.BS else None
-    pin_xs = inp.mmX_s.pin_memory() if wl.BS else None
+    # activations (and recvCounts, mmX) in from pinned memory, the bf16
+    # results back out; weights resident.  As in the bf16 line, step i + 1's
+    # copies in and step i's copies out run on copy streams beside step i's
+    # kernels, over two device buffer sets.
+    pin = {k: getattr(inp, k).pin_memory() for k in ("ataOut_q", "ataOut_s", "mmX_q", "mmX_s")
+           if getattr(inp, k) is not None}
+    rc_pin = torch.from_numpy(inp.recvCounts).pin_memory()
     out_y = torch.empty(A, wl.N1, dtype=torch.bfloat16).pin_memory()
     out_m = torch.empty(wl.BS, wl.N2, dtype=torch.bfloat16).pin_memory() if wl.BS else None
-    h2d = pin_q.numel() + pin_s.numel() + (pin_xq.numel() + pin_xs.numel() if wl.BS else 0) + rc_dev.numel() * 4
+    h2d = sum(t.numel() for t in pin.values()) + rc_pin.numel() * 4
     d2h = out_y.numel() * 2 + (out_m.numel() * 2 if wl.BS else 0)
-    rc_pin = torch.from_numpy(inp.recvCounts).pin_memory()
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    bufs = [sets[0], sets[1 % reps]]
+    rcs = [rc_dev, torch.empty_like(rc_dev)]
+    h2d_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    d2h_done = [torch.cuda.Event() for _ in range(2)]
     e2e_steps = max(3, min(args.steps, 20))
 
+    def issue_h2d(b):
+        with torch.cuda.stream(h2d_stream):
+            h2d_stream.wait_event(comp_done[b])
+            for k, t in pin.items():
+                bufs[b][k].copy_(t, non_blocking=True)
+            rcs[b].copy_(rc_pin, non_blocking=True)
+            h2d_done[b].record(h2d_stream)
+
     def e2e_step(i):
-        st = sets[i % 2]
-        st["ataOut_q"].copy_(pin_q, non_blocking=True)
-        st["ataOut_s"].copy_(pin_s, non_blocking=True)
-        rc_dev.copy_(rc_pin, non_blocking=True)
-        if wl.BS:
-            st["mmX_q"].copy_(pin_xq, non_blocking=True)
-            st["mmX_s"].copy_(pin_xs, non_blocking=True)
-        step(i % 2)
-        out_y.copy_(st["gmmY"], non_blocking=True)
-        if wl.BS:
-            out_m.copy_(st["mmY"], non_blocking=True)
+        b = i % 2
+        if i == 0:
+            issue_h2d(0)
+        stream.wait_event(h2d_done[b])
+        stream.wait_event(d2h_done[b])
+        st = bufs[b]
+        plan.run(st["ataOut_q"], st["ataOut_s"], rcs[b], st["gmmWeight_q"], st["gmmWeight_s"], st["mmX_q"],
+                 st["mmX_s"], st["mmWeight_q"], st["mmWeight_s"], gmmY=st["gmmY"], mmY=st["mmY"], stream=stream)
+        comp_done[b].record(stream)
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(comp_done[b])
+            out_y.copy_(st["gmmY"], non_blocking=True)
+            if wl.BS:
+                out_m.copy_(st["mmY"], non_blocking=True)
+            d2h_done[b].record(d2h_stream)
+        if i + 1 < e2e_steps:
+            issue_h2d(1 - b)
 
     _, e2e_max = timed_region(e2e_step, e2e_steps, world, dev, sync)
     e2e_tflops = reduce_sum(flops * e2e_steps, world, dev) / e2e_max / 1e12
@@ -955,7 +977,8 @@ def run_mx(args):
                      "algorithmic_bytes": nbytes},
         "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
-                "inputs_copied": "activation codes and scales, recvCounts, mmX codes and scales (weights resident)"},
+                "inputs_copied": "activation codes and scales, recvCounts, mmX codes and scales (weights resident)",
+                "overlap": "step i+1's H2D and step i's D2H run on copy streams beside step i's kernels"},
         "gpu_launches": (3 if A else 1) * args.steps,
         "clocks": clocks.summary(),
     }
