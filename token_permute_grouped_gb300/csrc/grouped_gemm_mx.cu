@@ -279,13 +279,17 @@ __device__ __forceinline__ void mx_cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// An arrival on a barrier of the even CTA (own CTA when single).
+// An arrival on a barrier of the even CTA (own CTA when single).  The odd
+// CTA arrives through the barrier's cluster address with the default
+// (CTA-scope release) semantics: what it hands over is TMEM content, ordered
+// by tcgen05.wait::st and tcgen05.fence::before_thread_sync before the arrival
+// and by the reader's tcgen05.fence::after_thread_sync after its wait.  A
+// cluster-scope release arrival measured about 1400 cycles here, more than a
+// stage's MMAs, once per stage and scale warp.
 template <bool PAIR>
-__device__ __forceinline__ void mx_arrive_leader(uint32_t own_addr) {
-    if constexpr (PAIR)
-        asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-                         mx_map_to_rank(own_addr, 0))
-                     : "memory");
+__device__ __forceinline__ void mx_arrive_leader(uint32_t own_addr, uint32_t rank) {
+    if (PAIR && rank != 0)
+        asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(mx_map_to_rank(own_addr, 0)) : "memory");
     else
         mbar_arrive(own_addr);
 }
@@ -597,7 +601,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mx_arrive_leader<PAIR>(smem_u32(&C.sf_full[s]));
+                if (lane == 0) mx_arrive_leader<PAIR>(smem_u32(&C.sf_full[s]), rank);
             }
         }
     } else if (warp == kMxScaleLoadWarp) {
@@ -668,7 +672,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 } else {  // every load of this tile has landed: release the accumulator
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mx_arrive_leader<PAIR>(smem_u32(&C.tempty[acc]));
+                    if (lane == 0) mx_arrive_leader<PAIR>(smem_u32(&C.tempty[acc]), rank);
                 }
                 if (valid) {
 #pragma unroll
