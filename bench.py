@@ -79,7 +79,7 @@ def algorithmic_bytes(wl, A, permute_out):
 # The sources each measured call depends on (kernels and host setup).
 GEMM_SOURCES = ("api.cu", "grouped_gemm.cu", "kernels.h", "permute.cu", "plan.cuh", "ptx.cuh")
 QREDUCE_SOURCES = ("quant_reduce.cu", "ptx.cuh", "../../include/a2av_quant_reduce.h")
-MX_SOURCES = ("grouped_gemm_mx.cu", "permute.cu", "plan.cuh", "ptx.cuh", "kernels.h", "../../include/a2av_gmm_mx.h")
+MX_SOURCES = ("grouped_gemm_mx.cu", "plan.cuh", "ptx.cuh", "../../include/a2av_gmm_mx.h")
 
 
 def source_hash(names=GEMM_SOURCES):

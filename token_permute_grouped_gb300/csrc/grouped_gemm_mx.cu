@@ -31,6 +31,7 @@
 // the main loop of the next), then per stage eight A-scale and eight B-scale
 // columns.  Every wait is bounded: on timeout the CTA sets kStatusTimeout and
 // winds down.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -39,7 +40,6 @@
 #include <mutex>
 
 #include "a2av_gmm_mx.h"
-#include "kernels.h"
 #include "plan.cuh"
 #include "ptx.cuh"
 
@@ -702,6 +702,64 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
     }
 }
 
+// ---------------------------------------------------------------- permute
+//
+// The Permute step for mx operands: the expert-major copy of each row's H1
+// code bytes and H1/32 scale bytes, one warp per row with one segment lookup
+// for both, 16-byte vectors.  only_straddling: only rows of 128-row halves
+// that straddle a segment boundary (the GEMM reads the others in place).
+constexpr int kMxPermThreads = 256;
+
+__device__ __forceinline__ uint4 mx_ld_stream(const uint4 *ptr) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
+}
+
+__global__ void __launch_bounds__(kMxPermThreads)
+    mx_permute_kernel(const int32_t *__restrict__ recvCounts, int W, int e, int A, int H1,
+                      const uint4 *__restrict__ src_q, const uint4 *__restrict__ src_s, uint4 *__restrict__ dst_q,
+                      uint4 *__restrict__ dst_s, int32_t *status, int only_straddling) {
+    __shared__ SegmentTable table;
+    __shared__ int ok;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (warp == 0) {
+        const bool good = build_segment_table(recvCounts, W, e, A, table, lane);
+        if (lane == 0) {
+            ok = good;
+            if (blockIdx.x == 0) *status = good ? 0 : kStatusBadCounts;  // the first kernel of the call
+        }
+    }
+    __syncthreads();
+    if (!ok) return;
+    const int vq = H1 / 16, vs = H1 / 512;  // 16-byte vectors per code row and per scale row
+    const int nwarps = gridDim.x * (kMxPermThreads / 32);
+    for (int d = blockIdx.x * (kMxPermThreads / 32) + warp; d < A; d += nwarps) {
+        const int seg = segment_of(table, W, e, d);
+        if (only_straddling) {
+            const int j = seg / W;
+            const int g0 = table.dst[j * W], g1 = table.dst[(j + 1) * W];
+            if (half_in_one_segment(table, W, e, g0 + (d - g0) / kHalfRows * kHalfRows, g1)) continue;
+        }
+        const size_t srow = static_cast<size_t>(source_row_in(table, W, e, seg, d));
+        const uint4 *in = src_q + srow * vq;
+        uint4 *out = dst_q + static_cast<size_t>(d) * vq;
+        int v = lane;
+        for (; v + 96 < vq; v += 128) {
+            const uint4 a = mx_ld_stream(in + v), b = mx_ld_stream(in + v + 32), c = mx_ld_stream(in + v + 64),
+                        f = mx_ld_stream(in + v + 96);
+            out[v] = a;
+            out[v + 32] = b;
+            out[v + 64] = c;
+            out[v + 96] = f;
+        }
+        for (; v < vq; v += 32) out[v] = mx_ld_stream(in + v);
+        for (int u = lane; u < vs; u += 32) dst_s[static_cast<size_t>(d) * vs + u] = mx_ld_stream(src_s + srow * vs + u);
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 constexpr size_t kMxStatusBytes = 256;
@@ -859,22 +917,22 @@ a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, 
             dq = static_cast<uint8_t *>(workspace) + kMxStatusBytes;
             ds = dq + align256(static_cast<size_t>(d.A) * d.H1);
         }
-        // The row permute moves 16-byte vectors of rows given in 2-byte
-        // elements: a code row is H1 / 2 of them, a scale row H1 / 64.
         // Without permuteOut only the 128-row halves that straddle a segment
-        // boundary are staged; the kernel reads the others from ataOut.
+        // boundary are staged; the GEMM reads the others from ataOut.
         const int32_t partial = d.want_permute_out ? 0 : 1;
-        PermuteLaunch pq{recvCounts, d.W, d.e, static_cast<int32_t>(d.A), static_cast<int32_t>(d.H1 / 2),
-                         ataOut_q, dq, status, 1, partial};
-        PermuteLaunch ps{recvCounts, d.W, d.e, static_cast<int32_t>(d.A), static_cast<int32_t>(d.H1 / 64),
-                         ataOut_s, ds, status, 0, partial};
         if (partial) {
             if (!mx_codes_map(&g.tmA_direct, ataOut_q, 1, d.A, d.H1)) return A2AV_ERR_CUDA;
             if (!mx_scales_map(&g.tmSA_direct, ataOut_s, 1, d.A, d.H1, MX_BM)) return A2AV_ERR_CUDA;
             g.direct_halves = 1;
         }
-        if (launch_permute(pq, sms, stream) != cudaSuccess) return A2AV_ERR_CUDA;
-        if (launch_permute(ps, sms, stream) != cudaSuccess) return A2AV_ERR_CUDA;
+        const int64_t warps = kMxPermThreads / 32;
+        const int blocks = static_cast<int>(
+            std::max<int64_t>(1, std::min<int64_t>((d.A + warps - 1) / warps, static_cast<int64_t>(sms) * 8)));
+        mx_permute_kernel<<<blocks, kMxPermThreads, 0, stream>>>(
+            recvCounts, d.W, d.e, static_cast<int32_t>(d.A), static_cast<int32_t>(d.H1),
+            static_cast<const uint4 *>(ataOut_q), static_cast<const uint4 *>(ataOut_s), reinterpret_cast<uint4 *>(dq),
+            reinterpret_cast<uint4 *>(ds), status, partial);
+        if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
         permute_ran = true;
         if (!mx_codes_map(&g.tmA, dq, 1, d.A, d.H1)) return A2AV_ERR_CUDA;
         if (!mx_scales_map(&g.tmSA, ds, 1, d.A, d.H1, MX_BM)) return A2AV_ERR_CUDA;
