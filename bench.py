@@ -991,6 +991,9 @@ def run_mx(args):
 
 
 def main(argv=None):
+    # NCCL may print its version banner on stdout when a process group starts
+    # (depending on NCCL_DEBUG); stdout carries exactly one JSON line.
+    os.environ.setdefault("NCCL_DEBUG_FILE", "/dev/stderr")
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
