@@ -598,9 +598,9 @@ def run_qreduce(args):
             for _ in range(reps)]
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
+    def step(i):  # on the current stream (the graph's capture stream while capturing)
         d, sc, o = sets[i % reps]
-        binding.a2av_quant_reduce(d, sc, wl.qtype, wl.mode, o, stream=stream)
+        binding.a2av_quant_reduce(d, sc, wl.qtype, wl.mode, o)
 
     sync = torch.cuda.synchronize
     for i in range(args.warmup):
@@ -608,6 +608,9 @@ def run_qreduce(args):
     sync()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
 
+    # Eager: the K calls launched one by one from Python.  A call's kernel
+    # takes about as long as its host-side argument checks and launch, so
+    # this also measures the launch path.
     def timed_step(i):
         if i == 0:
             ev[0].record(stream)
@@ -615,8 +618,24 @@ def run_qreduce(args):
         if i == args.steps - 1:
             ev[1].record(stream)
 
+    timed_region(timed_step, args.steps, world, dev, sync)
+    eager_s = ev[0].elapsed_time(ev[1]) / 1e3
+    # The same K calls captured in one CUDA graph and replayed: device time
+    # of the kernels back to back, which the value reports.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(args.steps):
+            step(i)
+    graph.replay()
+    sync()
+
+    def replay(_):
+        ev[0].record(stream)
+        graph.replay()
+        ev[1].record(stream)
+
     with ClockSampler(local) as clocks:
-        timed_region(timed_step, args.steps, world, dev, sync)
+        timed_region(replay, 1, world, dev, sync)
     dev_s = ev[0].elapsed_time(ev[1]) / 1e3
     dev_s_max = reduce_max(dev_s, world, dev)
     gbs = reduce_sum(nbytes * args.steps, world, dev) / dev_s_max / 1e9
@@ -672,6 +691,8 @@ def run_qreduce(args):
         "config": {"workload": wl.name, "W": wl.W, "rows": wl.rows, "H": wl.H, "qtype": wl.qtype, "mode": wl.mode,
                    "out": "bf16", "accumulate": "fp32", "bytes_per_call": nbytes,
                    "us_per_call": round(dev_s / args.steps * 1e6, 2),
+                   "timing": "the K calls captured in one CUDA graph and replayed (CUDA events around the replay)",
+                   "eager_us_per_call": round(eager_s / args.steps * 1e6, 2),
                    "l2": (f"inputs rotated over {reps} replicas ({reps * nbytes / 2**20:.0f} MiB > 129 MiB L2)"
                           if reps * nbytes > L2_BYTES else
                           f"all {reps} replicas ({reps * nbytes / 2**20:.0f} MiB) fit in L2: a latency-bound case")},

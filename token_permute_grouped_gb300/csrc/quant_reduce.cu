@@ -94,24 +94,47 @@ __device__ __forceinline__ float e8m0_to_float(uint32_t e) {
     return __uint_as_float(e << 23);
 }
 
+// Two float32 lanes in one 64-bit register, and their fused multiply-add
+// (fma.rn.f32x2: each lane is one fma.rn.f32, so results equal the scalar
+// form, in half the instructions).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ void f32x2_split(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
 // One unit: sum over the W ranks of 16 decoded codes times their scales, then
 // the 16 results (rounded to the output type) stored at out + off.
 template <int W, int QT, int OUT>
 __device__ __forceinline__ void reduce_unit(const uint4 (&q)[W], const float (&sc)[W], void *out, int64_t off) {
-    float acc[16];
+    uint64_t acc2[8];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+    for (int k = 0; k < 8; ++k) acc2[k] = 0;  // +0.0f in both lanes
 #pragma unroll
     for (int w = 0; w < W; ++w) {
         const uint32_t word[4] = {q[w].x, q[w].y, q[w].z, q[w].w};
+        const uint64_t s2 = f32x2(sc[w], sc[w]);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
             float v[4];
             decode_word<QT>(word[t], v);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) acc[4 * t + k] = __fmaf_rn(v[k], sc[w], acc[4 * t + k]);
+            acc2[2 * t] = fma_f32x2(f32x2(v[0], v[1]), s2, acc2[2 * t]);
+            acc2[2 * t + 1] = fma_f32x2(f32x2(v[2], v[3]), s2, acc2[2 * t + 1]);
         }
     }
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) f32x2_split(acc2[k], acc[2 * k], acc[2 * k + 1]);
     if constexpr (OUT == A2AV_FP32) {
         float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + off);
 #pragma unroll
