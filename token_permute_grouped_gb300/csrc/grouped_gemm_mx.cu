@@ -101,6 +101,7 @@ struct MxLaunch {
     void *mmY;
     int32_t *status;
     int32_t write_status;
+    int32_t after_permute;  // launched beside the permute kernel: wait for it before a staged read
     int32_t qtype;  // 0 E4M3FN, 1 E5M2 (both operands)
     int32_t pair;
     int32_t grid;
@@ -465,6 +466,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
+            bool staged_ready = !p.after_permute;  // the permute kernel's rows are visible
             for (int t = unit; t < total && ok; t += nunits) {
                 const MxTile w = mx_decode_tile(C, t);
                 const bool shared = w.g >= e;
@@ -476,6 +478,11 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 if (!shared && mx_direct_row(p, C.seg, C.g[w.g].row0, C.g[w.g].rows, ya, &src)) {
                     ta = &p.tmA_direct;
                     ya = src;
+                } else if (!shared && !staged_ready) {
+                    // This half reads staged rows: wait for the permute grid
+                    // (the tiles before needed none of its output).
+                    asm volatile("griddepcontrol.wait;" ::: "memory");
+                    staged_ready = true;
                 }
                 const int xn = w.n * TILE_N + static_cast<int>(rank) * MX_BNC;
                 const int z = shared ? 0 : w.g;
@@ -611,6 +618,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
         if (lane == 0) {
             uint32_t chunk = 0;
             bool ok = true;
+            bool staged_ready = !p.after_permute;
             for (int t = unit; t < total && ok; t += nunits) {
                 const MxTile w = mx_decode_tile(C, t);
                 const bool shared = w.g >= e;
@@ -622,6 +630,9 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 if (!shared && mx_direct_row(p, C.seg, C.g[w.g].row0, C.g[w.g].rows, ya, &src)) {
                     tsa = &p.tmSA_direct;
                     ya = src;
+                } else if (!shared && !staged_ready) {
+                    asm volatile("griddepcontrol.wait;" ::: "memory");
+                    staged_ready = true;
                 }
                 const int z = shared ? 0 : w.g;
                 for (int kb = 0; kb < K / MX_BK; kb += 2, ++chunk) {
@@ -723,7 +734,12 @@ __global__ void __launch_bounds__(kMxPermThreads)
                       const uint4 *__restrict__ src_q, const uint4 *__restrict__ src_s, uint4 *__restrict__ dst_q,
                       uint4 *__restrict__ dst_s, int32_t *status, int only_straddling) {
     __shared__ SegmentTable table;
+    __shared__ StagedHalves halves;
     __shared__ int ok;
+    // The GEMM launched after this kernel with programmatic dependent launch
+    // may start now: it waits for this grid's completion before it reads a
+    // row this kernel writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0) {
         const bool good = build_segment_table(recvCounts, W, e, A, table, lane);
@@ -734,29 +750,57 @@ __global__ void __launch_bounds__(kMxPermThreads)
     }
     __syncthreads();
     if (!ok) return;
+    // Work items are 2 KB pieces of a code row (four 16-byte vectors per lane,
+    // all loaded before any is stored); the first piece of a row also moves
+    // its scale row.  One memory round trip per item.
     const int vq = H1 / 16, vs = H1 / 512;  // 16-byte vectors per code row and per scale row
+    const int ppr = (vq + 127) / 128;
     const int nwarps = gridDim.x * (kMxPermThreads / 32);
-    for (int d = blockIdx.x * (kMxPermThreads / 32) + warp; d < A; d += nwarps) {
-        const int seg = segment_of(table, W, e, d);
-        if (only_straddling) {
-            const int j = seg / W;
-            const int g0 = table.dst[j * W], g1 = table.dst[(j + 1) * W];
-            if (half_in_one_segment(table, W, e, g0 + (d - g0) / kHalfRows * kHalfRows, g1)) continue;
-        }
+    const int gw = blockIdx.x * (kMxPermThreads / 32) + warp;
+    const auto copy_piece = [&](int d, int seg, int piece) {
+        const int v0 = piece * 128 + lane;
         const size_t srow = static_cast<size_t>(source_row_in(table, W, e, seg, d));
         const uint4 *in = src_q + srow * vq;
         uint4 *out = dst_q + static_cast<size_t>(d) * vq;
-        int v = lane;
-        for (; v + 96 < vq; v += 128) {
-            const uint4 a = mx_ld_stream(in + v), b = mx_ld_stream(in + v + 32), c = mx_ld_stream(in + v + 64),
-                        f = mx_ld_stream(in + v + 96);
-            out[v] = a;
-            out[v + 32] = b;
-            out[v + 64] = c;
-            out[v + 96] = f;
+        uint4 r[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (v0 + 32 * k < vq) r[k] = mx_ld_stream(in + v0 + 32 * k);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (v0 + 32 * k < vq) out[v0 + 32 * k] = r[k];
+        if (piece == 0)
+            for (int u = lane; u < vs; u += 32)
+                dst_s[static_cast<size_t>(d) * vs + u] = mx_ld_stream(src_s + srow * vs + u);
+    };
+    int listed = -1;
+    if (only_straddling) {
+        list_staged_halves(table, W, e, halves);
+        listed = halves.n;
+    }
+    if (listed >= 0) {
+        // Only the rows of the halves the GEMM cannot read in place.
+        const int per_half = kHalfRows * ppr;
+        for (int i = gw; i < listed * per_half; i += nwarps) {
+            const int hi = i / per_half, rem = i - hi * per_half;
+            const int r = rem / ppr;
+            const int2 span = halves.span[hi];
+            const int d = span.x + r;
+            if (d < span.y) copy_piece(d, segment_of(table, W, e, d), rem - r * ppr);
         }
-        for (; v < vq; v += 32) out[v] = mx_ld_stream(in + v);
-        for (int u = lane; u < vs; u += 32) dst_s[static_cast<size_t>(d) * vs + u] = mx_ld_stream(src_s + srow * vs + u);
+    } else {
+        const int64_t items = static_cast<int64_t>(A) * ppr;
+        for (int64_t i = gw; i < items; i += nwarps) {
+            const int d = static_cast<int>(i / ppr);
+            const int seg = segment_of(table, W, e, d);
+            if (only_straddling) {
+                // More staged halves than the list holds: test each row's half.
+                const int j = seg / W;
+                const int g0 = table.dst[j * W], g1 = table.dst[(j + 1) * W];
+                if (half_in_one_segment(table, W, e, g0 + (d - g0) / kHalfRows * kHalfRows, g1)) continue;
+            }
+            copy_piece(d, seg, static_cast<int>(i - static_cast<int64_t>(d) * ppr));
+        }
     }
 }
 
@@ -938,6 +982,7 @@ a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, 
         if (!mx_scales_map(&g.tmSA, ds, 1, d.A, d.H1, MX_BM)) return A2AV_ERR_CUDA;
     }
     g.write_status = permute_ran ? 0 : 1;
+    g.after_permute = permute_ran ? 1 : 0;
 
     // Persistent grid: one CTA (pair: cluster of two) per SM (pair), never
     // more than there can be tiles.
@@ -957,13 +1002,22 @@ a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, 
     cfg.blockDim = dim3(MX_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = pair ? 2 : 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n_attr = 0;
+    if (pair) {
+        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+        attr[n_attr].val.clusterDim.x = 2;
+        attr[n_attr].val.clusterDim.y = 1;
+        attr[n_attr].val.clusterDim.z = 1;
+        ++n_attr;
+    }
+    if (permute_ran) {  // start beside the permute kernel; the loaders wait where they must
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+        ++n_attr;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pair ? 1 : 0;
+    cfg.numAttrs = n_attr;
     if (cudaLaunchKernelEx(&cfg, kern, g) != cudaSuccess) return A2AV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? A2AV_OK : A2AV_ERR_CUDA;
 }

@@ -1,8 +1,8 @@
 // Permute: ataOut (rank-major) -> expert-major rows, a pure row gather.
 //
 // "aclnnAlltoAllvGroupedMatMul", Formula: permuteOut = Permute(ataOut).
-// One warp moves one row at a time with 16-byte vector loads and stores
-// (coalesced across the warp); each CTA first rebuilds the segment table from
+// A warp moves one 2 KB piece of a row at a time with 16-byte vector loads
+// and stores (coalesced across the warp); each CTA first rebuilds the segment table from
 // recvCounts in shared memory (one warp, a few hundred cycles).
 #include "kernels.h"
 #include "plan.cuh"
@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
                         const uint4 *__restrict__ src, uint4 *__restrict__ dst, int32_t *status,
                         int write_status, int only_straddling) {
     __shared__ SegmentTable table;
+    __shared__ StagedHalves halves;
     __shared__ int ok;
     // A GEMM launched after this kernel with programmatic dependent launch
     // may start now: it waits for this grid's completion before it reads
@@ -46,31 +47,53 @@ __global__ void __launch_bounds__(kPermuteThreads)
     __syncthreads();
     if (!ok) return;
 
+    // Work items are 2 KB pieces of a row (four 16-byte vectors per lane, all
+    // loaded before any is stored): one memory round trip per item, and the
+    // rows of a call spread over every warp of the grid.
     const int vpr = H1 / 8;  // 16-byte vectors per row
+    const int ppr = (vpr + 127) / 128;
     const int nwarps = gridDim.x * kPermuteWarps;
-    for (int d = blockIdx.x * kPermuteWarps + warp; d < A; d += nwarps) {
-        const int seg = segment_of(table, W, e, d);
-        if (only_straddling) {
-            // Copy only the rows of 128-row halves that the GEMM cannot read
-            // in place (see half_in_one_segment).
-            const int j = seg / W;
-            const int g0 = table.dst[j * W], g1 = table.dst[(j + 1) * W];
-            const int first = g0 + (d - g0) / kHalfRows * kHalfRows;
-            if (half_in_one_segment(table, W, e, first, g1)) continue;
-        }
-        const int s = source_row_in(table, W, e, seg, d);
-        const uint4 *in = src + static_cast<size_t>(s) * vpr;
+    const int gw = blockIdx.x * kPermuteWarps + warp;
+    const auto copy_piece = [&](int d, int seg, int piece) {
+        const int v0 = piece * 128 + lane;
+        const uint4 *in = src + static_cast<size_t>(source_row_in(table, W, e, seg, d)) * vpr;
         uint4 *out = dst + static_cast<size_t>(d) * vpr;
-        int v = lane;
-        for (; v + 96 < vpr; v += 128) {
-            uint4 a = ld_stream(in + v), b = ld_stream(in + v + 32), c = ld_stream(in + v + 64),
-                  f = ld_stream(in + v + 96);
-            out[v] = a;
-            out[v + 32] = b;
-            out[v + 64] = c;
-            out[v + 96] = f;
+        uint4 r[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (v0 + 32 * k < vpr) r[k] = ld_stream(in + v0 + 32 * k);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (v0 + 32 * k < vpr) out[v0 + 32 * k] = r[k];
+    };
+    int listed = -1;
+    if (only_straddling) {
+        list_staged_halves(table, W, e, halves);
+        listed = halves.n;
+    }
+    if (listed >= 0) {
+        // Only the rows of the halves the GEMM cannot read in place.
+        const int per_half = kHalfRows * ppr;
+        for (int i = gw; i < listed * per_half; i += nwarps) {
+            const int hi = i / per_half, rem = i - hi * per_half;
+            const int r = rem / ppr;
+            const int2 span = halves.span[hi];
+            const int d = span.x + r;
+            if (d < span.y) copy_piece(d, segment_of(table, W, e, d), rem - r * ppr);
         }
-        for (; v < vpr; v += 32) out[v] = ld_stream(in + v);
+    } else {
+        const int64_t items = static_cast<int64_t>(A) * ppr;
+        for (int64_t i = gw; i < items; i += nwarps) {
+            const int d = static_cast<int>(i / ppr);
+            const int seg = segment_of(table, W, e, d);
+            if (only_straddling) {
+                // More staged halves than the list holds: test each row's half.
+                const int j = seg / W;
+                const int g0 = table.dst[j * W], g1 = table.dst[(j + 1) * W];
+                if (half_in_one_segment(table, W, e, g0 + (d - g0) / kHalfRows * kHalfRows, g1)) continue;
+            }
+            copy_piece(d, seg, static_cast<int>(i - static_cast<int64_t>(d) * ppr));
+        }
     }
 }
 

@@ -110,6 +110,68 @@ __device__ __forceinline__ bool half_in_one_segment(const SegmentTable &t, int W
     return segment_of(t, W, e, first) == segment_of(t, W, e, last);
 }
 
+// The 128-row halves of the GEMM's routed tiles that do not lie in one
+// segment, which the GEMM reads from the staging copy: [first row, end row),
+// end the smaller of first + 128 and the group's end, in ascending order.
+constexpr int kMaxStagedHalves = 2048;
+
+struct StagedHalves {
+    int32_t n;  // halves listed, or -1 when there are more than kMaxStagedHalves
+    int32_t half0[kMaxExperts + 1];  // first half of each expert group; half0[e] = all halves
+    int32_t warp_count[32];
+    int2 span[kMaxStagedHalves];
+};
+
+// Built by the whole block (blockDim.x a multiple of 32) after the segment
+// table; every block of a grid builds the same list.
+__device__ __forceinline__ void list_staged_halves(const SegmentTable &t, int W, int e, StagedHalves &s) {
+    const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32, nwarps = blockDim.x / 32;
+    if (warp == 0) {
+        int nh = 0;
+        if (lane < e) nh = (t.dst[(lane + 1) * W] - t.dst[lane * W] + kHalfRows - 1) / kHalfRows;
+        int inc = nh;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += v;
+        }
+        if (lane < e) s.half0[lane] = inc - nh;
+        const int all = __shfl_sync(0xffffffffu, inc, 31);
+        if (lane == 0) s.half0[e] = all;
+    }
+    __syncthreads();
+    const int total = s.half0[e];
+    int base = 0;
+    for (int h0 = 0; h0 < total; h0 += blockDim.x) {
+        const int h = h0 + tid;
+        bool staged = false;
+        int first = 0, end = 0;
+        if (h < total) {
+            int j = 0;
+            while (h >= s.half0[j + 1]) ++j;  // the group holding half h
+            const int g1 = t.dst[(j + 1) * W];
+            first = t.dst[j * W] + (h - s.half0[j]) * kHalfRows;
+            end = min(first + kHalfRows, g1);
+            staged = !half_in_one_segment(t, W, e, first, g1);
+        }
+        const uint32_t mask = __ballot_sync(0xffffffffu, staged);
+        if (lane == 0) s.warp_count[warp] = __popc(mask);
+        __syncthreads();
+        int before = base, round = 0;
+        for (int w = 0; w < nwarps; ++w) {
+            const int c = s.warp_count[w];
+            if (w < warp) before += c;
+            round += c;
+        }
+        const int idx = before + __popc(mask & ((1u << lane) - 1u));
+        if (staged && idx < kMaxStagedHalves) s.span[idx] = make_int2(first, end);
+        base += round;
+        __syncthreads();  // warp_count is rewritten next round
+    }
+    if (tid == 0) s.n = base > kMaxStagedHalves ? -1 : base;
+    __syncthreads();
+}
+
 // ataOut row feeding permuteOut row d (0 <= d < A).
 __device__ __forceinline__ int32_t source_row(const SegmentTable &t, int W, int e, int32_t d) {
     return source_row_in(t, W, e, segment_of(t, W, e, d), d);
