@@ -720,6 +720,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
 // for both, 16-byte vectors.  only_straddling: only rows of 128-row halves
 // that straddle a segment boundary (the GEMM reads the others in place).
 constexpr int kMxPermThreads = 256;
+constexpr int kPieceVecs = 4;  // 16-byte vectors per lane in one work item (2 KB per warp)
 
 __device__ __forceinline__ uint4 mx_ld_stream(const uint4 *ptr) {
     uint4 v;
@@ -750,24 +751,24 @@ __global__ void __launch_bounds__(kMxPermThreads)
     }
     __syncthreads();
     if (!ok) return;
-    // Work items are 2 KB pieces of a code row (four 16-byte vectors per lane,
+    // Work items are pieces of a code row (kPieceVecs 16-byte vectors per lane,
     // all loaded before any is stored); the first piece of a row also moves
     // its scale row.  One memory round trip per item.
     const int vq = H1 / 16, vs = H1 / 512;  // 16-byte vectors per code row and per scale row
-    const int ppr = (vq + 127) / 128;
+    const int ppr = (vq + 32 * kPieceVecs - 1) / (32 * kPieceVecs);
     const int nwarps = gridDim.x * (kMxPermThreads / 32);
     const int gw = blockIdx.x * (kMxPermThreads / 32) + warp;
     const auto copy_piece = [&](int d, int seg, int piece) {
-        const int v0 = piece * 128 + lane;
+        const int v0 = piece * 32 * kPieceVecs + lane;
         const size_t srow = static_cast<size_t>(source_row_in(table, W, e, seg, d));
         const uint4 *in = src_q + srow * vq;
         uint4 *out = dst_q + static_cast<size_t>(d) * vq;
-        uint4 r[4];
+        uint4 r[kPieceVecs];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < kPieceVecs; ++k)
             if (v0 + 32 * k < vq) r[k] = mx_ld_stream(in + v0 + 32 * k);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < kPieceVecs; ++k)
             if (v0 + 32 * k < vq) out[v0 + 32 * k] = r[k];
         if (piece == 0)
             for (int u = lane; u < vs; u += 32)

@@ -13,6 +13,7 @@ namespace {
 
 constexpr int kPermuteThreads = 256;
 constexpr int kPermuteWarps = kPermuteThreads / 32;
+constexpr int kPieceVecs = 4;  // 16-byte vectors per lane in one work item (2 KB per warp)
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     uint4 v;
@@ -47,23 +48,23 @@ __global__ void __launch_bounds__(kPermuteThreads)
     __syncthreads();
     if (!ok) return;
 
-    // Work items are 2 KB pieces of a row (four 16-byte vectors per lane, all
+    // Work items are pieces of a row (kPieceVecs 16-byte vectors per lane, all
     // loaded before any is stored): one memory round trip per item, and the
     // rows of a call spread over every warp of the grid.
     const int vpr = H1 / 8;  // 16-byte vectors per row
-    const int ppr = (vpr + 127) / 128;
+    const int ppr = (vpr + 32 * kPieceVecs - 1) / (32 * kPieceVecs);
     const int nwarps = gridDim.x * kPermuteWarps;
     const int gw = blockIdx.x * kPermuteWarps + warp;
     const auto copy_piece = [&](int d, int seg, int piece) {
-        const int v0 = piece * 128 + lane;
+        const int v0 = piece * 32 * kPieceVecs + lane;
         const uint4 *in = src + static_cast<size_t>(source_row_in(table, W, e, seg, d)) * vpr;
         uint4 *out = dst + static_cast<size_t>(d) * vpr;
-        uint4 r[4];
+        uint4 r[kPieceVecs];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < kPieceVecs; ++k)
             if (v0 + 32 * k < vpr) r[k] = ld_stream(in + v0 + 32 * k);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < kPieceVecs; ++k)
             if (v0 + 32 * k < vpr) out[v0 + 32 * k] = r[k];
     };
     int listed = -1;
