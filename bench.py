@@ -394,7 +394,7 @@ def run_gpu(args):
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
-    print(json.dumps(line), flush=True)
+    emit(line)
     barrier(world)
 
 
@@ -470,7 +470,7 @@ def run_reference(args):
         "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
-    print(json.dumps(line), flush=True)
+    emit(line)
 
 
 def run_amp(args):
@@ -504,7 +504,7 @@ def run_amp(args):
     upd_us = ev[1].elapsed_time(ev[2]) * 1e3 / args.steps
     gbs = n * 2 / scan_s / 1e9
     pk, pk_kind = peaks()
-    print(json.dumps({
+    emit({
         "metric": "loss-scale step: inf/NaN scan GB/s over a bf16 layer output; us per scale update",
         "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(scan_s * 1e3, 4), "higher_is_better": True, "scaling": "weak",
@@ -516,7 +516,7 @@ def run_amp(args):
                      "peak_source": f"{pk_kind} copy bandwidth (read + write); the scan only reads"},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks.summary(),
-    }), flush=True)
+    })
 
 
 # ----------------------------------------------------------- quantised reduce
@@ -573,7 +573,7 @@ def run_qreduce(args):
             tot_b += b
             tot_s += sec
         gbs = tot_b / tot_s / 1e9
-        print(json.dumps({
+        emit({
             "impl": "reference", "metric": QR_METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s * 1e3 / max(1, args.steps), 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -583,7 +583,7 @@ def run_qreduce(args):
                              "sample": desc},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0,
-        }), flush=True)
+        })
         return
     assert torch.cuda.is_available(), "bench.py needs a GPU (use --impl reference for the CPU oracle)"
     torch.cuda.set_device(local)
@@ -712,7 +712,7 @@ def run_qreduce(args):
         b, sec, _, threads, desc = qreduce_oracle_sample(wl, data.numpy(), scales.numpy(), args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(b / sec / 1e9, 4), "unit": "GB/s", "cores": threads,
                                 "kind": "oracle", "sample": desc, "seconds": round(sec, 2)}
-    print(json.dumps(line), flush=True)
+    emit(line)
     barrier(world)
 
 
@@ -777,7 +777,7 @@ def run_layer(args):
         barrier(world)
         return
     pk, pk_kind = peaks()
-    print(json.dumps({
+    emit({
         "metric": METRIC + " (with the AlltoAllv in the step)", "value": round(tflops, 2), "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt_max * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
@@ -795,7 +795,7 @@ def run_layer(args):
         "e2e": None,
         "gpu_launches": launches * args.steps,
         "clocks": clocks.summary(),
-    }), flush=True)
+    })
     barrier(world)
 
 
@@ -861,7 +861,7 @@ def run_mx(args):
             tot_f += f
             tot_s += sec
         tf = tot_f / tot_s / 1e12
-        print(json.dumps({
+        emit({
             "impl": "reference", "metric": MX_METRIC, "value": round(tf, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s * 1e3 / max(1, args.steps), 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -869,7 +869,7 @@ def run_mx(args):
             "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-            "gpu_launches": 0}), flush=True)
+            "gpu_launches": 0})
         return
     assert torch.cuda.is_available(), "bench.py needs a GPU (use --impl reference for the CPU oracle)"
     torch.cuda.set_device(local)
@@ -1007,13 +1007,33 @@ def run_mx(args):
         f, sec, _, threads, desc = mx_oracle_sample(wl, inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(f / sec / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
                                 "kind": "oracle", "sample": desc, "seconds": round(sec, 2)}
-    print(json.dumps(line), flush=True)
+    emit(line)
     barrier(world)
 
 
+# The process's standard output as opened at start: it carries exactly one
+# JSON line.  main() points file descriptor 1 at stderr, so that whatever a
+# library prints there (NCCL's version banner, for one) stays off it.
+_JSON_OUT = None
+
+
+def emit(obj):
+    out = _JSON_OUT if _JSON_OUT is not None else sys.stdout
+    out.write(json.dumps(obj) + "\n")
+    out.flush()
+
+
+def claim_stdout():
+    """Keep the process's stdout for emit() and point file descriptor 1 at stderr."""
+    global _JSON_OUT
+    if _JSON_OUT is None:
+        sys.stdout.flush()
+        _JSON_OUT = os.fdopen(os.dup(1), "w")
+        os.dup2(2, 1)
+
+
 def main(argv=None):
-    # NCCL may print its version banner on stdout when a process group starts
-    # (depending on NCCL_DEBUG); stdout carries exactly one JSON line.
+    claim_stdout()
     os.environ.setdefault("NCCL_DEBUG_FILE", "/dev/stderr")
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
