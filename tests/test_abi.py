@@ -189,10 +189,19 @@ def test_mx_phase1_validation(lib, kw, status):
 
 
 def test_mx_workspace_sizes(lib):
+    # Status word, staged codes (without permuteOut), then 512-byte scale
+    # atoms, one per 128-row (or 128-column) block and per 128 codes of K:
+    # routed A (an upper bound of ceil(A/128) + e halves), mmX, gmmWeight and
+    # mmWeight; each part padded to 256 bytes.
+    def atoms(blocks, K):
+        return blocks * (K // 128) * 512
+    routed = atoms(-(-1000 // 128) + 4, 512) + atoms(4 * (1024 // 128), 512)  # A = 1000, e = 4, N1 = 1024
+    shared = atoms(2048 // 128, 4096) + atoms(1024 // 128, 4096)              # BS = 2048, N2 = 1024
     st, n = mx_ws(A=1000, H1=512)
-    assert st == 0 and n == 256 + 512000 + 16128  # status + codes + scales, each padded to 256 B
-    assert mx_ws(A=1000, H1=512, want_permute_out=1)[1] == 256
-    assert mx_ws(A=0)[1] == 256
+    assert st == 0 and n == 256 + 512000 + routed + shared
+    assert mx_ws(A=1000, H1=512, want_permute_out=1)[1] == 256 + routed + shared
+    assert mx_ws(A=0)[1] == 256 + shared
+    assert mx_ws(A=0, BS=0)[1] == 256
 
 
 def test_status_strings(lib):

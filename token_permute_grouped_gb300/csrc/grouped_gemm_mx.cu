@@ -8,29 +8,31 @@
 // apply the scales themselves (tcgen05.mma kind::mxf8f6f4 with block_scale):
 // an MMA of K = 32 takes one E8M0 scale per A row and per B column from TMEM.
 //
-// Tiles: 128 rows x 128 columns per CTA (cta_group::1); K in stages of 256
-// codes: two 128-byte swizzle rows per operand row (two 16 KB sub-tiles),
-// eight MMAs.  Per CTA:
-//   warp 0     one thread issues a stage's TMA loads: 128 expert-major A rows
-//              (staged by the permute kernel) and 128 K-major weight columns,
-//              one 4-D load of both sub-tiles per operand.
-//   warp 1     one thread issues the MMAs.
-//   warps 2-5  scales: lane l loads the E8M0 scales of the tile rows and
-//              columns 32c + l, 8 bytes per row per stage (one stage ahead),
-//              and writes each stage's two 32-bit words per row (byte i of
-//              word j for MMA 4j + i) into TMEM with tcgen05.st: per word, 32
-//              lanes x (rows / 32) columns, the layout the MMA reads, in the
-//              warp's own lane quarter (each quarter holds a copy).
-//   warps 6-13 epilogue, two warps per TMEM lane quarter, each draining half
+// Tiles: 128 rows x 128 columns per CTA (cta_group::1), or 256 x 256 on a
+// CTA pair (cta_group::2); K in stages of 256 codes: two 128-byte swizzle
+// rows per operand row (two 16 KB sub-tiles), eight MMAs.  Per CTA:
+//   warp 0     one thread issues a stage's TMA loads: the A rows (read in
+//              place from ataOut, or from the permute kernel's staging copy),
+//              the K-major weight columns, one 4-D load of both sub-tiles per
+//              operand, and the stage's scale atoms (below).
+//   warp 1     one thread copies the stage's scale atoms from shared memory
+//              into TMEM (tcgen05.cp .32x128b.warpx4) and issues the MMAs;
+//              copies and MMAs run in issue order on the tensor core.
+//   warps 2-9  epilogue, two warps per TMEM lane quarter, each draining half
 //              of the columns: TMEM -> registers -> bf16 (nearest even) ->
 //              global, rows past the group's end and columns past N masked.
-//              The load of the next 32 columns overlaps the stores of the
-//              previous ones, and the accumulator is released as soon as the
-//              last load has landed.
-// TMEM: two 128-column fp32 accumulators (the epilogue of one tile overlaps
-// the main loop of the next), then per stage eight A-scale and eight B-scale
-// columns.  Every wait is bounded: on timeout the CTA sets kStatusTimeout and
-// winds down.
+//              A warp loads all its columns, releases the accumulator, and
+//              only then converts and stores them.
+// Scale atoms: the permute kernel rewrites every operand's E8M0 scales as
+// 512-byte atoms, one per 128-row (or 128-column) block and per 4 K blocks
+// of 32 codes: 32 rows of 16 bytes, row l holding the four scale bytes of
+// block rows l, 32 + l, 64 + l and 96 + l.  tcgen05.cp .32x128b.warpx4 turns
+// an atom into the layout the MMA reads: row 32c + l at lane l, column
+// base + c, the same in every lane quarter.
+// TMEM: the accumulators (single: two of 128 columns, so the epilogue of one
+// tile overlaps the main loop of the next; pair: one of 256), then per stage
+// eight A-scale and eight (single) or sixteen (pair) B-scale columns.  Every
+// wait is bounded: on timeout the CTA sets kStatusTimeout and winds down.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -54,12 +56,12 @@ constexpr int MX_CH = 2;         // K chunks per stage
 constexpr int MX_BK = MX_KCHUNK * MX_CH;
 constexpr int MX_STAGES = 3;
 constexpr int kMxEpiWarps = 8;  // two per TMEM lane quarter, each draining half of the columns
-constexpr int kMxScaleLoadWarp = 6 + kMxEpiWarps;  // issues the scale TMA loads
-constexpr int MX_THREADS = (7 + kMxEpiWarps) * 32;
-constexpr int MX_SC_SLOTS = 4;  // scale ring: each slot holds two stages' scales (16 bytes per row)
+constexpr int MX_THREADS = (2 + kMxEpiWarps) * 32;
 constexpr int kMxMmaWarp = 1;
-constexpr int kMxScaleWarp0 = 2;
-constexpr int kMxEpiWarp0 = 6;
+constexpr int kMxEpiWarp0 = 2;
+constexpr int MX_ATOM_ROWS = 128;     // rows (columns) of a block that one scale atom covers
+constexpr uint32_t MX_ATOM_BYTES = 512;  // 32 rows of 16 bytes
+constexpr int MX_QUAD = 128;          // codes along K per atom: four E8M0 blocks of 32
 constexpr uint32_t MX_SUB_BYTES = MX_BM * MX_KCHUNK;      // 16 KB: 128 rows x one chunk
 constexpr uint32_t MX_TILE_BYTES = MX_SUB_BYTES * MX_CH;  // one operand's stage; B is the same size
 constexpr uint32_t kMxTmemCols = 512;
@@ -82,6 +84,11 @@ struct MxShape {
     static constexpr uint32_t kSfaCols = 2 * 4;
     static constexpr uint32_t kSfbCols = 2 * (TILE_N / 32);
     static constexpr uint32_t kSfStride = kSfaCols + kSfbCols;
+    // Scale atoms of one stage in shared memory: A, two quads of this CTA's
+    // 128 rows; B, two quads of each 128-column block of the tile.
+    static constexpr uint32_t kSfaBytes = 2 * MX_ATOM_BYTES;
+    static constexpr uint32_t kSfbBytes = 2 * kCtas * MX_ATOM_BYTES;
+    static constexpr uint32_t kSfStageBytes = kSfaBytes + kSfbBytes;
 };
 
 template <bool PAIR>
@@ -111,18 +118,20 @@ struct MxLaunch {
     CUtensorMap tmB;   // weight codes [e, N1, H1]
     CUtensorMap tmX;   // mmX codes [BS, H2]
     CUtensorMap tmMW;  // mmWeight codes [N2, H2]
-    // E8M0 scale maps, 3-D {K/32 bytes, rows, groups}, box 16 bytes (two
-    // stages) x 128 rows (A) or x TILE_N rows (B) x 1, no swizzle.
-    CUtensorMap tmSA;   // expert-major scales [A, H1/32]
-    CUtensorMap tmSB;   // weight scales [e, N1, H1/32]
-    CUtensorMap tmSX;   // mmX scales [BS, H2/32]
-    CUtensorMap tmSMW;  // mmWeight scales [N2, H2/32]
+    // Scale atoms (written by the permute kernel), as 16-byte rows, no
+    // swizzle.  A: 2-D {16, atom rows}, atom (half, quad) at row
+    // 32 (half * quads + quad), box 16 x 64 (a stage's two quads).  B: 3-D
+    // {16, 32 column blocks, groups * quads}, atom (group, quad, block) at
+    // row 32 block of plane group * quads + quad, box 16 x 32 kCtas x 2.
+    CUtensorMap tmSFA;  // routed A: halves of the expert groups (128 rows from each group's start)
+    CUtensorMap tmSFX;  // mmX: halves of the BS rows
+    CUtensorMap tmSFB;  // gmmWeight: 128-column blocks of each expert
+    CUtensorMap tmSFW;  // mmWeight: 128-column blocks
     // Halves of a tile (this CTA's 128 rows) whose rows of the group lie in
     // one (source, expert) segment are read in place from ataOut; the permute
     // kernel staged only the others (see half_in_one_segment).
     int32_t direct_halves;
-    CUtensorMap tmA_direct;   // ataOut codes [A, H1]
-    CUtensorMap tmSA_direct;  // ataOut scales [A, H1/32]
+    CUtensorMap tmA_direct;  // ataOut codes [A, H1]
 };
 
 // Where this CTA's 128 A rows of a routed tile come from: in place from
@@ -141,14 +150,12 @@ struct MxGroup {
     int32_t rows;
     int32_t tiles_n;
     int32_t tile_start;
+    int32_t half0;  // routed: this group's first 128-row half among all groups' (its scale atoms)
 };
 
 struct MxControl {
-    uint64_t full[MX_STAGES];     // a stage's codes landed (pair: both CTAs'; in the even CTA)
-    uint64_t empty[MX_STAGES];    // the MMAs reading a stage (codes and scale columns) completed
-    uint64_t sf_full[MX_STAGES];  // the stage's scale words are in TMEM (scale warps; pair: of both CTAs)
-    uint64_t sc_full[MX_SC_SLOTS];   // a slot's scale rows (two stages) landed in this CTA
-    uint64_t sc_empty[MX_SC_SLOTS];  // the scale warps have read both stages of a slot
+    uint64_t full[MX_STAGES];   // a stage's codes and scale atoms landed (pair: both CTAs'; in the even CTA)
+    uint64_t empty[MX_STAGES];  // the copies and MMAs reading a stage completed
     uint64_t tfull[2];
     uint64_t tempty[2];           // epilogue drained the accumulator (pair: both CTAs; in the even CTA)
     uint32_t tmem_base;
@@ -158,15 +165,9 @@ struct MxControl {
     SegmentTable seg;
 };
 
-// A scale slot: 16 bytes (the two stages sharing a 16-byte chunk of each
-// scale row) for each of the CTA's 128 A rows and each of TILE_N columns.
-constexpr uint32_t MX_SA_BYTES = MX_BM * 16;
-template <bool PAIR>
-__host__ __device__ constexpr uint32_t mx_sb_bytes() { return MxShape<PAIR>::TILE_N * 16; }
 template <bool PAIR>
 constexpr size_t mx_smem_bytes() {
-    return 1024 + MX_STAGES * 2 * MX_TILE_BYTES + MX_SC_SLOTS * (MX_SA_BYTES + mx_sb_bytes<PAIR>()) +
-           sizeof(MxControl);
+    return 1024 + MX_STAGES * (2 * MX_TILE_BYTES + MxShape<PAIR>::kSfStageBytes) + sizeof(MxControl);
 }
 static_assert(mx_smem_bytes<true>() <= 232448, "shared memory per CTA");
 
@@ -295,18 +296,32 @@ __device__ __forceinline__ void mx_arrive_leader(uint32_t own_addr, uint32_t ran
         mbar_arrive(own_addr);
 }
 
-// Thread i of the warp writes N consecutive 32-bit words to lane (quarter
-// base + i), columns [col, col + N).
-__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t *v) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-                 : "memory");
+// Copy of one scale atom (32 rows of 16 bytes in shared memory, no swizzle:
+// 8-row core matrices 128 bytes apart) into TMEM columns [col, col + 4) of
+// lanes 0-31, replicated into every lane quarter (.warpx4).  Pair: the same
+// offsets in both CTAs, each from its own shared memory into its own TMEM.
+template <bool PAIR>
+__device__ __forceinline__ void mx_sf_copy(uint32_t taddr, uint32_t smem_addr) {
+    const uint64_t desc = smem_desc(smem_addr, 128, 128, 0);
+    if constexpr (PAIR)
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void ld_shared_v2(uint32_t addr, uint32_t &a, uint32_t &b) {
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr) : "memory");
+// TMA 3-D load; PAIR: the barrier is the even CTA's (cta_group::2).
+template <bool PAIR>
+__device__ __forceinline__ void tma_load_3d_mx(uint32_t dst, const void *tmap, uint32_t bar, int32_t x, int32_t y,
+                                               int32_t z) {
+    if constexpr (PAIR) {
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z)
+            : "memory");
+    } else {
+        tma_load_3d(dst, tmap, bar, x, y, z);
+    }
 }
 
 // TMA 4-D load; PAIR: the barrier is the even CTA's (cta_group::2).
@@ -368,11 +383,9 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
     uint8_t *base_ptr = smem_raw + (base - raw);
     const uint32_t a_smem = base;
     const uint32_t b_smem = base + MX_STAGES * MX_TILE_BYTES;
-    constexpr uint32_t SB_BYTES = mx_sb_bytes<PAIR>();
-    const uint32_t sa_smem = base + 2 * MX_STAGES * MX_TILE_BYTES;
-    const uint32_t sb_smem = sa_smem + MX_SC_SLOTS * MX_SA_BYTES;
+    const uint32_t sf_smem = base + 2 * MX_STAGES * MX_TILE_BYTES;  // per stage: A atoms, then B atoms
     MxControl &C = *reinterpret_cast<MxControl *>(base_ptr + 2 * MX_STAGES * MX_TILE_BYTES +
-                                                  MX_SC_SLOTS * (MX_SA_BYTES + SB_BYTES));
+                                                  MX_STAGES * S::kSfStageBytes);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -385,29 +398,34 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
     if (warp == 0) {
         const bool good = build_segment_table(p.recvCounts, p.W, e, p.A, C.seg, lane);
         const int tn1 = (p.N1 + TILE_N - 1) / TILE_N;
-        int row0 = 0, rows = 0, tiles = 0;
+        int row0 = 0, rows = 0, tiles = 0, halves = 0;
         if (lane < e) {
             row0 = C.seg.dst[lane * p.W];
             rows = C.seg.dst[(lane + 1) * p.W] - row0;
             tiles = good ? ((rows + TILE_M - 1) / TILE_M) * tn1 : 0;
+            halves = (rows + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS;
         }
-        int inc = tiles;
+        int inc = tiles, hinc = halves;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int v = __shfl_up_sync(0xffffffffu, inc, off);
-            if (lane >= off) inc += v;
+            const int hv = __shfl_up_sync(0xffffffffu, hinc, off);
+            if (lane >= off) {
+                inc += v;
+                hinc += hv;
+            }
         }
-        if (lane < e) C.g[lane] = MxGroup{row0, rows, tn1, inc - tiles};
+        if (lane < e) C.g[lane] = MxGroup{row0, rows, tn1, inc - tiles, hinc - halves};
         const int routed_total = __shfl_sync(0xffffffffu, inc, 31);
         if (lane == 0) {
             int ng = e, total = routed_total;
             if (p.BS > 0) {
                 const int tn2 = (p.N2 + TILE_N - 1) / TILE_N;
-                C.g[e] = MxGroup{0, p.BS, tn2, total};
+                C.g[e] = MxGroup{0, p.BS, tn2, total, 0};
                 total += good ? ((p.BS + TILE_M - 1) / TILE_M) * tn2 : 0;
                 ng = e + 1;
             }
-            C.g[ng] = MxGroup{0, 0, 1, total};
+            C.g[ng] = MxGroup{0, 0, 1, total, 0};
             C.total_tiles = total;
             C.abort = 0;
             if (blockIdx.x == 0) {
@@ -420,11 +438,6 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
             for (int s = 0; s < MX_STAGES; ++s) {
                 mbar_init(smem_u32(&C.full[s]), 1);
                 mbar_init(smem_u32(&C.empty[s]), 1);
-                mbar_init(smem_u32(&C.sf_full[s]), 4 * kCtas);
-            }
-            for (int c = 0; c < MX_SC_SLOTS; ++c) {
-                mbar_init(smem_u32(&C.sc_full[c]), 1);
-                mbar_init(smem_u32(&C.sc_empty[c]), 4);
             }
             for (int a = 0; a < 2; ++a) {
                 mbar_init(smem_u32(&C.tfull[a]), 1);
@@ -439,18 +452,15 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
             if (p.A > 0) {
                 prefetch_tensormap(&p.tmA);
                 prefetch_tensormap(&p.tmB);
-                prefetch_tensormap(&p.tmSA);
-                prefetch_tensormap(&p.tmSB);
-                if (p.direct_halves) {
-                    prefetch_tensormap(&p.tmA_direct);
-                    prefetch_tensormap(&p.tmSA_direct);
-                }
+                prefetch_tensormap(&p.tmSFA);
+                prefetch_tensormap(&p.tmSFB);
+                if (p.direct_halves) prefetch_tensormap(&p.tmA_direct);
             }
             if (p.BS > 0) {
                 prefetch_tensormap(&p.tmX);
                 prefetch_tensormap(&p.tmMW);
-                prefetch_tensormap(&p.tmSX);
-                prefetch_tensormap(&p.tmSMW);
+                prefetch_tensormap(&p.tmSFX);
+                prefetch_tensormap(&p.tmSFW);
             }
         }
     }
@@ -464,26 +474,30 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
     if (warp == 0) {
         // =========================================================== TMA producer
         if (lane == 0) {
+            // Every tile's scale atoms come from the permute kernel: wait for
+            // that grid before the first load.
+            if (p.after_permute) asm volatile("griddepcontrol.wait;" ::: "memory");
             uint32_t it = 0;
             bool ok = true;
-            bool staged_ready = !p.after_permute;  // the permute kernel's rows are visible
             for (int t = unit; t < total && ok; t += nunits) {
                 const MxTile w = mx_decode_tile(C, t);
                 const bool shared = w.g >= e;
                 const int K = shared ? p.H2 : p.H1;
+                const int nq = K / MX_QUAD;  // scale atoms per 128-row block
                 const CUtensorMap *ta = shared ? &p.tmX : &p.tmA;
                 const CUtensorMap *tb = shared ? &p.tmMW : &p.tmB;
+                const CUtensorMap *tsa = shared ? &p.tmSFX : &p.tmSFA;
+                const CUtensorMap *tsb = shared ? &p.tmSFW : &p.tmSFB;
                 int ya = C.g[w.g].row0 + w.m * TILE_M + static_cast<int>(rank) * MX_BM;
                 int32_t src = 0;
                 if (!shared && mx_direct_row(p, C.seg, C.g[w.g].row0, C.g[w.g].rows, ya, &src)) {
                     ta = &p.tmA_direct;
                     ya = src;
-                } else if (!shared && !staged_ready) {
-                    // This half reads staged rows: wait for the permute grid
-                    // (the tiles before needed none of its output).
-                    asm volatile("griddepcontrol.wait;" ::: "memory");
-                    staged_ready = true;
                 }
+                // This CTA's 128-row half: its atoms' first row; the tile's
+                // first 128-column block.
+                const int half = (shared ? 0 : C.g[w.g].half0) + w.m * kCtas + static_cast<int>(rank);
+                const int cb0 = w.n * kCtas;
                 const int xn = w.n * TILE_N + static_cast<int>(rank) * MX_BNC;
                 const int z = shared ? 0 : w.g;
                 for (int kb = 0; kb < K / MX_BK; ++kb, ++it) {
@@ -494,10 +508,16 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     }
                     const uint32_t fb_own = smem_u32(&C.full[s]);
                     const uint32_t fb = PAIR ? mx_map_to_rank(fb_own, 0) : fb_own;  // the MMA CTA's barrier
-                    if (rank == 0) mbar_arrive_expect_tx(fb_own, kCtas * 2 * MX_TILE_BYTES);
+                    if (rank == 0)
+                        mbar_arrive_expect_tx(fb_own, kCtas * (2 * MX_TILE_BYTES + S::kSfStageBytes));
                     // {chunk column, row, chunk, group}: both chunks of the stage.
                     tma_load_4d_mx<PAIR>(a_smem + s * MX_TILE_BYTES, ta, fb, 0, ya, kb * MX_CH, 0);
                     tma_load_4d_mx<PAIR>(b_smem + s * MX_TILE_BYTES, tb, fb, 0, xn, kb * MX_CH, z);
+                    // Scale atoms of quads 2kb and 2kb + 1: this half's, then
+                    // each of the tile's column blocks'.
+                    const uint32_t sf_st = sf_smem + s * S::kSfStageBytes;
+                    tma_load_3d_mx<PAIR>(sf_st, tsa, fb, 0, 32 * (half * nq + 2 * kb), 0);
+                    tma_load_3d_mx<PAIR>(sf_st + S::kSfaBytes, tsb, fb, 0, 32 * cb0, z * nq + 2 * kb);
                 }
             }
             // Wait until the MMAs released every stage that was filled.
@@ -528,16 +548,30 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 for (int kb = 0; kb < K / MX_BK; ++kb, ++it) {
                     const int s = it % MX_STAGES;
                     const uint32_t par = (it / MX_STAGES) & 1;
-                    if (!mx_wait(&C.abort, &C.full[s], par, p.status) ||
-                        !mx_wait<PAIR>(&C.abort, &C.sf_full[s], par, p.status)) {
+                    // Codes and atoms arrive by TMA (async proxy), as the copies
+                    // and MMAs read them: the barrier phase orders the two.
+                    if (!mx_wait(&C.abort, &C.full[s], par, p.status)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after_sync();  // the scale words came by tcgen05.st from other threads
                     const uint64_t ad = a_desc0 + ((s * MX_TILE_BYTES) >> 4);
                     const uint64_t bd = b_desc0 + ((s * MX_TILE_BYTES) >> 4);
                     const uint32_t sfa = C.tmem_base + sfa_col<PAIR>(s);
                     const uint32_t sfb = C.tmem_base + sfb_col<PAIR>(s);
+                    // Scale word j (MMAs 4j .. 4j + 3): A's atom to 4 columns;
+                    // B's atom of column block i to columns 4i .. 4i + 3 of
+                    // the word's NB.  The TMEM columns of stage s are free:
+                    // this stage's smem was refilled only after the MMAs
+                    // that last read them completed.
+                    const uint32_t sf_st = sf_smem + s * S::kSfStageBytes;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        mx_sf_copy<PAIR>(sfa + 4 * j, sf_st + j * MX_ATOM_BYTES);
+#pragma unroll
+                        for (int i = 0; i < kCtas; ++i)
+                            mx_sf_copy<PAIR>(sfb + NB * j + 4 * i,
+                                             sf_st + S::kSfaBytes + (j * kCtas + i) * MX_ATOM_BYTES);
+                    }
 #pragma unroll
                     for (int kk = 0; kk < MX_BK / 32; ++kk) {
                         const uint32_t off = ((kk >> 2) * MX_SUB_BYTES + (kk & 3) * 32) >> 4;
@@ -549,108 +583,6 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 }
                 if (ok) mx_commit<PAIR>(smem_u32(&C.tfull[acc]));
             }
-        }
-    } else if (warp >= kMxScaleWarp0 && warp < kMxEpiWarp0) {
-        // =========================================================== scale writers
-        // The MMA reads a K block's scale bytes for 128 rows (columns) as 32
-        // lanes x 4 columns: row 32c + l at lane l, column base + c, and each
-        // 32-lane quarter of TMEM holds the same copy.  A warp reaches only
-        // its own quarter, so every scale warp writes the whole set: A for
-        // this CTA's 128 rows, B for all TILE_N columns of the tile.
-        const int q = warp & 3;
-        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        uint32_t it = 0;
-        bool ok = true;
-        for (int t = unit; t < total && ok; t += nunits) {
-            const MxTile w = mx_decode_tile(C, t);
-            const bool shared = w.g >= e;
-            const int K = shared ? p.H2 : p.H1;
-            const int kblocks = K / MX_BK;
-            for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                const int s = it % MX_STAGES;
-                bool free_slot = true;
-                if (lane == 0) free_slot = mx_wait(&C.abort, &C.empty[s], ((it / MX_STAGES) & 1) ^ 1, p.status);
-                if (!__shfl_sync(0xffffffffu, free_slot, 0)) {
-                    ok = false;
-                    break;
-                }
-                // Scale slot of this stage: stages 2i and 2i + 1 (tiles have an
-                // even number of stages) share slot i % MX_SC_SLOTS.
-                const uint32_t chunk = it >> 1;
-                const int slot = chunk % MX_SC_SLOTS;
-                if ((it & 1) == 0) {
-                    if (lane == 0)
-                        free_slot = mx_wait(&C.abort, &C.sc_full[slot], (chunk / MX_SC_SLOTS) & 1, p.status);
-                    if (!__shfl_sync(0xffffffffu, free_slot, 0)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                tc_fence_after_sync();
-                // Staged scale row r is 16 bytes at 16 r; this stage's two words
-                // are its half (it & 1).  Word j for row (column) 32c + lane goes
-                // to column (columns per word) * j + c.
-                uint32_t wa[8], wb[2 * NB];
-                const uint32_t half = (it & 1) * 8 + static_cast<uint32_t>(lane) * 16;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    ld_shared_v2(sa_smem + slot * MX_SA_BYTES + c * 512 + half, wa[c], wa[4 + c]);
-#pragma unroll
-                for (int c = 0; c < NB; ++c)
-                    ld_shared_v2(sb_smem + slot * SB_BYTES + c * 512 + half, wb[c], wb[NB + c]);
-                if (it & 1) {  // both stages of the slot read: free it for the loader
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&C.sc_empty[slot]));
-                }
-                tmem_st_x8(C.tmem_base + lane_base + sfa_col<PAIR>(s), wa);
-#pragma unroll
-                for (int h = 0; h < 2 * NB; h += 8) tmem_st_x8(C.tmem_base + lane_base + sfb_col<PAIR>(s) + h, wb + h);
-                tmem_st_wait();
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mx_arrive_leader<PAIR>(smem_u32(&C.sf_full[s]), rank);
-            }
-        }
-    } else if (warp == kMxScaleLoadWarp) {
-        // =========================================================== scale loader
-        // Walks the same stages two at a time and keeps the scale ring full,
-        // up to MX_SC_SLOTS slots ahead of the scale writers.
-        if (lane == 0) {
-            uint32_t chunk = 0;
-            bool ok = true;
-            bool staged_ready = !p.after_permute;
-            for (int t = unit; t < total && ok; t += nunits) {
-                const MxTile w = mx_decode_tile(C, t);
-                const bool shared = w.g >= e;
-                const int K = shared ? p.H2 : p.H1;
-                const CUtensorMap *tsa = shared ? &p.tmSX : &p.tmSA;
-                const CUtensorMap *tsb = shared ? &p.tmSMW : &p.tmSB;
-                int ya = C.g[w.g].row0 + w.m * TILE_M + static_cast<int>(rank) * MX_BM;
-                int32_t src = 0;
-                if (!shared && mx_direct_row(p, C.seg, C.g[w.g].row0, C.g[w.g].rows, ya, &src)) {
-                    tsa = &p.tmSA_direct;
-                    ya = src;
-                } else if (!shared && !staged_ready) {
-                    asm volatile("griddepcontrol.wait;" ::: "memory");
-                    staged_ready = true;
-                }
-                const int z = shared ? 0 : w.g;
-                for (int kb = 0; kb < K / MX_BK; kb += 2, ++chunk) {
-                    const int slot = chunk % MX_SC_SLOTS;
-                    if (!mx_wait(&C.abort, &C.sc_empty[slot], ((chunk / MX_SC_SLOTS) & 1) ^ 1, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t lb = smem_u32(&C.sc_full[slot]);
-                    mbar_arrive_expect_tx(lb, MX_SA_BYTES + SB_BYTES);
-                    // The 16-byte chunk of each scale row holding stages kb and kb + 1.
-                    tma_load_3d(sa_smem + slot * MX_SA_BYTES, tsa, lb, (kb >> 1) * 16, ya, 0);
-                    tma_load_3d(sb_smem + slot * SB_BYTES, tsb, lb, (kb >> 1) * 16, w.n * TILE_N, z);
-                }
-            }
-            // Wait until the scale writers have read every slot that was filled.
-            for (int i = 0; i < MX_SC_SLOTS && ok; ++i, ++chunk)
-                ok = mx_wait(&C.abort, &C.sc_empty[chunk % MX_SC_SLOTS], ((chunk / MX_SC_SLOTS) & 1) ^ 1, p.status);
         }
     } else {
         // =========================================================== epilogue
@@ -673,24 +605,25 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
             const size_t out_row = static_cast<size_t>(shared ? row : C.g[w.g].row0 + row);
             uint16_t *out = static_cast<uint16_t *>(shared ? p.mmY : p.gmmY) + out_row * N + n0;
             const uint32_t t_base = C.tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::kAccCols;
-            uint32_t v[2][32];
-            tmem_ld_32x32b_x32(t_base + c0 * 32, v[0]);
+            // All of this warp's columns come out of TMEM first (the loads are
+            // asynchronous, one wait for all), then the accumulator is
+            // released, and only then converted and stored: with one
+            // accumulator (pair tiles) the next tile's MMAs wait for this.
+            uint32_t v[kChunks][32];
 #pragma unroll
-            for (int i = 0; i < kChunks; ++i) {
-                tmem_ld_wait();
-                if (i + 1 < kChunks) {
-                    tmem_ld_32x32b_x32(t_base + (c0 + i + 1) * 32, v[(i + 1) & 1]);
-                } else {  // every load of this tile has landed: release the accumulator
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mx_arrive_leader<PAIR>(smem_u32(&C.tempty[acc]), rank);
-                }
-                if (valid) {
+            for (int i = 0; i < kChunks; ++i) tmem_ld_32x32b_x32(t_base + (c0 + i) * 32, v[i]);
+            tmem_ld_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mx_arrive_leader<PAIR>(smem_u32(&C.tempty[acc]), rank);
+            if (valid) {
+#pragma unroll
+                for (int i = 0; i < kChunks; ++i) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int col = (c0 + i) * 32 + j * 8;
                         if (n0 + col < N) {
-                            const uint32_t *r = v[i & 1] + j * 8;
+                            const uint32_t *r = v[i] + j * 8;
                             uint4 pk;
                             pk.x = pack_bf16(r[0], r[1]);
                             pk.y = pack_bf16(r[2], r[3]);
@@ -713,14 +646,32 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
     }
 }
 
-// ---------------------------------------------------------------- permute
+// ---------------------------------------------------------------- permute and scale atoms
 //
-// The Permute step for mx operands: the expert-major copy of each row's H1
-// code bytes and H1/32 scale bytes, one warp per row with one segment lookup
-// for both, 16-byte vectors.  only_straddling: only rows of 128-row halves
-// that straddle a segment boundary (the GEMM reads the others in place).
+// One kernel before the GEMM.  Its warps first do the Permute step for mx
+// operands: the expert-major copy of rows' H1 code bytes (and, into
+// permuteOut, their H1/32 scale bytes), in 2 KB pieces per warp.  Without
+// permuteOut only rows of 128-row halves that straddle a segment boundary are
+// copied (the GEMM reads the others in place).  Then its threads write every
+// operand's scale atoms (see the top of this file), one 16-byte atom row at a
+// time.
 constexpr int kMxPermThreads = 256;
 constexpr int kPieceVecs = 4;  // 16-byte vectors per lane in one work item (2 KB per warp)
+
+struct MxPrep {
+    const int32_t *recvCounts;
+    int32_t W, e, A, H1, N1, BS, H2, N2;
+    const uint4 *src_q;    // ataOut codes [A, H1]
+    const uint8_t *src_s;  // ataOut scales [A, H1/32]
+    uint4 *dst_q;          // expert-major codes: permuteOut or the staging copy
+    uint4 *dst_s;          // expert-major scales: permuteOut, or null
+    int32_t *status;
+    int32_t only_straddling;
+    const uint8_t *w_s;   // gmmWeight scales [e, N1, H1/32]
+    const uint8_t *x_s;   // mmX scales [BS, H2/32]
+    const uint8_t *mw_s;  // mmWeight scales [N2, H2/32]
+    uint8_t *sfa, *sfx, *sfb, *sfw;  // atoms: routed A halves, mmX halves, gmmWeight and mmWeight blocks
+};
 
 __device__ __forceinline__ uint4 mx_ld_stream(const uint4 *ptr) {
     uint4 v;
@@ -730,77 +681,155 @@ __device__ __forceinline__ uint4 mx_ld_stream(const uint4 *ptr) {
     return v;
 }
 
-__global__ void __launch_bounds__(kMxPermThreads)
-    mx_permute_kernel(const int32_t *__restrict__ recvCounts, int W, int e, int A, int H1,
-                      const uint4 *__restrict__ src_q, const uint4 *__restrict__ src_s, uint4 *__restrict__ dst_q,
-                      uint4 *__restrict__ dst_s, int32_t *status, int only_straddling) {
+// Row l of an atom: the quad's four scale bytes (byte offset q4 in each scale
+// row) of block rows l, 32 + l, 64 + l, 96 + l; 127 (a scale of 1) for rows at
+// or past `valid`.  row(r) is the scale row of block row r.
+template <typename Row>
+__device__ __forceinline__ uint4 mx_atom_row(const Row &row, int valid, int l, int q4) {
+    uint32_t w[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int r = 32 * c + l;
+        w[c] = r < valid ? *reinterpret_cast<const uint32_t *>(row(r) + q4) : 0x7F7F7F7Fu;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__global__ void __launch_bounds__(kMxPermThreads) mx_prep_kernel(const __grid_constant__ MxPrep p) {
     __shared__ SegmentTable table;
     __shared__ StagedHalves halves;
+    __shared__ int32_t half0[kMaxExperts + 1];  // routed: first 128-row half of each expert group
     __shared__ int ok;
     // The GEMM launched after this kernel with programmatic dependent launch
-    // may start now: it waits for this grid's completion before it reads a
-    // row this kernel writes.
+    // may start now: it waits for this grid's completion before it reads
+    // anything this kernel writes.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int W = p.W, e = p.e, H1 = p.H1;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0) {
-        const bool good = build_segment_table(recvCounts, W, e, A, table, lane);
+        const bool good = build_segment_table(p.recvCounts, W, e, p.A, table, lane);
+        int nh = 0;
+        if (lane < e) nh = (table.dst[(lane + 1) * W] - table.dst[lane * W] + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS;
+        int inc = nh;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += v;
+        }
+        if (lane < e) half0[lane] = inc - nh;
+        const int all = __shfl_sync(0xffffffffu, inc, 31);
         if (lane == 0) {
+            half0[e] = all;
             ok = good;
-            if (blockIdx.x == 0) *status = good ? 0 : kStatusBadCounts;  // the first kernel of the call
+            if (blockIdx.x == 0) *p.status = good ? 0 : kStatusBadCounts;  // the first kernel of the call
         }
     }
     __syncthreads();
-    if (!ok) return;
-    // Work items are pieces of a code row (kPieceVecs 16-byte vectors per lane,
-    // all loaded before any is stored); the first piece of a row also moves
-    // its scale row.  One memory round trip per item.
-    const int vq = H1 / 16, vs = H1 / 512;  // 16-byte vectors per code row and per scale row
-    const int ppr = (vq + 32 * kPieceVecs - 1) / (32 * kPieceVecs);
-    const int nwarps = gridDim.x * (kMxPermThreads / 32);
-    const int gw = blockIdx.x * (kMxPermThreads / 32) + warp;
-    const auto copy_piece = [&](int d, int seg, int piece) {
-        const int v0 = piece * 32 * kPieceVecs + lane;
-        const size_t srow = static_cast<size_t>(source_row_in(table, W, e, seg, d));
-        const uint4 *in = src_q + srow * vq;
-        uint4 *out = dst_q + static_cast<size_t>(d) * vq;
-        uint4 r[kPieceVecs];
+
+    if (ok && p.dst_q != nullptr) {
+        // Work items are pieces of a code row (kPieceVecs 16-byte vectors per
+        // lane, all loaded before any is stored); the first piece of a row
+        // also moves its scale row when permuteOut wants it.  One memory round
+        // trip per item.
+        const int vq = H1 / 16, vs = H1 / 512;  // 16-byte vectors per code row and per scale row
+        const int ppr = (vq + 32 * kPieceVecs - 1) / (32 * kPieceVecs);
+        const int nwarps = gridDim.x * (kMxPermThreads / 32);
+        const int gw = blockIdx.x * (kMxPermThreads / 32) + warp;
+        const auto copy_piece = [&](int d, int seg, int piece) {
+            const int v0 = piece * 32 * kPieceVecs + lane;
+            const size_t srow = static_cast<size_t>(source_row_in(table, W, e, seg, d));
+            const uint4 *in = p.src_q + srow * vq;
+            uint4 *out = p.dst_q + static_cast<size_t>(d) * vq;
+            uint4 r[kPieceVecs];
 #pragma unroll
-        for (int k = 0; k < kPieceVecs; ++k)
-            if (v0 + 32 * k < vq) r[k] = mx_ld_stream(in + v0 + 32 * k);
+            for (int k = 0; k < kPieceVecs; ++k)
+                if (v0 + 32 * k < vq) r[k] = mx_ld_stream(in + v0 + 32 * k);
 #pragma unroll
-        for (int k = 0; k < kPieceVecs; ++k)
-            if (v0 + 32 * k < vq) out[v0 + 32 * k] = r[k];
-        if (piece == 0)
-            for (int u = lane; u < vs; u += 32)
-                dst_s[static_cast<size_t>(d) * vs + u] = mx_ld_stream(src_s + srow * vs + u);
-    };
-    int listed = -1;
-    if (only_straddling) {
-        list_staged_halves(table, W, e, halves);
-        listed = halves.n;
-    }
-    if (listed >= 0) {
-        // Only the rows of the halves the GEMM cannot read in place.
-        const int per_half = kHalfRows * ppr;
-        for (int i = gw; i < listed * per_half; i += nwarps) {
-            const int hi = i / per_half, rem = i - hi * per_half;
-            const int r = rem / ppr;
-            const int2 span = halves.span[hi];
-            const int d = span.x + r;
-            if (d < span.y) copy_piece(d, segment_of(table, W, e, d), rem - r * ppr);
-        }
-    } else {
-        const int64_t items = static_cast<int64_t>(A) * ppr;
-        for (int64_t i = gw; i < items; i += nwarps) {
-            const int d = static_cast<int>(i / ppr);
-            const int seg = segment_of(table, W, e, d);
-            if (only_straddling) {
-                // More staged halves than the list holds: test each row's half.
-                const int j = seg / W;
-                const int g0 = table.dst[j * W], g1 = table.dst[(j + 1) * W];
-                if (half_in_one_segment(table, W, e, g0 + (d - g0) / kHalfRows * kHalfRows, g1)) continue;
+            for (int k = 0; k < kPieceVecs; ++k)
+                if (v0 + 32 * k < vq) out[v0 + 32 * k] = r[k];
+            if (piece == 0 && p.dst_s != nullptr) {
+                const uint4 *ins = reinterpret_cast<const uint4 *>(p.src_s) + srow * vs;
+                for (int u = lane; u < vs; u += 32) p.dst_s[static_cast<size_t>(d) * vs + u] = mx_ld_stream(ins + u);
             }
-            copy_piece(d, seg, static_cast<int>(i - static_cast<int64_t>(d) * ppr));
+        };
+        int listed = -1;
+        if (p.only_straddling) {
+            list_staged_halves(table, W, e, halves);
+            listed = halves.n;
+        }
+        if (listed >= 0) {
+            // Only the rows of the halves the GEMM cannot read in place.
+            const int per_half = kHalfRows * ppr;
+            for (int i = gw; i < listed * per_half; i += nwarps) {
+                const int hi = i / per_half, rem = i - hi * per_half;
+                const int r = rem / ppr;
+                const int2 span = halves.span[hi];
+                const int d = span.x + r;
+                if (d < span.y) copy_piece(d, segment_of(table, W, e, d), rem - r * ppr);
+            }
+        } else {
+            const int64_t items = static_cast<int64_t>(p.A) * ppr;
+            for (int64_t i = gw; i < items; i += nwarps) {
+                const int d = static_cast<int>(i / ppr);
+                const int seg = segment_of(table, W, e, d);
+                if (p.only_straddling) {
+                    // More staged halves than the list holds: test each row's half.
+                    const int j = seg / W;
+                    const int g0 = table.dst[j * W], g1 = table.dst[(j + 1) * W];
+                    if (half_in_one_segment(table, W, e, g0 + (d - g0) / kHalfRows * kHalfRows, g1)) continue;
+                }
+                copy_piece(d, seg, static_cast<int>(i - static_cast<int64_t>(d) * ppr));
+            }
+        }
+    }
+
+    // ---- scale atoms: routed A (valid counts only), mmX, gmmWeight, mmWeight
+    const int nq1 = H1 / MX_QUAD, nq2 = p.H2 / MX_QUAD;
+    const int ncb1 = (p.N1 + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS, ncb2 = (p.N2 + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS;
+    const int64_t rows_a = (ok && p.A > 0) ? static_cast<int64_t>(half0[e]) * nq1 * 32 : 0;
+    const int64_t rows_x = p.BS > 0 ? static_cast<int64_t>((p.BS + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS) * nq2 * 32 : 0;
+    const int64_t rows_b = p.A > 0 ? static_cast<int64_t>(e) * nq1 * ncb1 * 32 : 0;
+    const int64_t rows_w = p.BS > 0 ? static_cast<int64_t>(nq2) * ncb2 * 32 : 0;
+    const int64_t all = rows_a + rows_x + rows_b + rows_w;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kMxPermThreads;
+    const size_t kb1 = static_cast<size_t>(H1 / 32), kb2 = static_cast<size_t>(p.H2 / 32);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kMxPermThreads + threadIdx.x; i < all; i += stride) {
+        const int l = static_cast<int>(i % 32);
+        if (i < rows_a) {
+            const int atom = static_cast<int>(i / 32);
+            const int h = atom / nq1, q = atom - h * nq1;
+            int g = 0;
+            while (h >= half0[g + 1]) ++g;  // the expert group holding half h
+            const int first = table.dst[g * W] + (h - half0[g]) * MX_ATOM_ROWS;
+            const int valid = min(MX_ATOM_ROWS, table.dst[(g + 1) * W] - first);
+            const auto row = [&](int r) { return p.src_s + static_cast<size_t>(source_row(table, W, e, first + r)) * kb1; };
+            reinterpret_cast<uint4 *>(p.sfa + static_cast<size_t>(atom) * MX_ATOM_BYTES)[l] =
+                mx_atom_row(row, valid, l, 4 * q);
+        } else if (i < rows_a + rows_x) {
+            const int atom = static_cast<int>((i - rows_a) / 32);
+            const int h = atom / nq2, q = atom - h * nq2;
+            const int first = h * MX_ATOM_ROWS;
+            const auto row = [&](int r) { return p.x_s + static_cast<size_t>(first + r) * kb2; };
+            reinterpret_cast<uint4 *>(p.sfx + static_cast<size_t>(atom) * MX_ATOM_BYTES)[l] =
+                mx_atom_row(row, min(MX_ATOM_ROWS, p.BS - first), l, 4 * q);
+        } else if (i < rows_a + rows_x + rows_b) {
+            // Atom (z, q, cb) of gmmWeight: plane z * nq1 + q, block cb.
+            const int atom = static_cast<int>((i - rows_a - rows_x) / 32);
+            const int cb = atom % ncb1, plane = atom / ncb1;
+            const int z = plane / nq1, q = plane - z * nq1;
+            const int first = cb * MX_ATOM_ROWS;
+            const auto row = [&](int r) {
+                return p.w_s + (static_cast<size_t>(z) * p.N1 + static_cast<size_t>(first + r)) * kb1;
+            };
+            reinterpret_cast<uint4 *>(p.sfb + static_cast<size_t>(atom) * MX_ATOM_BYTES)[l] =
+                mx_atom_row(row, min(MX_ATOM_ROWS, p.N1 - first), l, 4 * q);
+        } else {
+            const int atom = static_cast<int>((i - rows_a - rows_x - rows_b) / 32);
+            const int cb = atom % ncb2, q = atom / ncb2;
+            const int first = cb * MX_ATOM_ROWS;
+            const auto row = [&](int r) { return p.mw_s + static_cast<size_t>(first + r) * kb2; };
+            reinterpret_cast<uint4 *>(p.sfw + static_cast<size_t>(atom) * MX_ATOM_BYTES)[l] =
+                mx_atom_row(row, min(MX_ATOM_ROWS, p.N2 - first), l, 4 * q);
         }
     }
 }
@@ -826,9 +855,34 @@ a2av_status mx_validate(const a2av_gmm_mx_desc *d) {
     return A2AV_OK;
 }
 
-size_t mx_staging_bytes(const a2av_gmm_mx_desc *d) {
-    if (d->want_permute_out || d->A == 0) return 0;
-    return align256(static_cast<size_t>(d->A) * d->H1) + align256(static_cast<size_t>(d->A) * d->H1 / 32);
+// Workspace after the status word: the staging copy of A's codes (without
+// permuteOut), then the scale atoms of routed A (one per 128-row half of each
+// expert group and quad of K), of mmX, of gmmWeight and of mmWeight.
+struct MxWorkspace {
+    size_t staging, sfa, sfx, sfb, sfw, total;
+    int64_t sfa_rows;  // 16-byte rows of the routed-A atom buffer (an upper bound on the halves used)
+};
+
+MxWorkspace mx_workspace_layout(const a2av_gmm_mx_desc *d) {
+    MxWorkspace w{};
+    const int64_t A = d->A, BS = d->BS;
+    const int64_t nq1 = d->H1 / MX_QUAD, nq2 = BS > 0 ? d->H2 / MX_QUAD : 0;
+    const int64_t ncb1 = (d->N1 + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS;
+    const int64_t ncb2 = BS > 0 ? (d->N2 + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS : 0;
+    size_t off = kMxStatusBytes;
+    w.staging = off;
+    if (!d->want_permute_out && A > 0) off += align256(static_cast<size_t>(A) * d->H1);
+    w.sfa = off;
+    w.sfa_rows = A > 0 ? ((A + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS + d->e) * nq1 * 32 : 0;
+    off += align256(static_cast<size_t>(w.sfa_rows) * 16);
+    w.sfx = off;
+    if (BS > 0) off += align256(static_cast<size_t>((BS + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS) * nq2 * MX_ATOM_BYTES);
+    w.sfb = off;
+    if (A > 0) off += align256(static_cast<size_t>(d->e) * nq1 * ncb1 * MX_ATOM_BYTES);
+    w.sfw = off;
+    if (BS > 0) off += align256(static_cast<size_t>(nq2) * ncb2 * MX_ATOM_BYTES);
+    w.total = off;
+    return w;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 mx_encode_fn() {
@@ -861,15 +915,15 @@ bool mx_codes_map(CUtensorMap *m, const void *ptr, int64_t groups, int64_t rows,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// E8M0 scales [groups][rows][K/32 bytes] as 3-D {K/32, rows, groups}; box
-// 16 bytes x box_rows x 1, no swizzle (row strides are multiples of 16 B).
-bool mx_scales_map(CUtensorMap *m, const void *ptr, int64_t groups, int64_t rows, int64_t K, uint32_t box_rows) {
+// Scale atoms as 16-byte rows: 3-D {16, rows, planes}, box 16 x box_rows x
+// box_planes, no swizzle; out-of-range rows load as zeros.
+bool mx_atoms_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t planes, uint32_t box_rows,
+                  uint32_t box_planes) {
     auto fn = mx_encode_fn();
     if (!fn) return false;
-    const int64_t kb = K / 32;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kb), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(groups)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kb), static_cast<cuuint64_t>(kb * rows)};
-    cuuint32_t box[3] = {16, box_rows, 1};
+    cuuint64_t dims[3] = {16, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(planes)};
+    cuuint64_t strides[2] = {16, static_cast<cuuint64_t>(rows * 16)};
+    cuuint32_t box[3] = {16, box_rows, box_planes};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -895,7 +949,7 @@ a2av_status a2av_gmm_mx_workspace_size(const a2av_gmm_mx_desc *desc, size_t *byt
     if (!desc || !bytes) return A2AV_ERR_NULLPTR;
     const a2av_status s = a2av::mx_validate(desc);
     if (s != A2AV_OK) return s;
-    *bytes = a2av::kMxStatusBytes + a2av::mx_staging_bytes(desc);
+    *bytes = a2av::mx_workspace_layout(desc).total;
     return A2AV_OK;
 }
 
@@ -944,46 +998,78 @@ a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, 
     g.status = status;
     g.qtype = d.qtype;
     const bool pair = d.tiles != A2AV_TILES_SINGLE;
-    const uint32_t tile_n = pair ? 2 * MX_BNC : MX_BNC;
+    const uint32_t ctas = pair ? 2 : 1;
+    const MxWorkspace ws = mx_workspace_layout(&d);
+    uint8_t *wsb = static_cast<uint8_t *>(workspace);
+    const int64_t nq1 = d.H1 / MX_QUAD, ncb1 = (d.N1 + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS;
     if (!mx_codes_map(&g.tmB, gmmWeight_q, d.e, d.N1, d.H1)) return A2AV_ERR_CUDA;
-    if (!mx_scales_map(&g.tmSB, gmmWeight_s, d.e, d.N1, d.H1, tile_n)) return A2AV_ERR_CUDA;
+    if (routed) {
+        // Atoms as 16-byte rows: routed A, 2-D in effect (one plane), a
+        // stage's two quads per load; gmmWeight, plane z * nq1 + quad, the
+        // tile's column blocks and two quads per load.
+        if (!mx_atoms_map(&g.tmSFA, wsb + ws.sfa, ws.sfa_rows, 1, 64, 1)) return A2AV_ERR_CUDA;
+        if (!mx_atoms_map(&g.tmSFB, wsb + ws.sfb, ncb1 * 32, d.e * nq1, 32 * ctas, 2)) return A2AV_ERR_CUDA;
+    }
     if (shared) {
+        const int64_t nq2 = d.H2 / MX_QUAD, ncb2 = (d.N2 + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS;
+        const int64_t nh2 = (d.BS + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS;
         if (!mx_codes_map(&g.tmX, mmX_q, 1, d.BS, d.H2)) return A2AV_ERR_CUDA;
         if (!mx_codes_map(&g.tmMW, mmWeight_q, 1, d.N2, d.H2)) return A2AV_ERR_CUDA;
-        if (!mx_scales_map(&g.tmSX, mmX_s, 1, d.BS, d.H2, MX_BM)) return A2AV_ERR_CUDA;
-        if (!mx_scales_map(&g.tmSMW, mmWeight_s, 1, d.N2, d.H2, tile_n)) return A2AV_ERR_CUDA;
+        if (!mx_atoms_map(&g.tmSFX, wsb + ws.sfx, nh2 * nq2 * 32, 1, 64, 1)) return A2AV_ERR_CUDA;
+        if (!mx_atoms_map(&g.tmSFW, wsb + ws.sfw, ncb2 * 32, nq2, 32 * ctas, 2)) return A2AV_ERR_CUDA;
     }
-    bool permute_ran = false;
+    // The prep kernel: expert-major codes (into permuteOut, or only the
+    // halves that straddle a segment boundary into the staging copy), and
+    // every operand's scale atoms.
+    MxPrep pp;
+    std::memset(&pp, 0, sizeof pp);
+    pp.recvCounts = recvCounts;
+    pp.W = d.W;
+    pp.e = d.e;
+    pp.A = static_cast<int32_t>(d.A);
+    pp.H1 = static_cast<int32_t>(d.H1);
+    pp.N1 = static_cast<int32_t>(d.N1);
+    pp.BS = g.BS;
+    pp.H2 = g.H2;
+    pp.N2 = g.N2;
+    pp.status = status;
+    pp.src_q = static_cast<const uint4 *>(ataOut_q);
+    pp.src_s = static_cast<const uint8_t *>(ataOut_s);
+    pp.w_s = static_cast<const uint8_t *>(gmmWeight_s);
+    pp.x_s = static_cast<const uint8_t *>(mmX_s);
+    pp.mw_s = static_cast<const uint8_t *>(mmWeight_s);
+    pp.sfa = wsb + ws.sfa;
+    pp.sfx = wsb + ws.sfx;
+    pp.sfb = wsb + ws.sfb;
+    pp.sfw = wsb + ws.sfw;
     if (routed) {
-        // Expert-major codes and scales: into permuteOut, or into the staging area.
         uint8_t *dq = static_cast<uint8_t *>(permuteOut_q);
-        uint8_t *ds = static_cast<uint8_t *>(permuteOut_s);
         if (!d.want_permute_out) {
-            dq = static_cast<uint8_t *>(workspace) + kMxStatusBytes;
-            ds = dq + align256(static_cast<size_t>(d.A) * d.H1);
-        }
-        // Without permuteOut only the 128-row halves that straddle a segment
-        // boundary are staged; the GEMM reads the others from ataOut.
-        const int32_t partial = d.want_permute_out ? 0 : 1;
-        if (partial) {
+            dq = wsb + ws.staging;
+            // Only the 128-row halves that straddle a segment boundary are
+            // staged; the GEMM reads the others from ataOut.
             if (!mx_codes_map(&g.tmA_direct, ataOut_q, 1, d.A, d.H1)) return A2AV_ERR_CUDA;
-            if (!mx_scales_map(&g.tmSA_direct, ataOut_s, 1, d.A, d.H1, MX_BM)) return A2AV_ERR_CUDA;
             g.direct_halves = 1;
         }
-        const int64_t warps = kMxPermThreads / 32;
-        const int blocks = static_cast<int>(
-            std::max<int64_t>(1, std::min<int64_t>((d.A + warps - 1) / warps, static_cast<int64_t>(sms) * 8)));
-        mx_permute_kernel<<<blocks, kMxPermThreads, 0, stream>>>(
-            recvCounts, d.W, d.e, static_cast<int32_t>(d.A), static_cast<int32_t>(d.H1),
-            static_cast<const uint4 *>(ataOut_q), static_cast<const uint4 *>(ataOut_s), reinterpret_cast<uint4 *>(dq),
-            reinterpret_cast<uint4 *>(ds), status, partial);
-        if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
-        permute_ran = true;
+        pp.dst_q = reinterpret_cast<uint4 *>(dq);
+        pp.dst_s = d.want_permute_out ? static_cast<uint4 *>(permuteOut_s) : nullptr;
+        pp.only_straddling = d.want_permute_out ? 0 : 1;
         if (!mx_codes_map(&g.tmA, dq, 1, d.A, d.H1)) return A2AV_ERR_CUDA;
-        if (!mx_scales_map(&g.tmSA, ds, 1, d.A, d.H1, MX_BM)) return A2AV_ERR_CUDA;
     }
-    g.write_status = permute_ran ? 0 : 1;
-    g.after_permute = permute_ran ? 1 : 0;
+    bool prep_ran = false;
+    if (routed || shared) {
+        // Blocks for a warp per row of A, or a thread per atom row, at most
+        // eight per SM (all resident at once).
+        const int64_t atom_rows = ws.sfa_rows + static_cast<int64_t>(ws.total - ws.sfx) / 16;
+        const int64_t want = std::max<int64_t>((d.A + kMxPermThreads / 32 - 1) / (kMxPermThreads / 32),
+                                               (atom_rows + kMxPermThreads - 1) / kMxPermThreads);
+        const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * 8)));
+        mx_prep_kernel<<<blocks, kMxPermThreads, 0, stream>>>(pp);
+        if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+        prep_ran = true;
+    }
+    g.write_status = prep_ran ? 0 : 1;
+    g.after_permute = prep_ran ? 1 : 0;
 
     // Persistent grid: one CTA (pair: cluster of two) per SM (pair), never
     // more than there can be tiles.
@@ -1012,7 +1098,7 @@ a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, 
         attr[n_attr].val.clusterDim.z = 1;
         ++n_attr;
     }
-    if (permute_ran) {  // start beside the permute kernel; the loaders wait where they must
+    if (prep_ran) {  // start beside the prep kernel; the producer waits for it before its first load
         attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
         ++n_attr;
