@@ -118,6 +118,17 @@ def test_matches_oracle(orc, qtype, W, e, H1, N1, A, zero, BS, H2, N2, tiles):
         assert_close(m, ref_m, "mmY")
 
 
+@pytest.mark.parametrize("tiles", TILES)
+def test_shared_expert_only(orc, tiles):
+    # No routed rows (A = 0): the prep kernel writes only the shared expert's
+    # scale atoms and the GEMM runs only the shared tiles.
+    inp = _custom(4, 2, 512, 128, [0] * 8, "e4m3fn", BS=300, H2=1024, N2=200, seed=9)
+    (y, m, _, _), st = run_mx(inp, tiles=tiles)
+    assert st[0] == 0, st
+    _, _, _, ref_m = reference(orc, inp)
+    assert_close(m, ref_m, "mmY")
+
+
 def test_permute_out_bit_exact_and_same_products(orc):
     rc = random_counts(4, 2, 600, seed=5, zero_prob=0.25)
     inp = _custom(4, 2, 1024, 128, rc, "e4m3fn", seed=5)

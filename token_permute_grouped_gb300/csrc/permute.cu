@@ -88,7 +88,8 @@ __global__ void __launch_bounds__(kPermuteThreads)
             const int d = static_cast<int>(i / ppr);
             const int seg = segment_of(table, W, e, d);
             if (only_straddling) {
-                // More staged halves than the list holds: test each row's half.
+                // More staged halves than the list holds (not reached: see
+                // kMaxStagedHalves): test each row's half.
                 const int j = seg / W;
                 const int g0 = table.dst[j * W], g1 = table.dst[(j + 1) * W];
                 if (half_in_one_segment(table, W, e, g0 + (d - g0) / kHalfRows * kHalfRows, g1)) continue;

@@ -113,7 +113,9 @@ __device__ __forceinline__ bool half_in_one_segment(const SegmentTable &t, int W
 // The 128-row halves of the GEMM's routed tiles that do not lie in one
 // segment, which the GEMM reads from the staging copy: [first row, end row),
 // end the smaller of first + 128 and the group's end, in ascending order.
-constexpr int kMaxStagedHalves = 2048;
+// Such a half holds a segment boundary strictly inside it, and a boundary
+// lies in one half only, so there are fewer than W * e <= kMaxSegments.
+constexpr int kMaxStagedHalves = kMaxSegments;
 
 struct StagedHalves {
     int32_t n;  // halves listed, or -1 when there are more than kMaxStagedHalves
