@@ -281,13 +281,13 @@ __device__ __forceinline__ void mx_cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// An arrival on a barrier of the even CTA (own CTA when single).  The odd
-// CTA arrives through the barrier's cluster address with the default
-// (CTA-scope release) semantics: what it hands over is TMEM content, ordered
-// by tcgen05.wait::st and tcgen05.fence::before_thread_sync before the arrival
-// and by the reader's tcgen05.fence::after_thread_sync after its wait.  A
-// cluster-scope release arrival measured about 1400 cycles here, more than a
-// stage's MMAs, once per stage and scale warp.
+// An arrival on a barrier of the even CTA (own CTA when single): an epilogue
+// warp handing the accumulator back.  The odd CTA arrives through the
+// barrier's cluster address with the default (CTA-scope release) semantics:
+// what it hands over is TMEM, whose reads are ordered by tcgen05.wait::ld and
+// tcgen05.fence::before_thread_sync before the arrival and by the MMA
+// thread's tcgen05.fence::after_thread_sync after its wait.  A cluster-scope
+// release arrival measured about 1400 cycles in this kernel.
 template <bool PAIR>
 __device__ __forceinline__ void mx_arrive_leader(uint32_t own_addr, uint32_t rank) {
     if (PAIR && rank != 0)
