@@ -81,13 +81,14 @@ struct MxShape {
     static constexpr uint32_t kAccCols = TILE_N;
     // Scale words per stage: 2 (eight MMAs, four per word); each word is 32
     // lanes x (rows / 32) columns.  A: this CTA's 128 rows; B: all TILE_N columns.
-    static constexpr uint32_t kSfaCols = 2 * 4;
-    static constexpr uint32_t kSfbCols = 2 * (TILE_N / 32);
+    static constexpr uint32_t kSfaCols = MX_CH * 4;
+    static constexpr uint32_t kSfbCols = MX_CH * (TILE_N / 32);
     static constexpr uint32_t kSfStride = kSfaCols + kSfbCols;
-    // Scale atoms of one stage in shared memory: A, two quads of this CTA's
-    // 128 rows; B, two quads of each 128-column block of the tile.
-    static constexpr uint32_t kSfaBytes = 2 * MX_ATOM_BYTES;
-    static constexpr uint32_t kSfbBytes = 2 * kCtas * MX_ATOM_BYTES;
+    // Scale atoms of one stage in shared memory: A, the stage's MX_CH quads
+    // of this CTA's 128 rows; B, the same quads of each 128-column block of
+    // the tile.
+    static constexpr uint32_t kSfaBytes = MX_CH * MX_ATOM_BYTES;
+    static constexpr uint32_t kSfbBytes = MX_CH * kCtas * MX_ATOM_BYTES;
     static constexpr uint32_t kSfStageBytes = kSfaBytes + kSfbBytes;
 };
 
@@ -120,7 +121,7 @@ struct MxLaunch {
     CUtensorMap tmMW;  // mmWeight codes [N2, H2]
     // Scale atoms (written by the permute kernel), as 16-byte rows, no
     // swizzle.  A: 2-D {16, atom rows}, atom (half, quad) at row
-    // 32 (half * quads + quad), box 16 x 64 (a stage's two quads).  B: 3-D
+    // 32 (half * quads + quad), box 16 x 32 MX_CH (a stage's quads).  B: 3-D
     // {16, 32 column blocks, groups * quads}, atom (group, quad, block) at
     // row 32 block of plane group * quads + quad, box 16 x 32 kCtas x 2.
     CUtensorMap tmSFA;  // routed A: halves of the expert groups (128 rows from each group's start)
@@ -516,8 +517,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     // Scale atoms of quads 2kb and 2kb + 1: this half's, then
                     // each of the tile's column blocks'.
                     const uint32_t sf_st = sf_smem + s * S::kSfStageBytes;
-                    tma_load_3d_mx<PAIR>(sf_st, tsa, fb, 0, 32 * (half * nq + 2 * kb), 0);
-                    tma_load_3d_mx<PAIR>(sf_st + S::kSfaBytes, tsb, fb, 0, 32 * cb0, z * nq + 2 * kb);
+                    tma_load_3d_mx<PAIR>(sf_st, tsa, fb, 0, 32 * (half * nq + MX_CH * kb), 0);
+                    tma_load_3d_mx<PAIR>(sf_st + S::kSfaBytes, tsb, fb, 0, 32 * cb0, z * nq + MX_CH * kb);
                 }
             }
             // Wait until the MMAs released every stage that was filled.
@@ -565,7 +566,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     // that last read them completed.
                     const uint32_t sf_st = sf_smem + s * S::kSfStageBytes;
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
+                    for (int j = 0; j < MX_CH; ++j) {
                         mx_sf_copy<PAIR>(sfa + 4 * j, sf_st + j * MX_ATOM_BYTES);
 #pragma unroll
                         for (int i = 0; i < kCtas; ++i)
@@ -1006,18 +1007,18 @@ a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, 
     if (!mx_codes_map(&g.tmB, gmmWeight_q, d.e, d.N1, d.H1)) return A2AV_ERR_CUDA;
     if (routed) {
         // Atoms as 16-byte rows: routed A, 2-D in effect (one plane), a
-        // stage's two quads per load; gmmWeight, plane z * nq1 + quad, the
-        // tile's column blocks and two quads per load.
-        if (!mx_atoms_map(&g.tmSFA, wsb + ws.sfa, ws.sfa_rows, 1, 64, 1)) return A2AV_ERR_CUDA;
-        if (!mx_atoms_map(&g.tmSFB, wsb + ws.sfb, ncb1 * 32, d.e * nq1, 32 * ctas, 2)) return A2AV_ERR_CUDA;
+        // stage's MX_CH quads per load; gmmWeight, plane z * nq1 + quad, the
+        // tile's column blocks and the stage's quads per load.
+        if (!mx_atoms_map(&g.tmSFA, wsb + ws.sfa, ws.sfa_rows, 1, 32 * MX_CH, 1)) return A2AV_ERR_CUDA;
+        if (!mx_atoms_map(&g.tmSFB, wsb + ws.sfb, ncb1 * 32, d.e * nq1, 32 * ctas, MX_CH)) return A2AV_ERR_CUDA;
     }
     if (shared) {
         const int64_t nq2 = d.H2 / MX_QUAD, ncb2 = (d.N2 + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS;
         const int64_t nh2 = (d.BS + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS;
         if (!mx_codes_map(&g.tmX, mmX_q, 1, d.BS, d.H2)) return A2AV_ERR_CUDA;
         if (!mx_codes_map(&g.tmMW, mmWeight_q, 1, d.N2, d.H2)) return A2AV_ERR_CUDA;
-        if (!mx_atoms_map(&g.tmSFX, wsb + ws.sfx, nh2 * nq2 * 32, 1, 64, 1)) return A2AV_ERR_CUDA;
-        if (!mx_atoms_map(&g.tmSFW, wsb + ws.sfw, ncb2 * 32, nq2, 32 * ctas, 2)) return A2AV_ERR_CUDA;
+        if (!mx_atoms_map(&g.tmSFX, wsb + ws.sfx, nh2 * nq2 * 32, 1, 32 * MX_CH, 1)) return A2AV_ERR_CUDA;
+        if (!mx_atoms_map(&g.tmSFW, wsb + ws.sfw, ncb2 * 32, nq2, 32 * ctas, MX_CH)) return A2AV_ERR_CUDA;
     }
     // The prep kernel: expert-major codes (into permuteOut, or only the
     // halves that straddle a segment boundary into the staging copy), and
