@@ -312,10 +312,12 @@ a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const in
             // straddle a segment boundary are staged; the GEMM reads the rest
             // in place.
             const int32_t partial = (!perm_out && resolve_path(&d) == A2AV_PATH_SPLIT_RUNS) ? 1 : 0;
-            // Two permute blocks per SM leave room for the GEMM CTA, which
-            // starts beside the permute and waits only before staged rows.
+            // Eight permute blocks per SM (all resident at once).  The GEMM
+            // is launched beside it (programmatic dependent launch) and waits
+            // only before staged rows; in practice its CTAs find SMs as the
+            // permute blocks retire.
             a2av::PermuteLaunch pl{recvCounts, d.W, d.e, static_cast<int32_t>(d.A),
-                                   static_cast<int32_t>(d.H1), ataOut, dst, status, 1, partial, 2};
+                                   static_cast<int32_t>(d.H1), ataOut, dst, status, 1, partial, 8};
             g.after_permute = 1;
             if (a2av::launch_permute(pl, sms, stream) != cudaSuccess) return A2AV_ERR_CUDA;
             permute_ran = true;
