@@ -80,6 +80,7 @@ def algorithmic_bytes(wl, A, permute_out):
 GEMM_SOURCES = ("api.cu", "grouped_gemm.cu", "kernels.h", "permute.cu", "plan.cuh", "ptx.cuh")
 QREDUCE_SOURCES = ("quant_reduce.cu", "ptx.cuh", "../../include/a2av_quant_reduce.h")
 MX_SOURCES = ("grouped_gemm_mx.cu", "plan.cuh", "ptx.cuh", "../../include/a2av_gmm_mx.h")
+AMP_SOURCES = ("amp.cu", "kernels.h")
 
 
 def source_hash(names=GEMM_SOURCES):
@@ -93,7 +94,8 @@ def source_hash(names=GEMM_SOURCES):
 def profiled_traffic(workload, permute_out=False, path="default", tiles="default", kernel="grouped_gemm_kernel"):
     """DRAM bytes per launch of a kernel from a committed ncu summary, only
     while the kernel's sources are unchanged since the capture."""
-    names = {"quant_reduce_kernel": QREDUCE_SOURCES, "grouped_gemm_mx_kernel": MX_SOURCES}.get(kernel, GEMM_SOURCES)
+    names = {"quant_reduce_kernel": QREDUCE_SOURCES, "grouped_gemm_mx_kernel": MX_SOURCES,
+             "nonfinite_scan_kernel": AMP_SOURCES}.get(kernel, GEMM_SOURCES)
     for f in glob.glob(os.path.join(ROOT, "profiles", "*.json")):
         try:
             with open(f) as fh:
@@ -514,7 +516,9 @@ def run_amp(args):
         "config": {"workload": "amp_scan_bf16_34502x4096", "bytes_per_scan": n * 2,
                    "l2": "two 283 MB buffers alternated (> 129 MiB L2)", "update_us_per_call": round(upd_us, 2)},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(gbs / pk["hbm_gbs"], 4),
+                     "traffic": profiled_traffic("amp_scan_bf16_34502x4096", kernel="nonfinite_scan_kernel"),
+                     "kernel": "nonfinite_scan_kernel",
                      "peak_source": f"{pk_kind} copy bandwidth (read + write); the scan only reads"},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks.summary(),
