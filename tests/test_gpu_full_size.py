@@ -1,21 +1,24 @@
-"""Full-size workloads on the GPU against the oracle (needs a GB300).
+"""Full-size workloads on the GPU against the oracle, every element (needs a GB300).
 
 Each workload runs in the launch configuration bench.py times (default path,
 permuteOut not requested) and again with permuteOut.  permuteOut is compared
-bit for bit in full; gmmY and mmY on sampled rows (every group's first and
-last rows, the rows around each group's last tile boundary, and a seeded
-random set), each checked element by element against the float64 oracle.
+bit for bit; every row of gmmY and mmY is compared element by element with
+the float64 oracle (|gpu - ref| <= 2e-2 * max(1, |ref|)), in blocks of rows
+so that the float64 reference never has to be held whole.  The oracle's
+products take about a minute for the largest workloads on 16 host cores.
 """
 
 import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import assert_bits_equal, assert_close, run_gpu, sample_rows
+from gpu_helpers import assert_bits_equal, assert_close, run_gpu
 from token_permute_grouped_gb300 import build
 from token_permute_grouped_gb300.workloads import WORKLOADS, make_inputs
 
 pytestmark = pytest.mark.gpu
+
+BLOCK_ROWS = 8192
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -47,10 +50,11 @@ def test_full_size_workload(orc, name):
     ref_perm = orc.permute(wl.W, wl.e, inp.recvCounts, inp.ataOut)
     assert_bits_equal(perm, ref_perm, "permuteOut")
     _, _, gr, _ = orc.plan(wl.W, wl.e, inp.recvCounts, inp.A)
-    rows = sample_rows(gr, 192, seed=1)
-    ref = orc.grouped_matmul(gr, ref_perm, inp.gmmWeight, rows)
-    assert_close(gmmY[rows], ref, f"gmmY rows of {name}")
-    if wl.BS:
-        srows = sample_rows([wl.BS], 96, seed=2)
-        ref = orc.matmul(inp.mmX, inp.mmWeight, srows)
-        assert_close(mmY[srows], ref, f"mmY rows of {name}")
+    for r0 in range(0, inp.A, BLOCK_ROWS):
+        rows = np.arange(r0, min(inp.A, r0 + BLOCK_ROWS), dtype=np.int64)
+        ref = orc.grouped_matmul(gr, ref_perm, inp.gmmWeight, rows)
+        assert_close(gmmY[r0:r0 + len(rows)], ref, f"gmmY rows {r0}.. of {name}")
+    for r0 in range(0, wl.BS, BLOCK_ROWS):
+        rows = np.arange(r0, min(wl.BS, r0 + BLOCK_ROWS), dtype=np.int64)
+        ref = orc.matmul(inp.mmX, inp.mmWeight, rows)
+        assert_close(mmY[r0:r0 + len(rows)], ref, f"mmY rows {r0}.. of {name}")

@@ -16,7 +16,7 @@ import torch
 
 from gpu_helpers import assert_close
 from token_permute_grouped_gb300 import binding, build
-from token_permute_grouped_gb300.workloads import (HEADLINE, WORKLOADS, make_mx_inputs, mx_quantize,
+from token_permute_grouped_gb300.workloads import (W8E4, WORKLOADS, make_mx_inputs, mx_quantize,
                                                    random_counts, MxInputs, Workload)
 
 pytestmark = pytest.mark.gpu
@@ -138,10 +138,10 @@ def test_permute_out_bit_exact_and_same_products(orc):
     assert torch.equal(pq, ref_q) and torch.equal(ps, ref_s)
     (y2, _, _, _), st = run_mx(inp, want_perm=False)
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
-    # The other tile shape gives the same products (fp32 sums of the same
-    # K blocks in the same order).
+    # The other tile shape gives the same bits (fp32 sums of the same K
+    # blocks in the same order).
     (y3, _, _, _), st = run_mx(inp, tiles="single")
-    assert st[0] == 0 and torch.allclose(y3.float(), y.float(), rtol=1e-2, atol=1e-2)
+    assert st[0] == 0 and torch.equal(y3.view(torch.int16), y.view(torch.int16))
 
 
 def test_integer_products_bit_exact(orc):
@@ -171,7 +171,7 @@ def test_bad_counts_are_reported(orc):
 
 def test_full_size_headline(orc):
     # The 8-rank x 4-expert workload in mx form, compared on sampled rows.
-    inp = make_mx_inputs(WORKLOADS[HEADLINE], seed=0, qtype="e4m3fn")
+    inp = make_mx_inputs(WORKLOADS[W8E4], seed=0, qtype="e4m3fn")
     (y, m, _, _), st = run_mx(inp)
     assert st[0] == 0, st
     rng = np.random.default_rng(7)
@@ -180,3 +180,35 @@ def test_full_size_headline(orc):
     _, _, ref_y, ref_m = reference(orc, inp, rows=rows, shared_rows=srows)
     assert_close(y[rows], ref_y, "gmmY")
     assert_close(m[srows], ref_m, "mmY")
+
+
+_MULTI = {}
+
+
+def _multi_tile_case():
+    # About 24K routed rows and a 4096-row shared expert: with 256 x 256 pair
+    # tiles about six tiles per pair unit, with 128 x 128 single tiles about
+    # eleven per CTA.  Each unit therefore reuses its accumulator and scale
+    # columns across tiles and wraps its stage ring many times.
+    if not _MULTI:
+        rc = random_counts(8, 4, 24000, seed=21, zero_prob=0.05)
+        inp = _custom(8, 4, 512, 1024, rc, "e4m3fn", BS=4096, H2=512, N2=1024, seed=21)
+        _MULTI["inp"] = inp
+    return _MULTI["inp"]
+
+
+@pytest.mark.parametrize("tiles", TILES)
+def test_multi_tile_every_element(orc, tiles):
+    inp = _multi_tile_case()
+    (y, m, _, _), st = run_mx(inp, tiles=tiles)
+    assert st[0] == 0, st
+    if "ref" not in _MULTI:
+        _MULTI["ref"] = reference(orc, inp)
+        _MULTI["first"] = (y, m)
+    _, _, ref_y, ref_m = _MULTI["ref"]
+    assert_close(y, ref_y, "gmmY")
+    assert_close(m, ref_m, "mmY")
+    # Both tile shapes give the same bits.
+    y0, m0 = _MULTI["first"]
+    assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+    assert torch.equal(m.view(torch.int16), m0.view(torch.int16))
