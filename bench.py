@@ -76,6 +76,24 @@ def algorithmic_bytes(wl, A, permute_out):
     return b
 
 
+def replicas_for(wl, A, permute_out):
+    """Input replicas rotated between steps so that no step finds its inputs in L2."""
+    return min(64, max(2, -(-3 * L2_BYTES // max(algorithmic_bytes(wl, A, permute_out), 1))))
+
+
+def workload_config(wl, A, args):
+    """The line's `config`: the workload and the protocol, identical in both arms."""
+    reps = replicas_for(wl, A, args.permute_out)
+    set_mib = reps * algorithmic_bytes(wl, A, args.permute_out) / 2**20
+    return {
+        "workload": wl.name, "W": wl.W, "e": wl.e, "A": A, "H1": wl.H1, "N1": wl.N1,
+        "BS": wl.BS, "H2": wl.H2, "N2": wl.N2, "dtype": wl.dtype, "path": args.path, "tiles": args.tiles,
+        "permute_out": bool(args.permute_out), "accumulate": "fp32",
+        "l2": (f"GPU arm: inputs rotated over {reps} replicas ({set_mib:.0f} MiB > 129 MiB L2); "
+               "reference arm: host memory"),
+    }
+
+
 # The sources each measured call depends on (kernels and host setup).
 GEMM_SOURCES = ("api.cu", "grouped_gemm.cu", "kernels.h", "permute.cu", "plan.cuh", "ptx.cuh")
 QREDUCE_SOURCES = ("quant_reduce.cu", "ptx.cuh", "../../include/a2av_quant_reduce.h")
@@ -239,9 +257,7 @@ def run_gpu(args):
     launches_per_call = binding.a2av_gmm_launch_count(plan.desc)
 
     # Input replicas, rotated so that no step finds its inputs in L2.
-    set_bytes = algorithmic_bytes(wl, A, args.permute_out)
-    reps = max(2, -(-3 * L2_BYTES // max(set_bytes, 1)))
-    reps = min(reps, 64)
+    reps = replicas_for(wl, A, args.permute_out)
     host = {"ataOut": inp.ataOut, "gmmWeight": inp.gmmWeight, "mmX": inp.mmX, "mmWeight": inp.mmWeight}
     rc_dev = torch.from_numpy(inp.recvCounts).to(dev)
     sets = []
@@ -253,10 +269,10 @@ def run_gpu(args):
         sets.append(s)
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
+    def step(i, gemm_events=None):
         s = sets[i % reps]
         plan.run(s["ataOut"], rc_dev, s["gmmWeight"], s["mmX"], s["mmWeight"], gmmY=s["gmmY"], mmY=s["mmY"],
-                 permuteOut=s["perm"], stream=stream)
+                 permuteOut=s["perm"], stream=stream, gemm_events=gemm_events)
 
     sync = torch.cuda.synchronize
     for i in range(args.warmup):
@@ -266,9 +282,8 @@ def run_gpu(args):
     if st != 0:
         raise RuntimeError(f"device status {st} ({code})")
 
-    # Per-call device time on the launching stream: the whole call, so the
-    # permute kernel that split paths launch before the GEMM is included and
-    # roofline.achieved understates the GEMM kernel alone.
+    # Per-call device time on the launching stream: the whole call (scan,
+    # permute and GEMM), which `value` reports.
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
 
     def timed_step(i):
@@ -286,6 +301,15 @@ def run_gpu(args):
     total_flops = reduce_sum(flops * args.steps, world, dev)
     tflops = total_flops / dev_s_max / 1e12
     ms_per_step = dev_s_max * 1e3 / args.steps
+
+    # The dominant kernel alone: K more calls through a2av_gmm_run_profiled,
+    # which records a pair of events on the launching stream right around the
+    # grouped-GEMM kernel (the GEMM then starts after the permute kernel in
+    # plain stream order).
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    timed_region(lambda i: step(i, gev[i]), args.steps, world, dev, sync)
+    gemm_ms = [b.elapsed_time(e) for b, e in gev]
 
     # End to end through the same public call with host buffers: this step's
     # activations (ataOut, recvCounts, mmX) copied in from pinned memory, the
@@ -348,8 +372,9 @@ def run_gpu(args):
         return
     pk, pk_kind = peaks()
     peak_tf = pk["bf16_tflops"]
-    per_call_us = statistics.median(per_call_ms) * 1e3
-    achieved = flops / (dev_s / args.steps) / 1e12
+    gemm_s = statistics.fmean(gemm_ms) / 1e3
+    achieved = flops / gemm_s / 1e12
+    whole = flops / (dev_s / args.steps) / 1e12
     line = {
         "metric": METRIC,
         "value": round(tflops, 2),
@@ -363,16 +388,16 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": wl.dtype,
         "data": "synthetic (seeded routing and N(0,1) tensors; no dataset)",
-        "config": {
-            "workload": wl.name, "W": wl.W, "e": wl.e, "A": A, "H1": wl.H1, "N1": wl.N1,
-            "BS": wl.BS, "H2": wl.H2, "N2": wl.N2, "path": args.path, "tiles": args.tiles,
-            "permute_out": bool(args.permute_out), "accumulate": "fp32",
-            "us_per_call_median": round(per_call_us, 2),
+        "config": workload_config(wl, A, args),
+        "timing": {
+            "us_per_call_median": round(statistics.median(per_call_ms) * 1e3, 2),
             "us_per_call_min": round(min(per_call_ms) * 1e3, 2),
+            "us_per_call_p90": round(float(np.percentile(per_call_ms, 90)) * 1e3, 2),
+            "gemm_kernel_us_mean": round(gemm_s * 1e6, 2),
+            "gemm_kernel_us_p90": round(float(np.percentile(gemm_ms, 90)) * 1e3, 2),
             "pct_of_bf16_peak": round(100 * tflops / world / peak_tf, 2),
             "pct_of_bf16_sustained": round(100 * tflops / world / pk["bf16_tflops_sustained"], 2),
             "gflop_per_call": round(flops / 1e9, 3),
-            "l2": f"inputs rotated over {reps} replicas ({reps * set_bytes / 2**20:.0f} MiB > 129 MiB L2)",
             "group_rows": inp.recvCounts.reshape(wl.W, wl.e).sum(0).tolist(),
             "launches_per_call": launches_per_call,
         },
@@ -384,9 +409,13 @@ def run_gpu(args):
             "frac": round(achieved / peak_tf, 4),
             "traffic": profiled_traffic(wl.name, bool(args.permute_out), args.path, args.tiles),
             "kernel": "grouped_gemm_kernel",
-            "timed": "whole call (CUDA events on the launching stream; the permute kernel included)",
+            "timed": ("the GEMM kernel alone: CUDA events recorded on its launching stream right before and "
+                      f"after it, mean of {args.steps} launches (a2av_gmm_run_profiled)"),
+            "whole_call": {"achieved": round(whole, 2), "frac": round(whole / peak_tf, 4),
+                           "timed": "scan + permute + GEMM, CUDA events around each call"},
             "peak_source": f"{pk_kind} bf16 dense burst (MEASURED_PEAKS.json bf16_tflops)" if pk_kind == "measured"
             else "fallback 1.9 PFLOP/s",
+            "algorithmic_flops_per_launch": flops,
             "algorithmic_bytes": algorithmic_bytes(wl, A, args.permute_out),
         },
         "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
@@ -467,10 +496,9 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot_s * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "W": wl.W, "e": wl.e, "A": inp.A, "H1": wl.H1, "N1": wl.N1,
-                   "BS": wl.BS, "H2": wl.H2, "N2": wl.N2, "seconds_per_step": per_step},
+        "config": workload_config(wl, inp.A, args),
         "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "seconds_per_step": per_step},
         "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }

@@ -136,6 +136,22 @@ a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut,
                          size_t workspace_bytes, a2av_stream_t stream);
 
 /*
+ * Diagnostic form of a2av_gmm_run for measurement: the same work, plus two
+ * CUDA events (cudaEvent_t, created by the caller) recorded on `stream`
+ * right before and right after the grouped-GEMM kernel, so that the
+ * elapsed time between them is that kernel's duration alone.  The GEMM then
+ * starts after the permute kernel in plain stream order instead of being
+ * launched beside it.  (The operator page has no counterpart.)
+ * Returns A2AV_ERR_NULLPTR when either event is NULL, else as a2av_gmm_run.
+ */
+a2av_status a2av_gmm_run_profiled(const a2av_gmm_desc *desc, const void *ataOut,
+                                  const int32_t *recvCounts, const void *gmmWeight,
+                                  const void *mmX, const void *mmWeight, void *permuteOut,
+                                  void *gmmY, void *mmY, void *workspace,
+                                  size_t workspace_bytes, a2av_stream_t stream,
+                                  void *gemm_begin_event, void *gemm_end_event);
+
+/*
  * Waits for `stream`, then reads the device-side status a2av_gmm_run left in
  * `workspace`: A2AV_OK, or A2AV_ERR_DEVICE_CHECK (recvCounts negative or not
  * summing to A; outputs were not written), or A2AV_ERR_CUDA (a kernel gave up
@@ -167,9 +183,12 @@ a2av_status a2av_gmm_read_device_status(const void *workspace, a2av_stream_t str
  * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  * routine.
  *
- * Set-up: the first call on each device (with that device current) looks up
- * the array's device address once; make that first call before any stream
- * capture begins.
+ * Set-up: every call looks up the array's device address in the current
+ * device's context (cudaGetSymbolAddress, a host-side query that allocates
+ * nothing), so a context that was torn down and created again (after
+ * cudaDeviceReset) gets the array's new address.  The first call on a device
+ * may also load the library's kernels into that context; make that first
+ * call before any stream capture begins.
  *
  * Sharing: every call on a device uses the same array, and the array keeps
  * the previous call's contents.  The kernels overwrite every scratch byte

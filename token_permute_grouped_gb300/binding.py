@@ -28,6 +28,7 @@ TILES = {"default": 0, "single": 1, "pair": 2, "pair_k64": 3}
 # Every function the headers under include/ declare.
 EXPORTS = ("a2av_gmm_workspace_size", "a2av_gmm_run", "a2av_gmm_read_device_status",
            "a2av_gmm_status_string", "a2av_gmm_launch_count", "a2av_gmm_run_static_scratch",
+           "a2av_gmm_run_profiled",
            "a2av_amp_update_scale", "a2av_found_nonfinite", "a2av_quant_reduce",
            "a2av_gmm_mx_workspace_size", "a2av_gmm_mx_run")
 
@@ -77,6 +78,8 @@ def load():
         L.a2av_gmm_workspace_size.restype = ctypes.c_int
         L.a2av_gmm_run.argtypes = [ctypes.POINTER(Desc), p, p, p, p, p, p, p, p, p, sz, p]
         L.a2av_gmm_run.restype = ctypes.c_int
+        L.a2av_gmm_run_profiled.argtypes = [ctypes.POINTER(Desc), p, p, p, p, p, p, p, p, p, sz, p, p, p]
+        L.a2av_gmm_run_profiled.restype = ctypes.c_int
         L.a2av_gmm_read_device_status.argtypes = [p, p, ctypes.POINTER(i32)]
         L.a2av_gmm_read_device_status.restype = ctypes.c_int
         L.a2av_gmm_status_string.argtypes = [ctypes.c_int]
@@ -134,6 +137,23 @@ def a2av_gmm_run(desc: Desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permu
                              _ptr(workspace), workspace.numel(), ctypes.c_void_p(s.cuda_stream))
     if st != A2AV_OK:
         raise A2avError(st, "a2av_gmm_run")
+
+
+def a2av_gmm_run_profiled(desc: Desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permuteOut, gmmY, mmY,
+                          workspace: torch.Tensor, gemm_begin: torch.cuda.Event, gemm_end: torch.cuda.Event,
+                          stream=None) -> None:
+    """a2av_gmm_run with two timing events (torch.cuda.Event(enable_timing=True)) recorded
+    right before and after the grouped-GEMM kernel."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    for ev in (gemm_begin, gemm_end):
+        if ev.cuda_event == 0:  # created lazily by torch: make it exist on this device
+            ev.record(s)
+    st = load().a2av_gmm_run_profiled(ctypes.byref(desc), _ptr(ataOut), _ptr(recvCounts), _ptr(gmmWeight),
+                                      _ptr(mmX), _ptr(mmWeight), _ptr(permuteOut), _ptr(gmmY), _ptr(mmY),
+                                      _ptr(workspace), workspace.numel(), ctypes.c_void_p(s.cuda_stream),
+                                      ctypes.c_void_p(gemm_begin.cuda_event), ctypes.c_void_p(gemm_end.cuda_event))
+    if st != A2AV_OK:
+        raise A2avError(st, "a2av_gmm_run_profiled")
 
 
 def a2av_gmm_run_static_scratch(desc: Desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permuteOut, gmmY,
@@ -223,7 +243,9 @@ class Plan:
         self.workspace = torch.empty(a2av_gmm_workspace_size(self.desc), dtype=torch.uint8, device=self.device)
 
     def run(self, ataOut, recvCounts, gmmWeight, mmX=None, mmWeight=None, gmmY=None, mmY=None,
-            permuteOut=None, stream=None):
+            permuteOut=None, stream=None, gemm_events=None):
+        """gemm_events: optional (begin, end) timing events recorded around the GEMM kernel
+        (a2av_gmm_run_profiled)."""
         d = self.desc
         if d.A:
             _check(ataOut, "ataOut", self.dtype, 2)
@@ -242,9 +264,13 @@ class Plan:
             _check(mmWeight, "mmWeight", self.dtype, 2)
             if mmY is None:
                 mmY = torch.empty(d.BS, d.N2, dtype=self.dtype, device=self.device)
-        a2av_gmm_run(d, ataOut if d.A else None, recvCounts, gmmWeight, mmX, mmWeight,
-                     permuteOut if d.want_permute_out else None, gmmY if d.A else None,
-                     mmY if d.BS else None, self.workspace, stream)
+        args = (d, ataOut if d.A else None, recvCounts, gmmWeight, mmX, mmWeight,
+                permuteOut if d.want_permute_out else None, gmmY if d.A else None,
+                mmY if d.BS else None, self.workspace)
+        if gemm_events is None:
+            a2av_gmm_run(*args, stream)
+        else:
+            a2av_gmm_run_profiled(*args, gemm_events[0], gemm_events[1], stream)
         return gmmY, mmY, permuteOut
 
 

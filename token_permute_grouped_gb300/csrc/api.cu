@@ -21,6 +21,7 @@ static __device__ __align__(256) uint8_t g_static_scratch[A2AV_STATIC_SCRATCH_BY
 namespace {
 
 constexpr size_t kStatusBytes = 256;  // status word, padded to keep what follows aligned
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bound on every device-side wait
 constexpr int kMaxDevices = 64;
 constexpr int kBM = 128;
 
@@ -188,21 +189,17 @@ int sm_count() {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Device address of g_static_scratch on the current device, looked up once
-// per device.  In host code the symbol name is only a host-side stand-in,
-// never a device address, so it must go through cudaGetSymbolAddress.
+// Device address of g_static_scratch in the current device's context.  In
+// host code the symbol name is only a host-side stand-in, never a device
+// address, so it must go through cudaGetSymbolAddress.  The lookup is a
+// host-side query that allocates nothing; it is repeated on every call
+// rather than cached, because a context torn down and created again (after
+// cudaDeviceReset, for one) loads the module afresh and the array may then
+// sit at another address.
 void *static_scratch_address() {
-    static void *addr[kMaxDevices] = {nullptr};
-    static std::mutex lock;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> guard(lock);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+    return p;
 }
 
 }  // namespace
@@ -222,10 +219,17 @@ int32_t a2av_gmm_launch_count(const a2av_gmm_desc *desc) {
     return (use_split(desc) && desc->A > 0) ? 2 : 1;
 }
 
-a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const int32_t *recvCounts,
-                         const void *gmmWeight, const void *mmX, const void *mmWeight, void *permuteOut,
-                         void *gmmY, void *mmY, void *workspace, size_t workspace_bytes,
-                         a2av_stream_t stream_handle) {
+}  // extern "C"
+
+namespace {
+
+// The body of a2av_gmm_run.  With gemm_begin / gemm_end set, those events
+// are recorded on the stream right before and right after the GEMM launch
+// (which then starts after the permute kernel in plain stream order).
+a2av_status run_impl(const a2av_gmm_desc *desc, const void *ataOut, const int32_t *recvCounts,
+                     const void *gmmWeight, const void *mmX, const void *mmWeight, void *permuteOut, void *gmmY,
+                     void *mmY, void *workspace, size_t workspace_bytes, a2av_stream_t stream_handle,
+                     cudaEvent_t gemm_begin, cudaEvent_t gemm_end) {
     const a2av_status vs = validate(desc);
     if (vs != A2AV_OK) return vs;
     const a2av_gmm_desc &d = *desc;
@@ -335,6 +339,7 @@ a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const in
         }
     }
     g.write_status = permute_ran ? 0 : 1;
+    g.wait_limit_ns = kWaitLimitNs;
 
     // Persistent grid: as many CTAs (pair: clusters of two) as fit on the
     // device at once, never more than there can be tiles.
@@ -348,8 +353,36 @@ a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const in
     g.pair = pair ? 1 : 0;
     const int64_t n_units = std::max<int64_t>(1, std::min<int64_t>(units, tiles));
     g.grid = static_cast<int32_t>(n_units * (pair ? 2 : 1));
+    if (gemm_begin) {
+        g.after_permute = 0;  // an event between the kernels: plain stream order
+        if (cudaEventRecord(gemm_begin, stream) != cudaSuccess) return A2AV_ERR_CUDA;
+    }
     if (a2av::launch_grouped_gemm(g, stream) != cudaSuccess) return A2AV_ERR_CUDA;
+    if (gemm_end && cudaEventRecord(gemm_end, stream) != cudaSuccess) return A2AV_ERR_CUDA;
     return A2AV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+a2av_status a2av_gmm_run(const a2av_gmm_desc *desc, const void *ataOut, const int32_t *recvCounts,
+                         const void *gmmWeight, const void *mmX, const void *mmWeight, void *permuteOut,
+                         void *gmmY, void *mmY, void *workspace, size_t workspace_bytes,
+                         a2av_stream_t stream) {
+    return run_impl(desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permuteOut, gmmY, mmY, workspace,
+                    workspace_bytes, stream, nullptr, nullptr);
+}
+
+a2av_status a2av_gmm_run_profiled(const a2av_gmm_desc *desc, const void *ataOut, const int32_t *recvCounts,
+                                  const void *gmmWeight, const void *mmX, const void *mmWeight,
+                                  void *permuteOut, void *gmmY, void *mmY, void *workspace,
+                                  size_t workspace_bytes, a2av_stream_t stream, void *gemm_begin_event,
+                                  void *gemm_end_event) {
+    if (!gemm_begin_event || !gemm_end_event) return A2AV_ERR_NULLPTR;
+    return run_impl(desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permuteOut, gmmY, mmY, workspace,
+                    workspace_bytes, stream, static_cast<cudaEvent_t>(gemm_begin_event),
+                    static_cast<cudaEvent_t>(gemm_end_event));
 }
 
 a2av_status a2av_gmm_run_static_scratch(const a2av_gmm_desc *desc, const void *ataOut,

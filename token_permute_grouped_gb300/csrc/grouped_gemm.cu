@@ -51,7 +51,6 @@ constexpr int kMmaWarp = 4;
 constexpr int kThreads = 9 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 256;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // CH = 64-wide K chunks per pipeline stage (1 or 2).  With CH = 2 each stage
 // holds 128 of K in the same bytes-in-flight budget as twice as many CH = 1
@@ -114,7 +113,8 @@ __device__ __forceinline__ Tile decode_tile(const C &c, int t) {
 // the abort flag and the status word are set.  CLUSTER: acquire at cluster
 // scope (the arrivals come from the peer CTA too).
 template <bool CLUSTER = false>
-__device__ __noinline__ bool wait_phase(int32_t *abort_flag, uint64_t *bar, uint32_t parity, int32_t *status) {
+__device__ __noinline__ bool wait_phase(int32_t *abort_flag, uint64_t *bar, uint32_t parity, int32_t *status,
+                                        uint64_t limit_ns) {
     const uint32_t b = smem_u32(bar);
     auto try_once = [&]() -> bool {
         if constexpr (CLUSTER) {
@@ -137,7 +137,7 @@ __device__ __noinline__ bool wait_phase(int32_t *abort_flag, uint64_t *bar, uint
         for (int i = 0; i < 64; ++i)
             if (try_once()) return true;
         if (*reinterpret_cast<volatile int32_t *>(abort_flag)) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > limit_ns) {
             *reinterpret_cast<volatile int32_t *>(abort_flag) = 1;
             atomicOr(status, kStatusTimeout);
             return false;
@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     const int s = it % STAGES;
                     bool free_slot = true;
                     if (lane == 0)
-                        free_slot = wait_phase(&C.abort, &C.empty[s], ((it / STAGES) & 1) ^ 1, p.status);
+                        free_slot = wait_phase(&C.abort, &C.empty[s], ((it / STAGES) & 1) ^ 1, p.status, p.wait_limit_ns);
                     if (!__shfl_sync(0xffffffffu, free_slot, 0)) {
                         ok = false;
                         break;
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             // Tail: wait until the MMAs released every stage we filled.
             if (lane == 0)
                 for (int i = 0; i < STAGES && ok; ++i, ++it)
-                    ok = wait_phase(&C.abort, &C.empty[it % STAGES], ((it / STAGES) & 1) ^ 1, p.status);
+                    ok = wait_phase(&C.abort, &C.empty[it % STAGES], ((it / STAGES) & 1) ^ 1, p.status, p.wait_limit_ns);
         } else if (GATHER && p.permuteOut != nullptr) {
             // Warps 1-3 write permuteOut for this CTA's rows of the tiles of
             // the first column, straight from ataOut (16-byte vectors, 4 in
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const uint32_t idesc = shared ? idesc2 : idesc1;
                 const int kblocks = (K + BK - 1) / BK;
                 const int acc = tl & 1;
-                if (!wait_phase<PAIR>(&C.abort, &C.tempty[acc], ((tl >> 1) & 1) ^ 1, p.status)) break;
+                if (!wait_phase<PAIR>(&C.abort, &C.tempty[acc], ((tl >> 1) & 1) ^ 1, p.status, p.wait_limit_ns)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = C.tmem_base + acc * kAccCols;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     // them: the barrier phase alone orders the two, and no
                     // tcgen05 fence is needed here.
                     if (!mbar_try_wait(full0 + s * sizeof(uint64_t), par) &&
-                        !wait_phase(&C.abort, &C.full[s], par, p.status)) {
+                        !wait_phase(&C.abort, &C.full[s], par, p.status, p.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -601,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const Tile w = decode_tile(C, t);
             const bool shared = w.g >= e;
             const int acc = tl & 1;
-            if (!wait_phase(&C.abort, &C.tfull[acc], (tl >> 1) & 1, p.status)) break;
+            if (!wait_phase(&C.abort, &C.tfull[acc], (tl >> 1) & 1, p.status, p.wait_limit_ns)) break;
             __syncwarp();  // lanes leave the wait independently; tcgen05.ld needs the whole warp
             tc_fence_after_sync();
             const int N = shared ? p.N2 : p.N1;

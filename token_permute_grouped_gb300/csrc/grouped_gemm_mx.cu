@@ -701,6 +701,15 @@ __global__ void __launch_bounds__(kMxPermThreads) mx_prep_kernel(const __grid_co
     __shared__ StagedHalves halves;
     __shared__ int32_t half0[kMaxExperts + 1];  // routed: first 128-row half of each expert group
     __shared__ int ok;
+    // The first kernel of the call clears the status word before the GEMM
+    // behind it can start; every later write to it is an atomicOr.
+    if (blockIdx.x == 0) {
+        if (threadIdx.x == 0) {
+            *p.status = 0;
+            __threadfence();
+        }
+        __syncthreads();
+    }
     // The GEMM launched after this kernel with programmatic dependent launch
     // may start now: it waits for this grid's completion before it reads
     // anything this kernel writes.
@@ -722,7 +731,7 @@ __global__ void __launch_bounds__(kMxPermThreads) mx_prep_kernel(const __grid_co
         if (lane == 0) {
             half0[e] = all;
             ok = good;
-            if (blockIdx.x == 0) *p.status = good ? 0 : kStatusBadCounts;  // the first kernel of the call
+            if (blockIdx.x == 0 && !good) atomicOr(p.status, kStatusBadCounts);
         }
     }
     __syncthreads();

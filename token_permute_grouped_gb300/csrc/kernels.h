@@ -55,6 +55,8 @@ struct GemmLaunch {
     int32_t b4_routed, b4_shared;
     int32_t after_permute;    // 1: launched to overlap the permute kernel before it (programmatic
                               // dependent launch); the producer waits for it before staged loads
+    uint64_t wait_limit_ns;   // bound on every pipeline wait; on expiry the kernel records
+                              // kStatusTimeout and winds down
 };
 
 cudaError_t launch_grouped_gemm(const GemmLaunch &p, cudaStream_t stream);

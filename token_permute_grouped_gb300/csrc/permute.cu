@@ -30,6 +30,16 @@ __global__ void __launch_bounds__(kPermuteThreads)
     __shared__ SegmentTable table;
     __shared__ StagedHalves halves;
     __shared__ int ok;
+    // The first kernel of a call clears the status word before the GEMM
+    // behind it can start, so that later kernels only ever set bits in it
+    // (atomicOr) and none of their bits is lost to this store.
+    if (write_status && blockIdx.x == 0) {
+        if (threadIdx.x == 0) {
+            *status = 0;
+            __threadfence();
+        }
+        __syncthreads();
+    }
     // A GEMM launched after this kernel with programmatic dependent launch
     // may start now: it waits for this grid's completion before it reads
     // any row this kernel writes.
@@ -39,10 +49,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
         bool good = build_segment_table(recvCounts, W, e, A, table, lane);
         if (lane == 0) {
             ok = good;
-            if (blockIdx.x == 0) {
-                if (write_status) *status = good ? 0 : kStatusBadCounts;
-                else if (!good) atomicOr(status, kStatusBadCounts);
-            }
+            if (blockIdx.x == 0 && !good) atomicOr(status, kStatusBadCounts);
         }
     }
     __syncthreads();
