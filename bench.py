@@ -249,7 +249,10 @@ def run_gpu(args):
     binding.load()
 
     wl = WORKLOADS[args.workload]
-    inp = make_inputs(wl, seed=0, rank=rank)
+    # One process simulates the expert-parallel rank it stands for: its own
+    # rank under torchrun, or --sim-rank on one GPU.
+    sim_rank = rank if args.sim_rank is None else args.sim_rank
+    inp = make_inputs(wl, seed=0, rank=sim_rank)
     A = inp.A
     dt = wl.torch_dtype
     plan = binding.Plan(wl.W, wl.e, A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, dt,
@@ -388,7 +391,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": wl.dtype,
         "data": "synthetic (seeded routing and N(0,1) tensors; no dataset)",
-        "config": workload_config(wl, A, args),
+        "config": {**workload_config(wl, A, args), **({"sim_rank": sim_rank} if args.sim_rank is not None else {})},
         "timing": {
             "us_per_call_median": round(statistics.median(per_call_ms) * 1e3, 2),
             "us_per_call_min": round(min(per_call_ms) * 1e3, 2),
@@ -1079,6 +1082,8 @@ def main(argv=None):
     ap.add_argument("--path", default="default", choices=["default", "fused", "split", "split_runs"])
     ap.add_argument("--tiles", default="default", choices=["default", "single", "pair", "pair_k64"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sim-rank", type=int, default=None,
+                    help="N=1: time the inputs of this expert-parallel rank of the workload (default: rank 0)")
     ap.add_argument("--mx-qtype", default="e4m3fn", choices=["e4m3fn", "e5m2"], help="--op mx: code format")
     ap.add_argument("--op", default="gemm", choices=["gemm", "amp", "qreduce", "layer", "mx"],
                     help="gemm: the hot path (default); amp: the loss-scale step; qreduce: the quantised "

@@ -74,16 +74,18 @@ typedef enum {
     A2AV_ERR_WORKSPACE = 4,    /* workspace too small or misaligned */
     A2AV_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
     A2AV_ERR_DEVICE_CHECK = 6, /* the device found inconsistent recvCounts */
-    A2AV_ERR_SCRATCH_LIMIT = 7 /* a2av_gmm_run_static_scratch: the problem needs more
-                                  scratch than the library's static array holds */
+    A2AV_ERR_SCRATCH_LIMIT = 7, /* a2av_gmm_run_static_scratch: the problem needs more
+                                   scratch than the library's static array holds */
+    A2AV_ERR_ARRIVAL_TIMEOUT = 8 /* a2av_gmm_run_arrivals: a source's rows did not arrive
+                                   within the wait limit (device-detected) */
 } a2av_status;
 
 typedef enum { A2AV_BF16 = 0, A2AV_FP16 = 1, A2AV_FP32 = 2 /* a2av_found_nonfinite only */ } a2av_dtype;
 
 /* Execution path.  All give bitwise-identical outputs. */
 typedef enum {
-    A2AV_PATH_DEFAULT = 0,     /* chosen from the shapes: SPLIT_RUNS when N1 <= 1024 and
-                                  the (source, expert) runs average >= 512 rows, else SPLIT */
+    A2AV_PATH_DEFAULT = 0,     /* SPLIT_RUNS: which halves are staged is decided on the
+                                  device from recvCounts */
     A2AV_PATH_FUSED = 1,       /* one kernel: the grouped GEMM gathers its A rows from ataOut */
     A2AV_PATH_SPLIT = 2,       /* a permute kernel stages every row expert-major, then the GEMM */
     A2AV_PATH_SPLIT_RUNS = 3   /* the permute kernel stages only the 128-row halves of a GEMM
@@ -152,10 +154,43 @@ a2av_status a2av_gmm_run_profiled(const a2av_gmm_desc *desc, const void *ataOut,
                                   void *gemm_begin_event, void *gemm_end_event);
 
 /*
+ * The same computation, started before the AlltoAllv has finished: the
+ * overlap of the exchange with the grouped GEMM ("aclnnAlltoAllvGroupedMatMul",
+ * API function: AlltoAllv fused with Permute and GroupedMatMul; Formula:
+ * ataOut = AlltoAllv(gmmX)).
+ *
+ * `arrived` is a device array of W 64-bit flags, one per source rank.  The
+ * rows source w sends (its e runs of ataOut, rank-major) may be read once
+ * arrived[w] == arrival_tag; whatever moves them (a copy engine, a peer GPU's
+ * stores, the host) sets the flag after the rows have landed, for example
+ * by a copy of the tag ordered after the row copies on the same stream.
+ * recvCounts must be final when the call starts.  The kernel computes the
+ * shared expert first (it reads no exchanged rows), then each routed tile
+ * waits for the flags of the sources its rows come from and gathers those
+ * rows straight from ataOut (the fused path; desc->path must be
+ * A2AV_PATH_DEFAULT or A2AV_PATH_FUSED).  Flags must be 8-byte aligned; a
+ * new call uses a new tag, so flags need no reset between calls.
+ *
+ * Every wait is bounded by wait_limit_ns (0: 2 s).  A source that has not
+ * arrived by then makes the kernel wind down without finishing; the device
+ * status then reads A2AV_ERR_ARRIVAL_TIMEOUT (a2av_gmm_read_device_status)
+ * and the outputs are incomplete.  Other arguments and return codes are
+ * those of a2av_gmm_run.
+ */
+a2av_status a2av_gmm_run_arrivals(const a2av_gmm_desc *desc, const void *ataOut,
+                                  const int32_t *recvCounts, const void *gmmWeight,
+                                  const void *mmX, const void *mmWeight, void *permuteOut,
+                                  void *gmmY, void *mmY, const uint64_t *arrived,
+                                  uint64_t arrival_tag, uint64_t wait_limit_ns,
+                                  void *workspace, size_t workspace_bytes, a2av_stream_t stream);
+
+/*
  * Waits for `stream`, then reads the device-side status a2av_gmm_run left in
  * `workspace`: A2AV_OK, or A2AV_ERR_DEVICE_CHECK (recvCounts negative or not
- * summing to A; outputs were not written), or A2AV_ERR_CUDA (a kernel gave up
- * waiting on one of its own pipeline barriers).  The raw device word is
+ * summing to A; outputs were not written; or, in a debug build compiled with
+ * A2AV_CHECKS, an index found out of range and not used), A2AV_ERR_ARRIVAL_TIMEOUT
+ * (a2av_gmm_run_arrivals: a source never arrived), or A2AV_ERR_CUDA (a kernel
+ * gave up waiting on one of its own pipeline barriers).  The raw device word is
  * written to *code when code is not NULL.  For tests and diagnostics: it
  * synchronises.
  */

@@ -42,6 +42,32 @@ def test_library_exports_every_declared_symbol(lib):
         assert re.search(rf"\bT {name}\b", out), name
 
 
+def test_checks_build_exports_every_declared_symbol():
+    # The debug build (-DA2AV_CHECKS: device-side bounds checks that record a
+    # status bit) cross-compiles here and has the same C ABI.
+    path = build.build(checks=True)
+    assert path == build.CHECKS_LIB
+    L = binding.load_checks()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert L.a2av_gmm_status_string(6).decode() == binding.load().a2av_gmm_status_string(6).decode()
+
+
+def test_arrivals_argument_checks(lib):
+    d = binding.make_desc(8, 4, 1000, 512, 256)
+    args = [ctypes.c_void_p(0x10000 + 0x1000 * i) for i in range(8)]  # ataOut .. mmY
+    ok_flags = ctypes.c_void_p(0x20000)
+    call = lambda desc, flags: lib.a2av_gmm_run_arrivals(ctypes.byref(desc), *args, flags, ctypes.c_uint64(1),
+                                                         ctypes.c_uint64(0), ctypes.c_void_p(0x40000),
+                                                         ctypes.c_size_t(1 << 20), None)
+    assert binding.STATUS_NAMES[call(d, None)] == "A2AV_ERR_NULLPTR"
+    assert binding.STATUS_NAMES[call(d, ctypes.c_void_p(0x20004))] == "A2AV_ERR_UNSUPPORTED"  # not 8-byte aligned
+    d_split = binding.make_desc(8, 4, 1000, 512, 256, path="split")
+    assert binding.STATUS_NAMES[call(d_split, ok_flags)] == "A2AV_ERR_UNSUPPORTED"
+    bad = binding.make_desc(8, 40, 1000, 512, 256)
+    assert binding.STATUS_NAMES[call(bad, ok_flags)] == "A2AV_ERR_INVALID"
+
+
 def ws(**kw):
     base = dict(W=8, e=4, A=16000, H1=4096, N1=1024, BS=2048, H2=4096, N2=1024)
     base.update(kw)

@@ -19,7 +19,7 @@ from . import build as _build
 A2AV_OK = 0
 STATUS_NAMES = {0: "A2AV_OK", 1: "A2AV_ERR_NULLPTR", 2: "A2AV_ERR_INVALID", 3: "A2AV_ERR_UNSUPPORTED",
                 4: "A2AV_ERR_WORKSPACE", 5: "A2AV_ERR_CUDA", 6: "A2AV_ERR_DEVICE_CHECK",
-                7: "A2AV_ERR_SCRATCH_LIMIT"}
+                7: "A2AV_ERR_SCRATCH_LIMIT", 8: "A2AV_ERR_ARRIVAL_TIMEOUT"}
 STATIC_SCRATCH_BYTES = 256 + (8 << 20)  # A2AV_STATIC_SCRATCH_BYTES
 DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 PATHS = {"default": 0, "fused": 1, "split": 2, "split_runs": 3}
@@ -28,7 +28,7 @@ TILES = {"default": 0, "single": 1, "pair": 2, "pair_k64": 3}
 # Every function the headers under include/ declare.
 EXPORTS = ("a2av_gmm_workspace_size", "a2av_gmm_run", "a2av_gmm_read_device_status",
            "a2av_gmm_status_string", "a2av_gmm_launch_count", "a2av_gmm_run_static_scratch",
-           "a2av_gmm_run_profiled",
+           "a2av_gmm_run_profiled", "a2av_gmm_run_arrivals",
            "a2av_amp_update_scale", "a2av_found_nonfinite", "a2av_quant_reduce",
            "a2av_gmm_mx_workspace_size", "a2av_gmm_mx_run")
 
@@ -70,36 +70,50 @@ def load():
     """Load the built library (raises if it was not built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(_build.LIB):
-            raise ImportError(f"CUDA library not built: {_build.LIB} (run __graft_entry__.build())")
-        L = ctypes.CDLL(_build.LIB)
-        p, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
-        L.a2av_gmm_workspace_size.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(sz)]
-        L.a2av_gmm_workspace_size.restype = ctypes.c_int
-        L.a2av_gmm_run.argtypes = [ctypes.POINTER(Desc), p, p, p, p, p, p, p, p, p, sz, p]
-        L.a2av_gmm_run.restype = ctypes.c_int
-        L.a2av_gmm_run_profiled.argtypes = [ctypes.POINTER(Desc), p, p, p, p, p, p, p, p, p, sz, p, p, p]
-        L.a2av_gmm_run_profiled.restype = ctypes.c_int
-        L.a2av_gmm_read_device_status.argtypes = [p, p, ctypes.POINTER(i32)]
-        L.a2av_gmm_read_device_status.restype = ctypes.c_int
-        L.a2av_gmm_status_string.argtypes = [ctypes.c_int]
-        L.a2av_gmm_status_string.restype = ctypes.c_char_p
-        L.a2av_gmm_launch_count.argtypes = [ctypes.POINTER(Desc)]
-        L.a2av_gmm_launch_count.restype = i32
-        L.a2av_gmm_run_static_scratch.argtypes = [ctypes.POINTER(Desc), p, p, p, p, p, p, p, p, p]
-        L.a2av_gmm_run_static_scratch.restype = ctypes.c_int
-        L.a2av_amp_update_scale.argtypes = [p, p, p, ctypes.c_float, ctypes.c_float, i32, p]
-        L.a2av_amp_update_scale.restype = ctypes.c_int
-        L.a2av_found_nonfinite.argtypes = [p, ctypes.c_int64, i32, p, p]
-        L.a2av_found_nonfinite.restype = ctypes.c_int
-        L.a2av_quant_reduce.argtypes = [i32, ctypes.c_int64, ctypes.c_int64, i32, i32, p, p, p, i32, p]
-        L.a2av_quant_reduce.restype = ctypes.c_int
-        L.a2av_gmm_mx_workspace_size.argtypes = [ctypes.POINTER(MxDesc), ctypes.POINTER(sz)]
-        L.a2av_gmm_mx_workspace_size.restype = ctypes.c_int
-        L.a2av_gmm_mx_run.argtypes = [ctypes.POINTER(MxDesc)] + [p] * 14 + [sz, p]
-        L.a2av_gmm_mx_run.restype = ctypes.c_int
-        _lib = L
+        _lib = load_library(_build.LIB)
     return _lib
+
+
+def load_checks():
+    """The debug build with device-side bounds checks (built by build.build(checks=True)),
+    as a separate handle with the same functions."""
+    return load_library(_build.CHECKS_LIB)
+
+
+def load_library(path: str):
+    """Open one build of the library and declare every C-ABI function's signature."""
+    if not os.path.exists(path):
+        raise ImportError(f"CUDA library not built: {path} (run __graft_entry__.build())")
+    L = ctypes.CDLL(path)
+    p, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+    L.a2av_gmm_workspace_size.argtypes = [ctypes.POINTER(Desc), ctypes.POINTER(sz)]
+    L.a2av_gmm_workspace_size.restype = ctypes.c_int
+    L.a2av_gmm_run.argtypes = [ctypes.POINTER(Desc), p, p, p, p, p, p, p, p, p, sz, p]
+    L.a2av_gmm_run.restype = ctypes.c_int
+    L.a2av_gmm_run_profiled.argtypes = [ctypes.POINTER(Desc), p, p, p, p, p, p, p, p, p, sz, p, p, p]
+    L.a2av_gmm_run_profiled.restype = ctypes.c_int
+    L.a2av_gmm_run_arrivals.argtypes = [ctypes.POINTER(Desc), p, p, p, p, p, p, p, p, p, ctypes.c_uint64,
+                                        ctypes.c_uint64, p, sz, p]
+    L.a2av_gmm_run_arrivals.restype = ctypes.c_int
+    L.a2av_gmm_read_device_status.argtypes = [p, p, ctypes.POINTER(i32)]
+    L.a2av_gmm_read_device_status.restype = ctypes.c_int
+    L.a2av_gmm_status_string.argtypes = [ctypes.c_int]
+    L.a2av_gmm_status_string.restype = ctypes.c_char_p
+    L.a2av_gmm_launch_count.argtypes = [ctypes.POINTER(Desc)]
+    L.a2av_gmm_launch_count.restype = i32
+    L.a2av_gmm_run_static_scratch.argtypes = [ctypes.POINTER(Desc), p, p, p, p, p, p, p, p, p]
+    L.a2av_gmm_run_static_scratch.restype = ctypes.c_int
+    L.a2av_amp_update_scale.argtypes = [p, p, p, ctypes.c_float, ctypes.c_float, i32, p]
+    L.a2av_amp_update_scale.restype = ctypes.c_int
+    L.a2av_found_nonfinite.argtypes = [p, ctypes.c_int64, i32, p, p]
+    L.a2av_found_nonfinite.restype = ctypes.c_int
+    L.a2av_quant_reduce.argtypes = [i32, ctypes.c_int64, ctypes.c_int64, i32, i32, p, p, p, i32, p]
+    L.a2av_quant_reduce.restype = ctypes.c_int
+    L.a2av_gmm_mx_workspace_size.argtypes = [ctypes.POINTER(MxDesc), ctypes.POINTER(sz)]
+    L.a2av_gmm_mx_workspace_size.restype = ctypes.c_int
+    L.a2av_gmm_mx_run.argtypes = [ctypes.POINTER(MxDesc)] + [p] * 14 + [sz, p]
+    L.a2av_gmm_mx_run.restype = ctypes.c_int
+    return L
 
 
 def make_desc(W, e, A, H1, N1, BS=0, H2=0, N2=0, dtype=torch.bfloat16, want_permute_out=False,
@@ -154,6 +168,22 @@ def a2av_gmm_run_profiled(desc: Desc, ataOut, recvCounts, gmmWeight, mmX, mmWeig
                                       ctypes.c_void_p(gemm_begin.cuda_event), ctypes.c_void_p(gemm_end.cuda_event))
     if st != A2AV_OK:
         raise A2avError(st, "a2av_gmm_run_profiled")
+
+
+def a2av_gmm_run_arrivals(desc: Desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permuteOut, gmmY, mmY,
+                          arrived: torch.Tensor, arrival_tag: int, wait_limit_ns: int, workspace: torch.Tensor,
+                          stream=None) -> None:
+    """a2av_gmm_run that starts before the rows have all arrived: source w's rows of ataOut are
+    read once arrived[w] (an int64 device tensor of W flags) equals arrival_tag."""
+    _check(arrived, "arrived", torch.int64, 1)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = load().a2av_gmm_run_arrivals(ctypes.byref(desc), _ptr(ataOut), _ptr(recvCounts), _ptr(gmmWeight),
+                                      _ptr(mmX), _ptr(mmWeight), _ptr(permuteOut), _ptr(gmmY), _ptr(mmY),
+                                      _ptr(arrived), ctypes.c_uint64(arrival_tag & (2**64 - 1)),
+                                      ctypes.c_uint64(wait_limit_ns), _ptr(workspace), workspace.numel(),
+                                      ctypes.c_void_p(s.cuda_stream))
+    if st != A2AV_OK:
+        raise A2avError(st, "a2av_gmm_run_arrivals")
 
 
 def a2av_gmm_run_static_scratch(desc: Desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permuteOut, gmmY,

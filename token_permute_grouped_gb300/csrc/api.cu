@@ -45,17 +45,16 @@ a2av_status validate(const a2av_gmm_desc *d) {
     return A2AV_OK;
 }
 
-// Defaults follow GB300 measurements.  The permute kernel + TMA-fed GEMM
-// beats the one-kernel fused path everywhere (its row gathers cost TMA
-// instructions, the main loop's bottleneck).  Staging only the straddling
-// halves saves most of the permute traffic but makes the GEMM read colder A
-// rows; it wins only when the permute is a large share of the call (narrow
-// outputs, N1 <= 1024) and runs are long (>= 4 halves on average).
+// Default: SPLIT_RUNS.  The permute kernel stages only the 128-row halves of
+// a tile that straddle a (source, expert) segment boundary, and the GEMM
+// reads every other half in place from ataOut; which halves those are is
+// decided on the device, from recvCounts, so no host-side threshold on the
+// shapes is involved.  Measured on GB300 it matches or beats staging every
+// row (SPLIT) on all the workloads, by 16 % on the 262K-row one, and the
+// one-kernel row-gathering FUSED path everywhere.
 int resolve_path(const a2av_gmm_desc *d) {
     if (d->path != A2AV_PATH_DEFAULT) return d->path;
-    const int64_t runs = static_cast<int64_t>(d->W) * d->e;
-    if (d->N1 <= 1024 && d->A >= 512 * runs) return A2AV_PATH_SPLIT_RUNS;
-    return A2AV_PATH_SPLIT;
+    return A2AV_PATH_SPLIT_RUNS;
 }
 
 bool use_split(const a2av_gmm_desc *d) { return resolve_path(d) != A2AV_PATH_FUSED; }
@@ -229,7 +228,8 @@ namespace {
 a2av_status run_impl(const a2av_gmm_desc *desc, const void *ataOut, const int32_t *recvCounts,
                      const void *gmmWeight, const void *mmX, const void *mmWeight, void *permuteOut, void *gmmY,
                      void *mmY, void *workspace, size_t workspace_bytes, a2av_stream_t stream_handle,
-                     cudaEvent_t gemm_begin, cudaEvent_t gemm_end) {
+                     cudaEvent_t gemm_begin, cudaEvent_t gemm_end, const uint64_t *arrived = nullptr,
+                     uint64_t arrival_tag = 0, uint64_t wait_limit_ns = kWaitLimitNs) {
     const a2av_status vs = validate(desc);
     if (vs != A2AV_OK) return vs;
     const a2av_gmm_desc &d = *desc;
@@ -339,7 +339,10 @@ a2av_status run_impl(const a2av_gmm_desc *desc, const void *ataOut, const int32_
         }
     }
     g.write_status = permute_ran ? 0 : 1;
-    g.wait_limit_ns = kWaitLimitNs;
+    g.wait_limit_ns = wait_limit_ns;
+    g.arrived = arrived;
+    g.arrival_tag = arrival_tag;
+    g.shared_first = arrived != nullptr ? 1 : 0;
 
     // Persistent grid: as many CTAs (pair: clusters of two) as fit on the
     // device at once, never more than there can be tiles.
@@ -383,6 +386,21 @@ a2av_status a2av_gmm_run_profiled(const a2av_gmm_desc *desc, const void *ataOut,
     return run_impl(desc, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permuteOut, gmmY, mmY, workspace,
                     workspace_bytes, stream, static_cast<cudaEvent_t>(gemm_begin_event),
                     static_cast<cudaEvent_t>(gemm_end_event));
+}
+
+a2av_status a2av_gmm_run_arrivals(const a2av_gmm_desc *desc, const void *ataOut, const int32_t *recvCounts,
+                                  const void *gmmWeight, const void *mmX, const void *mmWeight,
+                                  void *permuteOut, void *gmmY, void *mmY, const uint64_t *arrived,
+                                  uint64_t arrival_tag, uint64_t wait_limit_ns, void *workspace,
+                                  size_t workspace_bytes, a2av_stream_t stream) {
+    if (!desc || (desc->A > 0 && !arrived)) return A2AV_ERR_NULLPTR;
+    if (desc->path != A2AV_PATH_DEFAULT && desc->path != A2AV_PATH_FUSED) return A2AV_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(arrived) & 7u) != 0) return A2AV_ERR_UNSUPPORTED;
+    a2av_gmm_desc d = *desc;
+    d.path = A2AV_PATH_FUSED;  // the GEMM reads each row where it arrived
+    return run_impl(&d, ataOut, recvCounts, gmmWeight, mmX, mmWeight, permuteOut, gmmY, mmY, workspace,
+                    workspace_bytes, stream, nullptr, nullptr, desc->A > 0 ? arrived : nullptr, arrival_tag,
+                    wait_limit_ns > 0 ? wait_limit_ns : kWaitLimitNs);
 }
 
 a2av_status a2av_gmm_run_static_scratch(const a2av_gmm_desc *desc, const void *ataOut,
@@ -431,8 +449,9 @@ a2av_status a2av_gmm_read_device_status(const void *workspace, a2av_stream_t str
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return A2AV_ERR_CUDA;
     if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return A2AV_ERR_CUDA;
     if (code) *code = word;
+    if (word & a2av::kStatusArrivalTimeout) return A2AV_ERR_ARRIVAL_TIMEOUT;
     if (word & a2av::kStatusTimeout) return A2AV_ERR_CUDA;
-    if (word & a2av::kStatusBadCounts) return A2AV_ERR_DEVICE_CHECK;
+    if (word & (a2av::kStatusBadCounts | a2av::kStatusBoundsCheck)) return A2AV_ERR_DEVICE_CHECK;
     return A2AV_OK;
 }
 
@@ -446,6 +465,7 @@ const char *a2av_gmm_status_string(a2av_status status) {
         case A2AV_ERR_CUDA: return "CUDA call failed, or a kernel gave up waiting";
         case A2AV_ERR_DEVICE_CHECK: return "recvCounts negative or not summing to A";
         case A2AV_ERR_SCRATCH_LIMIT: return "needs more scratch than the static scratch array holds";
+        case A2AV_ERR_ARRIVAL_TIMEOUT: return "a source's rows did not arrive within the wait limit";
     }
     return "unknown status";
 }

@@ -86,6 +86,7 @@ struct Control {
     int32_t abort;
     int32_t ngroups;
     int32_t total_tiles;
+    int32_t routed_tiles;
     GroupInfo g[kMaxExperts + 2];  // routed, shared, sentinel
     SegmentTable seg;
 };
@@ -143,6 +144,54 @@ __device__ __noinline__ bool wait_phase(int32_t *abort_flag, uint64_t *bar, uint
             return false;
         }
     }
+}
+
+// Arrival-driven start: bounded wait, by the whole warp, until sources
+// w0 .. w1 have all arrived (arrived[w] == tag).  The flags are written by
+// whatever moved the rows (a copy engine, a peer GPU, the host) after the
+// rows themselves, so they are read at system scope, relaxed and all in
+// flight at once, then ordered by one acquire fence; the rows are read next
+// by TMA, hence the proxy fence.  On expiry the status word gets
+// kStatusArrivalTimeout and the caller winds the kernel down.
+__device__ __noinline__ bool wait_arrivals(int32_t *abort_flag, const uint64_t *arrived, int w0, int w1,
+                                           uint64_t tag, int32_t *status, uint64_t limit_ns) {
+    const int lane = threadIdx.x & 31;
+    const auto all_arrived = [&]() {
+        bool mine = true;
+        for (int w = w0 + lane; w <= w1; w += 32) {
+            uint64_t v;
+            asm volatile("ld.relaxed.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(arrived + w) : "memory");
+            mine &= v == tag;
+        }
+        return __all_sync(0xffffffffu, mine);
+    };
+    if (!all_arrived()) {
+        const uint64_t t0 = global_timer_ns();
+        while (true) {
+            bool done = false;
+            for (int i = 0; i < 16 && !done; ++i) {
+                __nanosleep(256);
+                done = all_arrived();
+            }
+            if (done) break;
+            const bool give_up = *reinterpret_cast<volatile int32_t *>(abort_flag) ||
+                                 global_timer_ns() - t0 > limit_ns;
+            if (__any_sync(0xffffffffu, give_up)) {
+                if (lane == 0) atomicOr(status, kStatusArrivalTimeout);
+                return false;
+            }
+        }
+    }
+    asm volatile("fence.acq_rel.sys;\n\tfence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
+// Sources whose rows a routed tile half reads: expert-major rows
+// [first, min(first + 128, group end)) of one expert lie in segments
+// j * W + w0 .. j * W + w1.
+__device__ __forceinline__ int2 sources_of_rows(const SegmentTable &t, int W, int e, int32_t first, int32_t g_end) {
+    const int last = min(first + kHalfRows, g_end) - 1;
+    return make_int2(segment_of(t, W, e, first) % W, segment_of(t, W, e, last) % W);
 }
 
 // ---- cluster (CTA pair) helpers
@@ -358,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             C.g[ng] = GroupInfo{0, 0, 1, total};
             C.ngroups = ng;
             C.total_tiles = total;
+            C.routed_tiles = routed_total;
             C.abort = 0;
             if (blockIdx.x == 0) {
                 if (p.write_status) *p.status = good ? 0 : kStatusBadCounts;
@@ -396,6 +446,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
     const int total = C.total_tiles;
     const uint32_t full0 = smem_u32(&C.full[0]);
+    // Tile order: routed groups, then the shared expert.  With shared_first
+    // the shared tiles are rotated to the front (they read no exchanged
+    // rows, so they run while the routed rows are still arriving).
+    const int rot = (p.shared_first && total > C.routed_tiles) ? C.routed_tiles : 0;
+    const auto tile_at = [&](int t) {
+        int u = t + rot;
+        if (u >= total) u -= total;
+        return decode_tile(C, u);
+    };
 
     if (warp < kProducerWarps) {
         // =========================================================== producers
@@ -404,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             bool ok = true;
             bool staged_ready = !p.after_permute;  // the permute kernel's rows are visible
             for (int t = unit; t < total && ok; t += nunits) {
-                const Tile w = decode_tile(C, t);
+                const Tile w = tile_at(t);
                 const bool shared = w.g >= e;
                 const CUtensorMap *tb = shared ? &p.tmB_shared : &p.tmB_routed;
                 const CUtensorMap *tb4 = shared ? &p.tmB4_shared : &p.tmB4_routed;
@@ -437,6 +496,34 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     if (y < g_end && half_in_one_segment(C.seg, p.W, e, y, g_end)) {
                         direct = true;
                         direct_row = source_row(C.seg, p.W, e, y);
+                        // The half's rows of this group are one run of ataOut.
+                        if (!in_bounds(direct_row >= 0 && direct_row + min(BM, g_end - y) <= p.A, p.status))
+                            direct = false;
+                    }
+                }
+                if (GATHER && !shared && p.arrived != nullptr) {
+                    // Arrival-driven start: this half's rows must have
+                    // arrived from every source they come from.  (Rows past
+                    // the group's end are loaded too, but their products
+                    // are discarded.)
+                    const int g_end = C.g[w.g].row0 + C.g[w.g].rows;
+                    if (y < g_end) {
+                        const int2 ws = sources_of_rows(C.seg, p.W, e, y, g_end);
+                        if (!wait_arrivals(&C.abort, p.arrived, ws.x, ws.y, p.arrival_tag, p.status,
+                                           p.wait_limit_ns)) {
+                            // Give up: first let the MMAs release every stage
+                            // already filled (no copy left in flight), then
+                            // make every role wind down.
+                            if (lane == 0) {
+                                for (int i = 0; i < STAGES; ++i, ++it)
+                                    if (!wait_phase(&C.abort, &C.empty[it % STAGES], ((it / STAGES) & 1) ^ 1,
+                                                    p.status, p.wait_limit_ns))
+                                        break;
+                                *reinterpret_cast<volatile int32_t *>(&C.abort) = 1;
+                            }
+                            ok = false;
+                            break;
+                        }
                     }
                 }
                 int32_t src[4] = {0, 0, 0, 0};
@@ -449,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         const int d = y + 4 * lane + k;
                         const int sg = d < p.A ? segment_of(C.seg, p.W, e, d) : nseg;
                         src[k] = sg < nseg ? source_row_in(C.seg, p.W, e, sg, d) : p.A - 1;
+                        if (!in_bounds(src[k] >= 0 && src[k] < p.A, p.status)) src[k] = p.A - 1;
                         if (k == 0) seg_first = sg;
                         if (k == 3) seg_last = sg;
                     }
@@ -519,11 +607,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const uint4 *ata = static_cast<const uint4 *>(p.ataOut);
             uint4 *perm = static_cast<uint4 *>(p.permuteOut);
             for (int t = unit; t < total; t += nunits) {
-                const Tile w = decode_tile(C, t);
+                const Tile w = tile_at(t);
                 if (w.g >= e || w.n != 0) continue;
                 const int first = w.m * TILE_M + static_cast<int>(rank) * BM;  // row within the group
                 const int r_end = min(BM, C.g[w.g].rows - first);
                 const int y = C.g[w.g].row0 + first;
+                if (p.arrived != nullptr && r_end > 0) {
+                    const int2 ws = sources_of_rows(C.seg, p.W, e, y, C.g[w.g].row0 + C.g[w.g].rows);
+                    // (On expiry the producer, waiting for the same rows,
+                    // winds the kernel down.)
+                    if (!wait_arrivals(&C.abort, p.arrived, ws.x, ws.y, p.arrival_tag, p.status, p.wait_limit_ns))
+                        break;
+                }
                 for (int r = cw; r < r_end; r += kProducerWarps - 1) {
                     const int d = y + r;
                     const uint4 *in = ata + static_cast<size_t>(source_row(C.seg, p.W, e, d)) * vpr;
@@ -557,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             uint32_t it = 0, tl = 0;  // stages consumed, tiles done
             bool ok = true;
             for (int t = unit; t < total && ok; t += nunits, ++tl) {
-                const Tile w = decode_tile(C, t);
+                const Tile w = tile_at(t);
                 const bool shared = w.g >= e;
                 const int K = shared ? p.H2 : p.H1;
                 const uint32_t idesc = shared ? idesc2 : idesc1;
@@ -598,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const uint32_t tempty0 = smem_u32(&C.tempty[0]);
         uint32_t tl = 0;
         for (int t = unit; t < total; t += nunits, ++tl) {
-            const Tile w = decode_tile(C, t);
+            const Tile w = tile_at(t);
             const bool shared = w.g >= e;
             const int acc = tl & 1;
             if (!wait_phase(&C.abort, &C.tfull[acc], (tl >> 1) & 1, p.status, p.wait_limit_ns)) break;
@@ -607,7 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const int N = shared ? p.N2 : p.N1;
             const int bn = shared ? p.bn2 : p.bn1;
             const int row = w.m * TILE_M + static_cast<int>(rank) * BM + q * 32 + lane;
-            const bool valid = row < C.g[w.g].rows;
+            const bool valid = row < C.g[w.g].rows &&
+                               in_bounds(static_cast<int64_t>(shared ? row : C.g[w.g].row0 + row) <
+                                             static_cast<int64_t>(shared ? p.BS : p.A),
+                                         p.status);
             const int n0 = w.n * bn;
             const size_t out_row = static_cast<size_t>(shared ? row : C.g[w.g].row0 + row);
             uint16_t *out = static_cast<uint16_t *>(shared ? p.mmY : p.gmmY) + out_row * N + n0;

@@ -57,6 +57,12 @@ struct GemmLaunch {
                               // dependent launch); the producer waits for it before staged loads
     uint64_t wait_limit_ns;   // bound on every pipeline wait; on expiry the kernel records
                               // kStatusTimeout and winds down
+    // Arrival-driven start (fused path): the rows of source w in ataOut may
+    // be read once arrived[w] == arrival_tag; every tile that reads a
+    // source's rows waits for its flag first.  NULL: everything has arrived.
+    const uint64_t *arrived;
+    uint64_t arrival_tag;
+    int32_t shared_first;     // 1: shared-expert tiles first (they read no exchanged rows)
 };
 
 cudaError_t launch_grouped_gemm(const GemmLaunch &p, cudaStream_t stream);

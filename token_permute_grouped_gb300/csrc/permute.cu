@@ -64,7 +64,9 @@ __global__ void __launch_bounds__(kPermuteThreads)
     const int gw = blockIdx.x * kPermuteWarps + warp;
     const auto copy_piece = [&](int d, int seg, int piece) {
         const int v0 = piece * 32 * kPieceVecs + lane;
-        const uint4 *in = src + static_cast<size_t>(source_row_in(table, W, e, seg, d)) * vpr;
+        const int32_t s_row = source_row_in(table, W, e, seg, d);
+        if (!in_bounds(seg >= 0 && seg < W * e && d >= 0 && d < A && s_row >= 0 && s_row < A, status)) return;
+        const uint4 *in = src + static_cast<size_t>(s_row) * vpr;
         uint4 *out = dst + static_cast<size_t>(d) * vpr;
         uint4 r[kPieceVecs];
 #pragma unroll

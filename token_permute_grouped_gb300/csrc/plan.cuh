@@ -15,8 +15,23 @@ constexpr int kMaxSegments = 256;  // W * e <= 256
 constexpr int kMaxExperts = 32;    // e <= 32
 
 // Device status word bits (written into the workspace).
-constexpr int32_t kStatusBadCounts = 1;  // a negative count, or sum != A
-constexpr int32_t kStatusTimeout = 2;    // a pipeline wait gave up
+constexpr int32_t kStatusBadCounts = 1;    // a negative count, or sum != A
+constexpr int32_t kStatusTimeout = 2;      // a pipeline wait gave up
+constexpr int32_t kStatusBoundsCheck = 4;  // a debug build (A2AV_CHECKS) found an index out of range
+constexpr int32_t kStatusArrivalTimeout = 8;  // a source's rows did not arrive within the wait limit
+
+// Debug builds (-DA2AV_CHECKS) check segment indices and row coordinates on
+// the device before they are used: a failed check sets kStatusBoundsCheck
+// in the status word and the access is skipped (nothing traps).  Other
+// builds compile the checks away.
+#ifdef A2AV_CHECKS
+__device__ __forceinline__ bool in_bounds(bool ok, int32_t *status) {
+    if (!ok) atomicOr(status, kStatusBoundsCheck);
+    return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(bool, int32_t *) { return true; }
+#endif
 
 struct SegmentTable {
     int32_t src[kMaxSegments];      // rank-major index -> first ataOut row
