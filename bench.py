@@ -21,6 +21,7 @@ Other measurements (one JSON line each):
     --op qreduce   the dequantising rank reduce [--qworkload NAME]
     --op layer     AlltoAllv (NCCL) + the hot path, per rank [--overlap]
     --op mx        the hot path with block-scaled FP8 operands [--mx-qtype]
+    --op arrivals  rows landing source by source while the kernel runs (one GPU)
 """
 
 from __future__ import annotations
@@ -836,6 +837,112 @@ def run_layer(args):
     barrier(world)
 
 
+# ------------------------------------- arrival-driven start (emulated exchange)
+
+ARR_METRIC = ("AlltoAllv landing + permute+grouped-GEMM TFLOP/s per step, rows arriving while the kernel runs "
+              "(exchange emulated by host-to-device copies); us per step")
+
+
+def run_arrivals(args):
+    """One GPU: each step's received rows land in ataOut source by source (copies from pinned host
+    memory on a side stream, each followed by its source's flag) while a2av_gmm_run_arrivals runs on
+    the compute stream; beside it, the same step in sequence (all rows copied, then the default call)."""
+    world, rank, local = dist_env()
+    assert torch.cuda.is_available(), "bench.py needs a GPU"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    binding.load()
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl, seed=0, rank=rank)
+    A, dt = inp.A, wl.torch_dtype
+    per_source = inp.recvCounts.reshape(wl.W, wl.e).astype(np.int64).sum(1)
+    ends = np.cumsum(per_source)
+    spans = [(int(b), int(t)) for b, t in zip(ends - per_source, ends)]
+    host = inp.ataOut.pin_memory()
+    ata = torch.empty(A, wl.H1, dtype=dt, device=dev)
+    rc = torch.from_numpy(inp.recvCounts).to(dev)
+    gw = inp.gmmWeight.to(dev)
+    mmX = inp.mmX.to(dev) if wl.BS else None
+    mmW = inp.mmWeight.to(dev) if wl.BS else None
+    y = torch.empty(A, wl.N1, dtype=dt, device=dev)
+    my = torch.empty(wl.BS, wl.N2, dtype=dt, device=dev) if wl.BS else None
+    arrived = torch.zeros(wl.W, dtype=torch.int64, device=dev)
+    n_all = args.warmup + args.steps
+    tags = torch.arange(1, 2 * n_all + 1, dtype=torch.int64).mul_(0x9E3779B9).pin_memory()
+    desc = binding.make_desc(wl.W, wl.e, A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, dt, path="fused")
+    ws = torch.empty(binding.a2av_gmm_workspace_size(desc), dtype=torch.uint8, device=dev)
+    plan = binding.Plan(wl.W, wl.e, A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, dt, device=dev)
+    main = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
+    done = [torch.cuda.Event() for _ in range(2)]
+    landed = torch.cuda.Event()
+
+    def land(i, flags):
+        # the exchange's rows for step i, source by source; each source's flag after its rows
+        with torch.cuda.stream(side):
+            side.wait_event(done[(i - 1) % 2])  # the previous step has read ataOut
+            for w, (b, t) in enumerate(spans):
+                if t > b:
+                    ata[b:t].copy_(host[b:t], non_blocking=True)
+                if flags:
+                    arrived[w:w + 1].copy_(tags[i:i + 1], non_blocking=True)
+            landed.record(side)
+
+    def overlapped(i):
+        land(i, True)
+        binding.a2av_gmm_run_arrivals(desc, ata, rc, gw, mmX, mmW, None, y, my, arrived, int(tags[i]), 0, ws,
+                                      stream=main)
+        done[i % 2].record(main)
+
+    def sequential(i):
+        land(i, False)
+        main.wait_event(landed)
+        plan.run(ata, rc, gw, mmX, mmW, gmmY=y, mmY=my, stream=main)
+        done[i % 2].record(main)
+
+    sync = torch.cuda.synchronize
+    for i in range(2):
+        done[i].record(main)
+    res = {}
+    for name, fn, base in (("overlapped", overlapped, 0), ("sequential", sequential, n_all)):
+        for i in range(args.warmup):
+            fn(base + i)
+        sync()
+        with ClockSampler(local) as clocks:
+            dt_s, _ = timed_region(lambda i: fn(base + args.warmup + i), args.steps, world, dev, sync)
+        res[name] = (dt_s, clocks.summary())
+    st, code = binding.a2av_gmm_read_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({code})")
+    flops = flops_of(wl, A)
+    h2d = sum(t - b for b, t in spans) * wl.H1 * 2 + wl.W * 8
+    ov, sq = res["overlapped"][0] / args.steps, res["sequential"][0] / args.steps
+    pk, pk_kind = peaks()
+    emit({
+        "metric": ARR_METRIC, "value": round(flops / ov / 1e12, 2), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ov * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded routing and N(0,1) tensors; no dataset)",
+        "config": {"workload": wl.name, "W": wl.W, "e": wl.e, "A": A, "H1": wl.H1, "N1": wl.N1, "BS": wl.BS,
+                   "H2": wl.H2, "N2": wl.N2, "dtype": wl.dtype,
+                   "exchange": "rows of each source copied host-to-device from pinned memory on a side stream, "
+                               "then that source's 8-byte flag",
+                   "l2": "ataOut rewritten by the copies every step"},
+        "timing": {"us_per_step_overlapped": round(ov * 1e6, 2), "us_per_step_sequential": round(sq * 1e6, 2),
+                   "sequential": "all rows copied, then the default call (split_runs)",
+                   "overlapped": "a2av_gmm_run_arrivals (fused path) launched beside the copies",
+                   "h2d_bytes_per_step": int(h2d), "h2d_gbs_overlapped": round(h2d / ov / 1e9, 1)},
+        "roofline": {"bound": "hbm", "achieved": round(h2d / ov / 1e9, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": None, "traffic": None,
+                     "note": "bound by the host-to-device link, not by HBM or the tensor cores"},
+        "e2e": {"value": round(flops / ov / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": args.steps,
+        "clocks": res["overlapped"][1],
+    })
+
+
 # ------------------------------------------------ block-scaled FP8 (mx) GEMM
 
 MX_METRIC = "mx (block-scaled FP8) permute+grouped-GEMM TFLOP/s, % of GB300 FP8 dense peak; us per call"
@@ -1085,7 +1192,7 @@ def main(argv=None):
     ap.add_argument("--sim-rank", type=int, default=None,
                     help="N=1: time the inputs of this expert-parallel rank of the workload (default: rank 0)")
     ap.add_argument("--mx-qtype", default="e4m3fn", choices=["e4m3fn", "e5m2"], help="--op mx: code format")
-    ap.add_argument("--op", default="gemm", choices=["gemm", "amp", "qreduce", "layer", "mx"],
+    ap.add_argument("--op", default="gemm", choices=["gemm", "amp", "qreduce", "layer", "mx", "arrivals"],
                     help="gemm: the hot path (default); amp: the loss-scale step; qreduce: the quantised "
                          "rank reduce; layer: AlltoAllv + the hot path; mx: the hot path in block-scaled FP8")
     ap.add_argument("--overlap", action="store_true",
@@ -1102,6 +1209,8 @@ def main(argv=None):
         run_layer(args)
     elif args.op == "mx":
         run_mx(args)
+    elif args.op == "arrivals":
+        run_arrivals(args)
     elif args.impl == "reference":
         run_reference(args)
     elif args.op == "amp":
