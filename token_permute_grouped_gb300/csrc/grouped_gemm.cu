@@ -76,6 +76,12 @@ struct GroupInfo {
     int32_t tile_start;  // first linear tile of this group
 };
 
+// Arrival-driven start: the routed row tiles (each with all its column tiles)
+// are taken in the order of the latest source their rows come from, so the
+// units work on tiles whose rows have arrived while later sources are still
+// landing.  Up to kMaxOrder row tiles; beyond that, group order.
+constexpr int kMaxOrder = 2048;
+
 template <int STAGES>
 struct Control {
     uint64_t full[STAGES];     // A and B of a stage landed (pair: in both CTAs; used in the even CTA)
@@ -89,6 +95,8 @@ struct Control {
     int32_t routed_tiles;
     GroupInfo g[kMaxExperts + 2];  // routed, shared, sentinel
     SegmentTable seg;
+    int32_t order_n;               // row tiles in `order` (0: group order)
+    uint16_t order[kMaxOrder];     // routed row tiles by latest source (arrival-driven start)
 };
 
 template <bool PAIR, int CH>
@@ -167,10 +175,12 @@ __device__ __noinline__ bool wait_arrivals(int32_t *abort_flag, const uint64_t *
     };
     if (!all_arrived()) {
         const uint64_t t0 = global_timer_ns();
+        uint32_t pause = 256;  // backs off to 4 us: many CTAs poll while the rows stream in
         while (true) {
             bool done = false;
-            for (int i = 0; i < 16 && !done; ++i) {
-                __nanosleep(256);
+            for (int i = 0; i < 8 && !done; ++i) {
+                __nanosleep(pause);
+                pause = min(2u * pause, 4096u);
                 done = all_arrived();
             }
             if (done) break;
@@ -409,10 +419,62 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             C.total_tiles = total;
             C.routed_tiles = routed_total;
             C.abort = 0;
+            C.order_n = 0;
             if (blockIdx.x == 0) {
                 if (p.write_status) *p.status = good ? 0 : kStatusBadCounts;
                 else if (!good) atomicOr(p.status, kStatusBadCounts);
             }
+        }
+        __syncwarp();
+        const int total_m = tn1 > 0 ? routed_total / tn1 : 0;  // routed row tiles
+        if (p.arrived != nullptr && good && total_m > 0 && total_m <= kMaxOrder) {
+            // Stable counting sort of the row tiles by the latest source of
+            // their rows (C.seg.tmp is free after the scan: the histogram).
+            int32_t *base = C.seg.tmp;
+            for (int w = lane; w < p.W; w += 32) base[w] = 0;
+            __syncwarp();
+            // key: the source of the tile's last row that belongs to its group
+            const auto key_of = [&](int mt) {
+                int g = 0;
+                while (mt >= C.g[g + 1].tile_start / tn1) ++g;
+                const int m = mt - C.g[g].tile_start / tn1;
+                const int g_end = C.g[g].row0 + C.g[g].rows;
+                const int last = min(C.g[g].row0 + (m + 1) * TILE_M, g_end) - 1;
+                return segment_of(C.seg, p.W, e, last) % p.W;
+            };
+            for (int mt0 = 0; mt0 < total_m; mt0 += 32) {
+                const int mt = mt0 + lane;
+                const int k = mt < total_m ? key_of(mt) : p.W;  // p.W: no tile
+                const uint32_t same = __match_any_sync(0xffffffffu, k);
+                if (k < p.W && (same & ((1u << lane) - 1u)) == 0) base[k] += __popc(same);
+                __syncwarp();
+            }
+            // exclusive prefix over the sources (base[] -> first slot of each key)
+            int run = 0;
+            for (int w0 = 0; w0 < p.W; w0 += 32) {
+                const int w = w0 + lane;
+                const int c = w < p.W ? base[w] : 0;
+                int inc = c;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, inc, off);
+                    if (lane >= off) inc += v;
+                }
+                if (w < p.W) base[w] = run + inc - c;
+                run += __shfl_sync(0xffffffffu, inc, 31);
+                __syncwarp();
+            }
+            for (int mt0 = 0; mt0 < total_m; mt0 += 32) {
+                const int mt = mt0 + lane;
+                const int k = mt < total_m ? key_of(mt) : p.W;
+                const uint32_t same = __match_any_sync(0xffffffffu, k);
+                const uint32_t before = same & ((1u << lane) - 1u);
+                if (k < p.W) C.order[base[k] + __popc(before)] = static_cast<uint16_t>(mt);
+                __syncwarp();
+                if (k < p.W && before == 0) base[k] += __popc(same);
+                __syncwarp();
+            }
+            if (lane == 0) C.order_n = total_m;
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -450,9 +512,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     // the shared tiles are rotated to the front (they read no exchanged
     // rows, so they run while the routed rows are still arriving).
     const int rot = (p.shared_first && total > C.routed_tiles) ? C.routed_tiles : 0;
+    const int tn_routed = (p.N1 + p.bn1 - 1) / p.bn1;
     const auto tile_at = [&](int t) {
         int u = t + rot;
         if (u >= total) u -= total;
+        if (u < C.routed_tiles && C.order_n > 0) {  // arrival order of the routed row tiles
+            const int mt = C.order[u / tn_routed];
+            int g = 0;
+            while (mt >= C.g[g + 1].tile_start / tn_routed) ++g;
+            return Tile{g, mt - C.g[g].tile_start / tn_routed, u % tn_routed};
+        }
         return decode_tile(C, u);
     };
 
