@@ -45,7 +45,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 from token_permute_grouped_gb300 import binding, build  # noqa: E402
-from token_permute_grouped_gb300.workloads import HEADLINE, WORKLOADS, make_inputs  # noqa: E402
+from token_permute_grouped_gb300.workloads import HEADLINE, SMALL, W8E4, WORKLOADS, make_inputs  # noqa: E402
 
 METRIC = "permute+grouped-GEMM TFLOP/s, % of GB300 bf16 dense peak; us per call"
 L2_BYTES = 129 * 2**20
@@ -473,8 +473,21 @@ def oracle_sample(wl, inp, seconds, seed=0):
 
 def cpu_baseline(wl, inp, seconds):
     flops, el, rows, threads, desc = oracle_sample(wl, inp, seconds)
-    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+    line = {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": desc, "seconds": round(el, 2)}
+    if wl.name in (SMALL, W8E4):
+        # The same oracle on one core, beside all of them.
+        import oracle
+        orc = oracle.Oracle()
+        all_threads = orc.num_threads()
+        orc.set_threads(1)
+        try:
+            f1, el1, _, _, desc1 = oracle_sample(wl, inp, seconds / 3, seed=1)
+        finally:
+            orc.set_threads(all_threads)
+        line["one_thread"] = {"value": round(f1 / el1 / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "sample": desc1,
+                              "seconds": round(el1, 2)}
+    return line
 
 
 def run_reference(args):

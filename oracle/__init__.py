@@ -56,13 +56,14 @@ def _declare(lib):
     lib.a2av_ref_grouped_matmul.argtypes = [i32, p, i64, i64, i64, i32, p, p, p, i64, p]
     lib.a2av_ref_matmul.argtypes = [i64, i64, i64, i32, p, p, p, i64, p]
     lib.a2av_ref_num_threads.argtypes = []
+    lib.a2av_ref_set_threads.argtypes = [ctypes.c_int]
     lib.a2av_ref_amp_update_scale.argtypes = [p, p, ctypes.c_float, ctypes.c_float, ctypes.c_float, i32]
     lib.a2av_ref_any_nonfinite.argtypes = [ctypes.c_int, p, i64, p]
     lib.a2av_ref_decode8.argtypes = [ctypes.c_int, p, i64, p]
     lib.a2av_ref_quant_reduce.argtypes = [i32, i64, i64, i32, i32, p, p, p]
     lib.a2av_ref_mx_grouped_matmul.argtypes = [i32, p, i64, i64, i64, i32, i32, p, p, p, p, p, i64, p]
     for f in ("a2av_ref_decode", "a2av_ref_plan", "a2av_ref_permute",
-              "a2av_ref_grouped_matmul", "a2av_ref_matmul", "a2av_ref_num_threads",
+              "a2av_ref_grouped_matmul", "a2av_ref_matmul", "a2av_ref_num_threads", "a2av_ref_set_threads",
               "a2av_ref_amp_update_scale", "a2av_ref_any_nonfinite", "a2av_ref_decode8",
               "a2av_ref_quant_reduce", "a2av_ref_mx_grouped_matmul"):
         getattr(lib, f).restype = ctypes.c_int
@@ -112,6 +113,10 @@ class Oracle:
 
     def num_threads(self) -> int:
         return int(self.L.a2av_ref_num_threads())
+
+    def set_threads(self, n: int) -> int:
+        """OpenMP threads for the following calls (results do not depend on it)."""
+        return int(self.L.a2av_ref_set_threads(n))
 
     def decode(self, t: torch.Tensor) -> np.ndarray:
         b = _bits(t).reshape(-1)

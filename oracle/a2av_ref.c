@@ -307,6 +307,21 @@ int a2av_ref_matmul(int64_t BS, int64_t H2, int64_t N2, int32_t dtype,
 }
 
 /* Threads the product loops use (the CPU baseline reports it). */
+/* Threads the OpenMP loops use from here on (n >= 1); the results do not
+ * depend on it: every output row is one sequential float64 sum.  Returns the
+ * new count.  (For timing the oracle on one core beside all of them.) */
+int a2av_ref_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
 int a2av_ref_num_threads(void)
 {
 #ifdef _OPENMP
