@@ -53,12 +53,12 @@ def _source_spans(inp):
     return [(int(b), int(t)) for b, t in zip(ends - per_source, ends)]
 
 
-def _setup(inp, want_perm):
+def _setup(inp, want_perm, tiles="default"):
     wl = inp.wl
     dev = torch.device("cuda:0")
     dt = wl.torch_dtype
     d = binding.make_desc(wl.W, wl.e, inp.A, wl.H1, wl.N1, wl.BS, wl.H2, wl.N2, dt,
-                          want_permute_out=want_perm, path="fused")
+                          want_permute_out=want_perm, path="fused", tiles=tiles)
     t = dict(
         ata=torch.empty(inp.A, wl.H1, dtype=dt, device=dev),
         rc=torch.from_numpy(inp.recvCounts).to(dev),
@@ -101,11 +101,31 @@ def _exchange(inp, t, bufs, order, skip=None):
     return side
 
 
+# The kernel takes the routed row tiles in the order of the latest source
+# their rows come from (up to 2048 row tiles; beyond that, group order):
+# both orders, single-CTA and pair tiles.
+CASES = {
+    "bf16": lambda: _case("bf16"),
+    "fp16": lambda: _case("fp16"),
+    # 32 experts of about 8,800 rows: 128-row tiles on one CTA give more than
+    # 2048 row tiles (group order), 256-row pair tiles fewer (arrival order).
+    "over_order_capacity": lambda: custom_inputs(4, 32, 128, 128, [2000 + (i * 37) % 400 for i in range(128)],
+                                                 "bf16", 256, 128, 128, seed=34),
+}
+
+
+def test_order_capacity_case_spans_both_orders():
+    rc = np.array([2000 + (i * 37) % 400 for i in range(128)]).reshape(4, 32).sum(0)
+    assert sum(-(-int(g) // 128) for g in rc) > 2048
+    assert sum(-(-int(g) // 256) for g in rc) <= 2048
+
+
 @pytest.mark.parametrize("want_perm", [False, True])
-@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-def test_rows_arriving_during_the_kernel(orc, dtype, want_perm):
-    inp = _case(dtype)
-    d, t = _setup(inp, want_perm)
+@pytest.mark.parametrize("tiles", ["pair", "single"])
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_rows_arriving_during_the_kernel(orc, case, tiles, want_perm):
+    inp = CASES[case]()
+    d, t = _setup(inp, want_perm, tiles)
     tag = int(np.random.default_rng(7).integers(1, 2**62))
     bufs = _exchange_buffers(inp, tag)
     torch.cuda.synchronize()
@@ -121,7 +141,7 @@ def test_rows_arriving_during_the_kernel(orc, dtype, want_perm):
     check_full(orc, inp, y, m, perm)
     # The same bits as the ordinary call of the fused path on the arrived rows.
     plan = binding.Plan(inp.wl.W, inp.wl.e, inp.A, inp.wl.H1, inp.wl.N1, inp.wl.BS, inp.wl.H2, inp.wl.N2,
-                        inp.wl.torch_dtype, path="fused")
+                        inp.wl.torch_dtype, path="fused", tiles=tiles)
     y2, m2, _ = plan.run(t["ata"], t["rc"], t["gw"], t["mmX"], t["mmW"])
     torch.cuda.synchronize()
     assert_bits_equal(y, y2.cpu(), "gmmY")
