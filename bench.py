@@ -130,35 +130,43 @@ def profiled_traffic(workload, permute_out=False, path="default", tiles="default
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    """nvidia-smi clocks, power and throttle reasons, sampled every 20 ms while
+    the block runs.  timed_region() marks the timed calls' wall-clock window
+    on the active sampler, and summary() reports the samples that fell inside
+    those windows (those around them only when none did, and says so)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
+    active = None
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time when read, csv line)
+        self.windows = []
         self.thread = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
             self.proc = None
         time.sleep(0.25)
+        ClockSampler.active = self
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
     def __exit__(self, *exc):
+        ClockSampler.active = None
         if self.proc is not None:
             time.sleep(0.15)
             self.proc.terminate()
@@ -168,10 +176,13 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=2)
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def _parse(self, lines):
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        sm, pw, mx, reasons = [], [], None, set()
+        for _, line in lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -180,13 +191,33 @@ class ClockSampler:
                 mx = float(parts[2])
             except ValueError:
                 continue
+            try:
+                pw.append(float(parts[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+        return sm, pw, mx, reasons
+
+    def summary(self):
+        # A line is read a moment after nvidia-smi took the sample: allow one
+        # period of slack at the end of each window.
+        slack = self.PERIOD_MS / 1e3
+        inside = [x for x in self.lines if any(t0 <= x[0] <= t1 + slack for t0, t1 in self.windows)]
+        sm, pw, mx, reasons = self._parse(inside)
+        basis = "samples taken during the timed calls"
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+            sm, pw, mx, reasons = self._parse(self.lines)
+            span = sum(t1 - t0 for t0, t1 in self.windows) * 1e3
+            basis = f"no sample fell inside the timed calls ({span:.0f} ms): samples around them"
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "samples_total": len(self.lines), "basis": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_mhz_min": min(sm), "sm_max_mhz": mx,
+                "power_w_median": statistics.median(pw) if pw else None, "reasons": sorted(reasons),
+                "samples": len(sm), "samples_total": len(self.lines), "period_ms": self.PERIOD_MS,
+                "basis": basis}
 
 
 # ------------------------------------------------------------ distributed glue
@@ -230,11 +261,15 @@ def timed_region(step, steps, world, device, sync):
     barrier(world)
     sync()
     t0 = time.perf_counter()
+    w0 = time.time()
     for i in range(steps):
         step(i)
     sync()
+    w1 = time.time()
     barrier(world)
     dt = time.perf_counter() - t0
+    if ClockSampler.active is not None:
+        ClockSampler.active.mark(w0, w1)
     return dt, reduce_max(dt, world, device)
 
 
@@ -371,6 +406,28 @@ def run_gpu(args):
     _, e2e_max = timed_region(e2e_step, e2e_steps, world, dev, sync)
     e2e_tflops = reduce_sum(flops * e2e_steps, world, dev) / e2e_max / 1e12
 
+    # Sustained: the same call back to back for about --sustained-s seconds
+    # (power draw settles and the 1.4 kW cap may lower the SM clock), timed
+    # as a whole with two events; reported beside the burst figures above.
+    sustained = None
+    if args.sustained_s > 0:
+        n_sus = max(args.steps, int(args.sustained_s * 1e3 / max(ms_per_step, 1e-3)))
+        sus_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+
+        def sus_step(i):
+            if i == 0:
+                sus_ev[0].record(stream)
+            step(i)
+            if i == n_sus - 1:
+                sus_ev[1].record(stream)
+
+        with ClockSampler(local) as sus_clocks:
+            timed_region(sus_step, n_sus, world, dev, sync)
+        sus_s = reduce_max(sus_ev[0].elapsed_time(sus_ev[1]) / 1e3, world, dev)
+        sustained = {"calls": n_sus, "us_per_call": round(sus_s * 1e6 / n_sus, 2),
+                     "tflops": round(reduce_sum(flops * n_sus, world, dev) / sus_s / 1e12, 2),
+                     "clocks": sus_clocks.summary()}
+
     if rank != 0:
         barrier(world)
         return
@@ -429,6 +486,11 @@ def run_gpu(args):
         "gpu_launches": launches_per_call * args.steps,
         "clocks": clocks.summary(),
     }
+    if sustained is not None:
+        sustained["frac_of_bf16_sustained"] = round(sustained["tflops"] / world / pk["bf16_tflops_sustained"], 4)
+        sustained["timed"] = ("the same call back to back, outside the K timed steps; CUDA events around the "
+                              "whole run; peak: MEASURED_PEAKS.json bf16_tflops_sustained")
+        line["sustained"] = sustained
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
     emit(line)
@@ -1050,10 +1112,11 @@ def run_mx(args):
     rc_dev = torch.from_numpy(inp.recvCounts).to(dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
+    def step(i, gemm_events=None):
         st = sets[i % reps]
         plan.run(st["ataOut_q"], st["ataOut_s"], rc_dev, st["gmmWeight_q"], st["gmmWeight_s"], st["mmX_q"],
-                 st["mmX_s"], st["mmWeight_q"], st["mmWeight_s"], gmmY=st["gmmY"], mmY=st["mmY"], stream=stream)
+                 st["mmX_s"], st["mmWeight_q"], st["mmWeight_s"], gmmY=st["gmmY"], mmY=st["mmY"], stream=stream,
+                 gemm_events=gemm_events)
 
     sync = torch.cuda.synchronize
     for i in range(args.warmup):
@@ -1077,6 +1140,13 @@ def run_mx(args):
     dev_s_max = reduce_max(dev_s, world, dev)
     flops = flops_of(wl, A)
     tflops = reduce_sum(flops * args.steps, world, dev) / dev_s_max / 1e12
+
+    # The dominant kernel alone, as in the bf16 line: K more calls through
+    # a2av_gmm_mx_run_profiled, whose events sit right around the GEMM.
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    timed_region(lambda i: step(i, gev[i]), args.steps, world, dev, sync)
+    gemm_ms = [b.elapsed_time(e) for b, e in gev]
 
     # End to end through the same call: codes and scales of this step's
     # activations (and recvCounts, mmX) in from pinned memory, the bf16
@@ -1132,7 +1202,10 @@ def run_mx(args):
         return
     pk, pk_kind = peaks()
     peak = 2.0 * pk["bf16_tflops"]  # FP8 dense = 2x bf16 dense (nominal 4.5 vs 2.25 PFLOP/s)
-    achieved = flops / (dev_s / args.steps) / 1e12
+    gemm_s = statistics.fmean(gemm_ms) / 1e3
+    achieved = flops / gemm_s / 1e12
+    whole = flops / (dev_s / args.steps) / 1e12
+    launches = 2 if (A or wl.BS) else 0  # the prep kernel (codes and scale atoms), then the GEMM
     line = {
         "metric": MX_METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dev_s_max * 1e3 / args.steps, 4), "higher_is_better": True,
@@ -1141,24 +1214,34 @@ def run_mx(args):
         "config": {"workload": wl.name + "_mx_" + args.mx_qtype, "tiles": mx_tiles, "W": wl.W, "e": wl.e, "A": A,
                    "H1": wl.H1,
                    "N1": wl.N1, "BS": wl.BS, "H2": wl.H2, "N2": wl.N2, "accumulate": "fp32", "out": "bf16",
-                   "us_per_call_median": round(statistics.median(per_call_ms) * 1e3, 2),
-                   "pct_of_fp8_peak": round(100 * tflops / world / peak, 2),
-                   "gflop_per_call": round(flops / 1e9, 3),
-                   "l2": f"inputs rotated over {reps} replicas ({reps * nbytes / 2**20:.0f} MiB > 129 MiB L2)",
-                   "launches_per_call": 3 if A else 1},
+                   "l2": f"inputs rotated over {reps} replicas ({reps * nbytes / 2**20:.0f} MiB > 129 MiB L2)"},
+        "timing": {
+            "us_per_call_median": round(statistics.median(per_call_ms) * 1e3, 2),
+            "us_per_call_min": round(min(per_call_ms) * 1e3, 2),
+            "us_per_call_p90": round(float(np.percentile(per_call_ms, 90)) * 1e3, 2),
+            "gemm_kernel_us_mean": round(gemm_s * 1e6, 2),
+            "gemm_kernel_us_p90": round(float(np.percentile(gemm_ms, 90)) * 1e3, 2),
+            "pct_of_fp8_peak": round(100 * tflops / world / peak, 2),
+            "gflop_per_call": round(flops / 1e9, 3),
+            "launches_per_call": launches,
+        },
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(wl.name + "_mx_" + args.mx_qtype, tiles=mx_tiles,
                                                  kernel="grouped_gemm_mx_kernel"),
                      "kernel": "grouped_gemm_mx_kernel",
-                     "timed": "whole call (CUDA events on the launching stream; the permute kernel included)",
+                     "timed": ("the GEMM kernel alone: CUDA events recorded on its launching stream right before "
+                               f"and after it, mean of {args.steps} launches (a2av_gmm_mx_run_profiled)"),
+                     "whole_call": {"achieved": round(whole, 2), "frac": round(whole / peak, 4),
+                                    "timed": "scan + prep (codes and scale atoms) + GEMM, CUDA events around each call"},
                      "peak_source": f"2 x {pk_kind} bf16 dense burst (nominal FP8:bf16 ratio 4.5:2.25)",
+                     "algorithmic_flops_per_launch": flops,
                      "algorithmic_bytes": nbytes},
         "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
                 "inputs_copied": "activation codes and scales, recvCounts, mmX codes and scales (weights resident)",
                 "overlap": "step i+1's H2D and step i's D2H run on copy streams beside step i's kernels"},
-        "gpu_launches": (3 if A else 1) * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks.summary(),
     }
     if not args.no_cpu_baseline:
@@ -1213,6 +1296,8 @@ def main(argv=None):
     ap.add_argument("--qworkload", default="qreduce_mx_e4m3_w8_rows1536_h7168",
                     help="workload of --op qreduce")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sustained-s", type=float, default=1.0,
+                    help="seconds of back-to-back calls for the sustained figures (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps

@@ -72,6 +72,22 @@ a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, 
                             void *permuteOut_q, void *permuteOut_s, void *gmmY, void *mmY, void *workspace,
                             size_t workspace_bytes, a2av_stream_t stream);
 
+/*
+ * Diagnostic form of a2av_gmm_mx_run for measurement, as a2av_gmm_run_profiled
+ * is for the bf16 call: the same work, plus two CUDA events (cudaEvent_t,
+ * created by the caller) recorded on `stream` right before and right after
+ * the grouped-GEMM kernel, which then follows the prep kernel in plain
+ * stream order.  Returns A2AV_ERR_NULLPTR when either event is NULL, else as
+ * a2av_gmm_mx_run.
+ */
+a2av_status a2av_gmm_mx_run_profiled(const a2av_gmm_mx_desc *desc, const void *ataOut_q, const void *ataOut_s,
+                                     const int32_t *recvCounts, const void *gmmWeight_q,
+                                     const void *gmmWeight_s, const void *mmX_q, const void *mmX_s,
+                                     const void *mmWeight_q, const void *mmWeight_s, void *permuteOut_q,
+                                     void *permuteOut_s, void *gmmY, void *mmY, void *workspace,
+                                     size_t workspace_bytes, a2av_stream_t stream, void *gemm_begin_event,
+                                     void *gemm_end_event);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,7 @@ EXPORTS = ("a2av_gmm_workspace_size", "a2av_gmm_run", "a2av_gmm_read_device_stat
            "a2av_gmm_status_string", "a2av_gmm_launch_count", "a2av_gmm_run_static_scratch",
            "a2av_gmm_run_profiled", "a2av_gmm_run_arrivals",
            "a2av_amp_update_scale", "a2av_found_nonfinite", "a2av_quant_reduce",
-           "a2av_gmm_mx_workspace_size", "a2av_gmm_mx_run")
+           "a2av_gmm_mx_workspace_size", "a2av_gmm_mx_run", "a2av_gmm_mx_run_profiled")
 
 # a2av_qtype / a2av_qmode of include/a2av_quant_reduce.h.
 QTYPES = {"e4m3fn": 0, "e5m2": 1, "int8": 2}
@@ -113,6 +113,8 @@ def load_library(path: str):
     L.a2av_gmm_mx_workspace_size.restype = ctypes.c_int
     L.a2av_gmm_mx_run.argtypes = [ctypes.POINTER(MxDesc)] + [p] * 14 + [sz, p]
     L.a2av_gmm_mx_run.restype = ctypes.c_int
+    L.a2av_gmm_mx_run_profiled.argtypes = [ctypes.POINTER(MxDesc)] + [p] * 14 + [sz, p, p, p]
+    L.a2av_gmm_mx_run_profiled.restype = ctypes.c_int
     return L
 
 
@@ -340,8 +342,10 @@ class MxPlan:
 
     def run(self, ataOut_q, ataOut_s, recvCounts, gmmWeight_q, gmmWeight_s, mmX_q=None, mmX_s=None,
             mmWeight_q=None, mmWeight_s=None, gmmY=None, mmY=None, permuteOut_q=None, permuteOut_s=None,
-            stream=None):
-        """Returns (gmmY, mmY, permuteOut_q, permuteOut_s); outputs are bf16."""
+            stream=None, gemm_events=None):
+        """Returns (gmmY, mmY, permuteOut_q, permuteOut_s); outputs are bf16.
+        gemm_events: optional (begin, end) timing events recorded around the
+        GEMM kernel (a2av_gmm_mx_run_profiled)."""
         d = self.desc
         for t, name in ((ataOut_q, "ataOut_q"), (ataOut_s, "ataOut_s")):
             if d.A:
@@ -367,13 +371,23 @@ class MxPlan:
             if mmY is None:
                 mmY = torch.empty(d.BS, d.N2, dtype=torch.bfloat16, device=self.device)
         s = stream if stream is not None else torch.cuda.current_stream()
-        st = load().a2av_gmm_mx_run(
-            ctypes.byref(d), _ptr(ataOut_q) if d.A else None, _ptr(ataOut_s) if d.A else None, _ptr(recvCounts),
-            _ptr(gmmWeight_q), _ptr(gmmWeight_s), _ptr(mmX_q) if d.BS else None, _ptr(mmX_s) if d.BS else None,
-            _ptr(mmWeight_q) if d.BS else None, _ptr(mmWeight_s) if d.BS else None,
-            _ptr(permuteOut_q) if d.want_permute_out else None, _ptr(permuteOut_s) if d.want_permute_out else None,
-            _ptr(gmmY) if d.A else None, _ptr(mmY) if d.BS else None, _ptr(self.workspace), self.workspace.numel(),
-            ctypes.c_void_p(s.cuda_stream))
+        args = (ctypes.byref(d), _ptr(ataOut_q) if d.A else None, _ptr(ataOut_s) if d.A else None,
+                _ptr(recvCounts), _ptr(gmmWeight_q), _ptr(gmmWeight_s), _ptr(mmX_q) if d.BS else None,
+                _ptr(mmX_s) if d.BS else None, _ptr(mmWeight_q) if d.BS else None,
+                _ptr(mmWeight_s) if d.BS else None, _ptr(permuteOut_q) if d.want_permute_out else None,
+                _ptr(permuteOut_s) if d.want_permute_out else None, _ptr(gmmY) if d.A else None,
+                _ptr(mmY) if d.BS else None, _ptr(self.workspace), self.workspace.numel(),
+                ctypes.c_void_p(s.cuda_stream))
+        if gemm_events is None:
+            name = "a2av_gmm_mx_run"
+            st = load().a2av_gmm_mx_run(*args)
+        else:
+            name = "a2av_gmm_mx_run_profiled"
+            for ev in gemm_events:
+                if ev.cuda_event == 0:  # created lazily by torch: make it exist on this device
+                    ev.record(s)
+            st = load().a2av_gmm_mx_run_profiled(*args, ctypes.c_void_p(gemm_events[0].cuda_event),
+                                                 ctypes.c_void_p(gemm_events[1].cuda_event))
         if st != A2AV_OK:
-            raise A2avError(st, "a2av_gmm_mx_run")
+            raise A2avError(st, name)
         return gmmY, mmY, permuteOut_q, permuteOut_s

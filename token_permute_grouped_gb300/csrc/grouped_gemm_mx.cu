@@ -61,6 +61,8 @@ constexpr int kMxMmaWarp = 1;
 constexpr int kMxEpiWarp0 = 2;
 constexpr int MX_ATOM_ROWS = 128;     // rows (columns) of a block that one scale atom covers
 constexpr uint32_t MX_ATOM_BYTES = 512;  // 32 rows of 16 bytes
+constexpr uint32_t kMxAtomLine = 128;    // atoms move as 128-byte lines: 8 atom rows each
+constexpr int kMxAtomLineRows = 8;
 constexpr int MX_QUAD = 128;          // codes along K per atom: four E8M0 blocks of 32
 constexpr uint32_t MX_SUB_BYTES = MX_BM * MX_KCHUNK;      // 16 KB: 128 rows x one chunk
 constexpr uint32_t MX_TILE_BYTES = MX_SUB_BYTES * MX_CH;  // one operand's stage; B is the same size
@@ -119,11 +121,11 @@ struct MxLaunch {
     CUtensorMap tmB;   // weight codes [e, N1, H1]
     CUtensorMap tmX;   // mmX codes [BS, H2]
     CUtensorMap tmMW;  // mmWeight codes [N2, H2]
-    // Scale atoms (written by the permute kernel), as 16-byte rows, no
-    // swizzle.  A: 2-D {16, atom rows}, atom (half, quad) at row
-    // 32 (half * quads + quad), box 16 x 32 MX_CH (a stage's quads).  B: 3-D
-    // {16, 32 column blocks, groups * quads}, atom (group, quad, block) at
-    // row 32 block of plane group * quads + quad, box 16 x 32 kCtas x 2.
+    // Scale atoms (written by the permute kernel) as 128-byte lines, four
+    // per atom, no swizzle.  A: 2-D {128, lines}, atom (half, quad) at line
+    // 4 (half * quads + quad), box 128 x 4 MX_CH (a stage's quads).  B: 3-D
+    // {128, 4 column blocks, groups * quads}, atom (group, quad, block) at
+    // line 4 block of plane group * quads + quad, box 128 x 4 kCtas x 2.
     CUtensorMap tmSFA;  // routed A: halves of the expert groups (128 rows from each group's start)
     CUtensorMap tmSFX;  // mmX: halves of the BS rows
     CUtensorMap tmSFB;  // gmmWeight: 128-column blocks of each expert
@@ -517,8 +519,9 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     // Scale atoms of quads 2kb and 2kb + 1: this half's, then
                     // each of the tile's column blocks'.
                     const uint32_t sf_st = sf_smem + s * S::kSfStageBytes;
-                    tma_load_3d_mx<PAIR>(sf_st, tsa, fb, 0, 32 * (half * nq + MX_CH * kb), 0);
-                    tma_load_3d_mx<PAIR>(sf_st + S::kSfaBytes, tsb, fb, 0, 32 * cb0, z * nq + MX_CH * kb);
+                    constexpr int kLines = 32 / kMxAtomLineRows;  // 128-byte lines per atom
+                    tma_load_3d_mx<PAIR>(sf_st, tsa, fb, 0, kLines * (half * nq + MX_CH * kb), 0);
+                    tma_load_3d_mx<PAIR>(sf_st + S::kSfaBytes, tsb, fb, 0, kLines * cb0, z * nq + MX_CH * kb);
                 }
             }
             // Wait until the MMAs released every stage that was filled.
@@ -926,15 +929,19 @@ bool mx_codes_map(CUtensorMap *m, const void *ptr, int64_t groups, int64_t rows,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Scale atoms as 16-byte rows: 3-D {16, rows, planes}, box 16 x box_rows x
-// box_planes, no swizzle; out-of-range rows load as zeros.
+// Scale atoms, counted in 16-byte atom rows (rows, box_rows: multiples of
+// 8), loaded as 128-byte lines: 3-D {128, rows / 8, planes}, box 128 x
+// box_rows / 8 x box_planes, no swizzle, so shared memory receives the same
+// bytes in the same order with an eighth of the requests; out-of-range rows
+// load as zeros.
 bool mx_atoms_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t planes, uint32_t box_rows,
                   uint32_t box_planes) {
     auto fn = mx_encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {16, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(planes)};
-    cuuint64_t strides[2] = {16, static_cast<cuuint64_t>(rows * 16)};
-    cuuint32_t box[3] = {16, box_rows, box_planes};
+    if (!fn || rows % kMxAtomLineRows != 0 || box_rows % kMxAtomLineRows != 0) return false;
+    cuuint64_t dims[3] = {kMxAtomLine, static_cast<cuuint64_t>(rows / kMxAtomLineRows),
+                          static_cast<cuuint64_t>(planes)};
+    cuuint64_t strides[2] = {kMxAtomLine, static_cast<cuuint64_t>(rows * 16)};
+    cuuint32_t box[3] = {kMxAtomLine, box_rows / kMxAtomLineRows, box_planes};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -954,9 +961,7 @@ bool mx_aligned16(const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u)
 
 }  // namespace a2av
 
-extern "C" {
-
-a2av_status a2av_gmm_mx_workspace_size(const a2av_gmm_mx_desc *desc, size_t *bytes) {
+extern "C" a2av_status a2av_gmm_mx_workspace_size(const a2av_gmm_mx_desc *desc, size_t *bytes) {
     if (!desc || !bytes) return A2AV_ERR_NULLPTR;
     const a2av_status s = a2av::mx_validate(desc);
     if (s != A2AV_OK) return s;
@@ -964,11 +969,17 @@ a2av_status a2av_gmm_mx_workspace_size(const a2av_gmm_mx_desc *desc, size_t *byt
     return A2AV_OK;
 }
 
-a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, const void *ataOut_s,
-                            const int32_t *recvCounts, const void *gmmWeight_q, const void *gmmWeight_s,
-                            const void *mmX_q, const void *mmX_s, const void *mmWeight_q, const void *mmWeight_s,
-                            void *permuteOut_q, void *permuteOut_s, void *gmmY, void *mmY, void *workspace,
-                            size_t workspace_bytes, a2av_stream_t stream_handle) {
+namespace {
+
+// The call; with gemm_begin / gemm_end, those events are recorded right
+// around the GEMM launch, which then follows the prep kernel in plain stream
+// order (no programmatic dependent launch), so that they time it alone.
+a2av_status mx_run_impl(const a2av_gmm_mx_desc *desc, const void *ataOut_q, const void *ataOut_s,
+                        const int32_t *recvCounts, const void *gmmWeight_q, const void *gmmWeight_s,
+                        const void *mmX_q, const void *mmX_s, const void *mmWeight_q, const void *mmWeight_s,
+                        void *permuteOut_q, void *permuteOut_s, void *gmmY, void *mmY, void *workspace,
+                        size_t workspace_bytes, a2av_stream_t stream_handle, cudaEvent_t gemm_begin,
+                        cudaEvent_t gemm_end) {
     using namespace a2av;
     const a2av_status vs = mx_validate(desc);
     if (vs != A2AV_OK) return vs;
@@ -1080,7 +1091,7 @@ a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, 
         prep_ran = true;
     }
     g.write_status = prep_ran ? 0 : 1;
-    g.after_permute = prep_ran ? 1 : 0;
+    g.after_permute = (prep_ran && !gemm_begin) ? 1 : 0;
 
     // Persistent grid: one CTA (pair: cluster of two) per SM (pair), never
     // more than there can be tiles.
@@ -1109,15 +1120,44 @@ a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, 
         attr[n_attr].val.clusterDim.z = 1;
         ++n_attr;
     }
-    if (prep_ran) {  // start beside the prep kernel; the producer waits for it before its first load
+    if (g.after_permute) {  // start beside the prep kernel; the producer waits for it before its first load
         attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
         ++n_attr;
     }
     cfg.attrs = attr;
     cfg.numAttrs = n_attr;
+    if (gemm_begin && cudaEventRecord(gemm_begin, stream) != cudaSuccess) return A2AV_ERR_CUDA;
     if (cudaLaunchKernelEx(&cfg, kern, g) != cudaSuccess) return A2AV_ERR_CUDA;
+    if (gemm_end && cudaEventRecord(gemm_end, stream) != cudaSuccess) return A2AV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? A2AV_OK : A2AV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+a2av_status a2av_gmm_mx_run(const a2av_gmm_mx_desc *desc, const void *ataOut_q, const void *ataOut_s,
+                            const int32_t *recvCounts, const void *gmmWeight_q, const void *gmmWeight_s,
+                            const void *mmX_q, const void *mmX_s, const void *mmWeight_q, const void *mmWeight_s,
+                            void *permuteOut_q, void *permuteOut_s, void *gmmY, void *mmY, void *workspace,
+                            size_t workspace_bytes, a2av_stream_t stream) {
+    return mx_run_impl(desc, ataOut_q, ataOut_s, recvCounts, gmmWeight_q, gmmWeight_s, mmX_q, mmX_s, mmWeight_q,
+                       mmWeight_s, permuteOut_q, permuteOut_s, gmmY, mmY, workspace, workspace_bytes, stream,
+                       nullptr, nullptr);
+}
+
+a2av_status a2av_gmm_mx_run_profiled(const a2av_gmm_mx_desc *desc, const void *ataOut_q, const void *ataOut_s,
+                                     const int32_t *recvCounts, const void *gmmWeight_q,
+                                     const void *gmmWeight_s, const void *mmX_q, const void *mmX_s,
+                                     const void *mmWeight_q, const void *mmWeight_s, void *permuteOut_q,
+                                     void *permuteOut_s, void *gmmY, void *mmY, void *workspace,
+                                     size_t workspace_bytes, a2av_stream_t stream, void *gemm_begin_event,
+                                     void *gemm_end_event) {
+    if (!gemm_begin_event || !gemm_end_event) return A2AV_ERR_NULLPTR;
+    return mx_run_impl(desc, ataOut_q, ataOut_s, recvCounts, gmmWeight_q, gmmWeight_s, mmX_q, mmX_s, mmWeight_q,
+                       mmWeight_s, permuteOut_q, permuteOut_s, gmmY, mmY, workspace, workspace_bytes, stream,
+                       static_cast<cudaEvent_t>(gemm_begin_event), static_cast<cudaEvent_t>(gemm_end_event));
 }
 
 }  // extern "C"
