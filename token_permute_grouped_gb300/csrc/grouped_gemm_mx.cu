@@ -957,6 +957,20 @@ int mx_sm_count() {
 
 bool mx_aligned16(const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
 
+// Prep-kernel blocks resident on one SM at once (per device, queried once).
+int mx_prep_blocks_per_sm() {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mx_prep_kernel, kMxPermThreads, 0) != cudaSuccess)
+            return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 }  // namespace
 
 }  // namespace a2av
@@ -1081,11 +1095,15 @@ a2av_status mx_run_impl(const a2av_gmm_mx_desc *desc, const void *ataOut_q, cons
     bool prep_ran = false;
     if (routed || shared) {
         // Blocks for a warp per row of A, or a thread per atom row, at most
-        // eight per SM (all resident at once).
+        // as many as are resident at once (registers allow five per SM), so
+        // that no block waits for a second wave.
         const int64_t atom_rows = ws.sfa_rows + static_cast<int64_t>(ws.total - ws.sfx) / 16;
         const int64_t want = std::max<int64_t>((d.A + kMxPermThreads / 32 - 1) / (kMxPermThreads / 32),
                                                (atom_rows + kMxPermThreads - 1) / kMxPermThreads);
-        const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * 8)));
+        const int per_sm = mx_prep_blocks_per_sm();
+        if (per_sm <= 0) return A2AV_ERR_CUDA;
+        const int blocks =
+            static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * per_sm)));
         mx_prep_kernel<<<blocks, kMxPermThreads, 0, stream>>>(pp);
         if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
         prep_ran = true;
