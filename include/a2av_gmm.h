@@ -70,7 +70,7 @@ typedef enum {
     A2AV_OK = 0,
     A2AV_ERR_NULLPTR = 1,      /* a required pointer is NULL */
     A2AV_ERR_INVALID = 2,      /* shape, range or dtype outside the limits above */
-    A2AV_ERR_UNSUPPORTED = 3,  /* allowed by the operator, not by this build (alignment) */
+    A2AV_ERR_UNSUPPORTED = 3,  /* allowed by the operator, not by this library (alignment) */
     A2AV_ERR_WORKSPACE = 4,    /* workspace too small or misaligned */
     A2AV_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
     A2AV_ERR_DEVICE_CHECK = 6, /* the device found inconsistent recvCounts */
@@ -95,7 +95,7 @@ typedef enum {
 
 /* GEMM tile shape.  All give bitwise-identical outputs. */
 typedef enum {
-    A2AV_TILES_DEFAULT = 0,    /* the faster shape for this build */
+    A2AV_TILES_DEFAULT = 0,    /* the faster shape for this library */
     A2AV_TILES_SINGLE = 1,     /* 128-row tiles, one CTA each */
     A2AV_TILES_PAIR = 2,       /* 256-row tiles on a cluster of two CTAs; pipeline stages
                                   128 deep in K where H1, H2 are multiples of 128 and the

@@ -18,7 +18,7 @@
  * Shapes (as in a2av_gmm.h): W ranks, e local experts (1 <= e <= 32,
  * W * e <= 256), A routed rows (sum of recvCounts, 0 allowed), H1 x N1 routed
  * weights, BS x H2 shared-expert input, H2 x N2 shared weight (BS = 0: none).
- * This build needs H1 and H2 to be multiples of 512 (scale rows of H/32
+ * This library needs H1 and H2 to be multiples of 512 (scale rows of H/32
  * bytes start on 16-byte boundaries), N1 and N2 multiples of 8, and the
  * same code format for activations and weights.
  *
@@ -38,7 +38,7 @@
  * found on the device (recvCounts inconsistent with A) are recorded in the
  * workspace's status word: read them with a2av_gmm_read_device_status.
  * Status codes: those of a2av_gmm.h (A2AV_ERR_INVALID: a shape or format
- * outside the limits; A2AV_ERR_UNSUPPORTED: a limit of this build or a
+ * outside the limits; A2AV_ERR_UNSUPPORTED: a limit of this library or a
  * misaligned pointer; A2AV_ERR_WORKSPACE: workspace too small or not 256-byte
  * aligned).
  */

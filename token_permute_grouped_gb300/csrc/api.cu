@@ -460,7 +460,7 @@ const char *a2av_gmm_status_string(a2av_status status) {
         case A2AV_OK: return "ok";
         case A2AV_ERR_NULLPTR: return "a required pointer is NULL";
         case A2AV_ERR_INVALID: return "shape, range or dtype outside the operator's limits";
-        case A2AV_ERR_UNSUPPORTED: return "not supported by this build (alignment)";
+        case A2AV_ERR_UNSUPPORTED: return "not supported by this library (alignment)";
         case A2AV_ERR_WORKSPACE: return "workspace too small or misaligned";
         case A2AV_ERR_CUDA: return "CUDA call failed, or a kernel gave up waiting";
         case A2AV_ERR_DEVICE_CHECK: return "recvCounts negative or not summing to A";
