@@ -12,7 +12,7 @@
 // CTA pair (cta_group::2); K in stages of 256 codes: two 128-byte swizzle
 // rows per operand row (two 16 KB sub-tiles), eight MMAs.  Per CTA:
 //   warp 0     one thread issues a stage's TMA loads: the A rows (read in
-//              place from ataOut, or from the permute kernel's staging copy),
+//              place from ataOut, or from the prep kernel's staging copy),
 //              the K-major weight columns, one 4-D load of both sub-tiles per
 //              operand, and the stage's scale atoms (below).
 //   warp 1     one thread copies the stage's scale atoms from shared memory
@@ -23,7 +23,7 @@
 //              global, rows past the group's end and columns past N masked.
 //              A warp loads all its columns, releases the accumulator, and
 //              only then converts and stores them.
-// Scale atoms: the permute kernel rewrites every operand's E8M0 scales as
+// Scale atoms: the prep kernel rewrites every operand's E8M0 scales as
 // 512-byte atoms, one per 128-row (or 128-column) block and per 4 K blocks
 // of 32 codes: 32 rows of 16 bytes, row l holding the four scale bytes of
 // block rows l, 32 + l, 64 + l and 96 + l.  tcgen05.cp .32x128b.warpx4 turns
@@ -111,7 +111,7 @@ struct MxLaunch {
     void *mmY;
     int32_t *status;
     int32_t write_status;
-    int32_t after_permute;  // launched beside the permute kernel: wait for it before a staged read
+    int32_t after_permute;  // launched beside the prep kernel: wait for it before the first load
     int32_t qtype;  // 0 E4M3FN, 1 E5M2 (both operands)
     int32_t pair;
     int32_t grid;
@@ -121,7 +121,7 @@ struct MxLaunch {
     CUtensorMap tmB;   // weight codes [e, N1, H1]
     CUtensorMap tmX;   // mmX codes [BS, H2]
     CUtensorMap tmMW;  // mmWeight codes [N2, H2]
-    // Scale atoms (written by the permute kernel) as 128-byte lines, four
+    // Scale atoms (written by the prep kernel) as 128-byte lines, four
     // per atom, no swizzle.  A: 2-D {128, lines}, atom (half, quad) at line
     // 4 (half * quads + quad), box 128 x 4 MX_CH (a stage's quads).  B: 3-D
     // {128, 4 column blocks, groups * quads}, atom (group, quad, block) at
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
     if (warp == 0) {
         // =========================================================== TMA producer
         if (lane == 0) {
-            // Every tile's scale atoms come from the permute kernel: wait for
+            // Every tile's scale atoms come from the prep kernel: wait for
             // that grid before the first load.
             if (p.after_permute) asm volatile("griddepcontrol.wait;" ::: "memory");
             uint32_t it = 0;
