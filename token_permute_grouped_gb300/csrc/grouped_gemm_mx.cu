@@ -15,9 +15,12 @@
 //              place from ataOut, or from the prep kernel's staging copy),
 //              the K-major weight columns, one 4-D load of both sub-tiles per
 //              operand, and the stage's scale atoms (below).
-//   warp 1     one thread copies the stage's scale atoms from shared memory
-//              into TMEM (tcgen05.cp .32x128b.warpx4) and issues the MMAs;
-//              copies and MMAs run in issue order on the tensor core.
+//   warp 1     one thread issues the MMAs of a stage once its codes have
+//              landed and its scale atoms are in TMEM.
+//   warp 10    one thread copies each stage's scale atoms from shared memory
+//              into TMEM (tcgen05.cp .32x128b.warpx4) as soon as they land,
+//              then commits to the stage's sfready barrier; the copies no
+//              longer sit in the MMA thread's issue stream.
 //   warps 2-9  epilogue, two warps per TMEM lane quarter, each draining half
 //              of the columns: TMEM -> registers -> bf16 (nearest even) ->
 //              global, rows past the group's end and columns past N masked.
@@ -56,9 +59,10 @@ constexpr int MX_CH = 2;         // K chunks per stage
 constexpr int MX_BK = MX_KCHUNK * MX_CH;
 constexpr int MX_STAGES = 3;
 constexpr int kMxEpiWarps = 8;  // two per TMEM lane quarter, each draining half of the columns
-constexpr int MX_THREADS = (2 + kMxEpiWarps) * 32;
+constexpr int MX_THREADS = (3 + kMxEpiWarps) * 32;
 constexpr int kMxMmaWarp = 1;
 constexpr int kMxEpiWarp0 = 2;
+constexpr int kMxScaleWarp = kMxEpiWarp0 + kMxEpiWarps;  // copies each stage's scale atoms into TMEM
 constexpr int MX_ATOM_ROWS = 128;     // rows (columns) of a block that one scale atom covers
 constexpr uint32_t MX_ATOM_BYTES = 512;  // 32 rows of 16 bytes
 constexpr uint32_t kMxAtomLine = 128;    // atoms move as 128-byte lines: 8 atom rows each
@@ -159,6 +163,7 @@ struct MxGroup {
 struct MxControl {
     uint64_t full[MX_STAGES];   // a stage's codes and scale atoms landed (pair: both CTAs'; in the even CTA)
     uint64_t empty[MX_STAGES];  // the copies and MMAs reading a stage completed
+    uint64_t sfready[MX_STAGES];  // a stage's scale atoms are in TMEM (in the even CTA)
     uint64_t tfull[2];
     uint64_t tempty[2];           // epilogue drained the accumulator (pair: both CTAs; in the even CTA)
     uint32_t tmem_base;
@@ -261,6 +266,22 @@ __device__ __forceinline__ void mx_commit(uint32_t bar) {
             "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
             " [%0], %1;" ::"r"(bar),
             "h"(both)
+            : "memory");
+    } else {
+        mma_commit(bar);
+    }
+}
+
+// Arrival on this CTA's barrier once the calling thread's earlier tcgen05
+// operations have completed.
+template <bool PAIR>
+__device__ __forceinline__ void mx_commit_own(uint32_t bar) {
+    if constexpr (PAIR) {
+        const uint16_t own = 1;  // the even CTA, the only caller
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+            " [%0], %1;" ::"r"(bar),
+            "h"(own)
             : "memory");
     } else {
         mma_commit(bar);
@@ -441,6 +462,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
             for (int s = 0; s < MX_STAGES; ++s) {
                 mbar_init(smem_u32(&C.full[s]), 1);
                 mbar_init(smem_u32(&C.empty[s]), 1);
+                mbar_init(smem_u32(&C.sfready[s]), 1);
             }
             for (int a = 0; a < 2; ++a) {
                 mbar_init(smem_u32(&C.tfull[a]), 1);
@@ -552,9 +574,11 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 for (int kb = 0; kb < K / MX_BK; ++kb, ++it) {
                     const int s = it % MX_STAGES;
                     const uint32_t par = (it / MX_STAGES) & 1;
-                    // Codes and atoms arrive by TMA (async proxy), as the copies
-                    // and MMAs read them: the barrier phase orders the two.
-                    if (!mx_wait(&C.abort, &C.full[s], par, p.status)) {
+                    // Codes arrive by TMA (async proxy), as the MMAs read them:
+                    // the barrier phase orders the two.  The scale warp has
+                    // copied the stage's atoms into TMEM once sfready flips.
+                    if (!mx_wait(&C.abort, &C.full[s], par, p.status) ||
+                        !mx_wait(&C.abort, &C.sfready[s], par, p.status)) {
                         ok = false;
                         break;
                     }
@@ -562,20 +586,6 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     const uint64_t bd = b_desc0 + ((s * MX_TILE_BYTES) >> 4);
                     const uint32_t sfa = C.tmem_base + sfa_col<PAIR>(s);
                     const uint32_t sfb = C.tmem_base + sfb_col<PAIR>(s);
-                    // Scale word j (MMAs 4j .. 4j + 3): A's atom to 4 columns;
-                    // B's atom of column block i to columns 4i .. 4i + 3 of
-                    // the word's NB.  The TMEM columns of stage s are free:
-                    // this stage's smem was refilled only after the MMAs
-                    // that last read them completed.
-                    const uint32_t sf_st = sf_smem + s * S::kSfStageBytes;
-#pragma unroll
-                    for (int j = 0; j < MX_CH; ++j) {
-                        mx_sf_copy<PAIR>(sfa + 4 * j, sf_st + j * MX_ATOM_BYTES);
-#pragma unroll
-                        for (int i = 0; i < kCtas; ++i)
-                            mx_sf_copy<PAIR>(sfb + NB * j + 4 * i,
-                                             sf_st + S::kSfaBytes + (j * kCtas + i) * MX_ATOM_BYTES);
-                    }
 #pragma unroll
                     for (int kk = 0; kk < MX_BK / 32; ++kk) {
                         const uint32_t off = ((kk >> 2) * MX_SUB_BYTES + (kk & 3) * 32) >> 4;
@@ -586,6 +596,40 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     mx_commit<PAIR>(smem_u32(&C.empty[s]));
                 }
                 if (ok) mx_commit<PAIR>(smem_u32(&C.tfull[acc]));
+            }
+        }
+    } else if (warp == kMxScaleWarp) {
+        // =========================================================== scale atoms into TMEM
+        if (lane == 0 && rank == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = unit; t < total && ok; t += nunits) {
+                const MxTile w = mx_decode_tile(C, t);
+                const int K = w.g >= e ? p.H2 : p.H1;
+                for (int kb = 0; kb < K / MX_BK; ++kb, ++it) {
+                    const int s = it % MX_STAGES;
+                    if (!mx_wait(&C.abort, &C.full[s], (it / MX_STAGES) & 1, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    // Scale word j (MMAs 4j .. 4j + 3): A's atom to 4 columns;
+                    // B's atom of column block i to columns 4i .. 4i + 3 of
+                    // the word's NB.  The TMEM columns of stage s are free:
+                    // the producer refilled this stage only after the MMAs
+                    // that last read them completed.
+                    const uint32_t sfa = C.tmem_base + sfa_col<PAIR>(s);
+                    const uint32_t sfb = C.tmem_base + sfb_col<PAIR>(s);
+                    const uint32_t sf_st = sf_smem + s * S::kSfStageBytes;
+#pragma unroll
+                    for (int j = 0; j < MX_CH; ++j) {
+                        mx_sf_copy<PAIR>(sfa + 4 * j, sf_st + j * MX_ATOM_BYTES);
+#pragma unroll
+                        for (int i = 0; i < kCtas; ++i)
+                            mx_sf_copy<PAIR>(sfb + NB * j + 4 * i,
+                                             sf_st + S::kSfaBytes + (j * kCtas + i) * MX_ATOM_BYTES);
+                    }
+                    mx_commit_own<PAIR>(smem_u32(&C.sfready[s]));
+                }
             }
         }
     } else {
