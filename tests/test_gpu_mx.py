@@ -106,6 +106,8 @@ def test_scale_placement_exact(orc, case, tiles):
     (2, 2, 512, 128, 300, 0.0, 0, 0, 0),
     (4, 3, 1024, 200, 700, 0.3, 100, 512, 136),
     (8, 4, 2048, 256, 1500, 0.1, 257, 1024, 384),
+    # The largest H1 below 65536 that is a multiple of 512: 254 stages of 256 codes.
+    (2, 2, 65024, 64, 200, 0.0, 0, 0, 0),
 ])
 def test_matches_oracle(orc, qtype, W, e, H1, N1, A, zero, BS, H2, N2, tiles):
     rc = random_counts(W, e, A, seed=A + W, zero_prob=zero)

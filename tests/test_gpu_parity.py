@@ -48,6 +48,12 @@ EDGE = {
     "fp16_mixed": (8, 4, 256, 512, None, 640, 512, 1024, "fp16"),
     "max_segments_256": (8, 32, 64, 64, None, 0, 0, 0, "bf16"),
     "max_w_256_e1": (256, 1, 64, 128, None, 0, 0, 0, "bf16"),
+    # The page's largest hidden and output sizes ("aclnnAlltoAllvGroupedMatMul",
+    # Shape variables: H1, N1 < 65536; the shared expert's H2 <= 12288):
+    # 512 K stages per tile with a K tail of 120, and 256 column tiles with a
+    # ragged last one.
+    "max_h1_65528": (2, 2, 65528, 136, [90, 130, 5, 70], 33, 12288, 72, "bf16"),
+    "max_n1_65528": (2, 2, 64, 65528, [40, 3, 0, 90], 17, 64, 65528, "fp16"),
 }
 
 
