@@ -60,3 +60,33 @@ def test_offsets_past_2_31(case, path, want_perm):
     del perm
     idx = torch.from_numpy(rows).to(y.device)
     assert_close(y.index_select(0, idx).cpu(), ref_y, f"gmmY sampled rows ({path})")
+
+
+@pytest.fixture(scope="module")
+def mx_case(orc):
+    from token_permute_grouped_gb300.workloads import Workload, make_mx_inputs
+    wl = Workload("mx_offsets", W=W, e=E, H1=H1, N1=N1, dtype="bf16", routing="given")
+    inp = make_mx_inputs(wl, seed=42, qtype="e4m3fn", recvCounts=np.asarray(COUNTS, np.int32))
+    assert inp.A * H1 > 2**31
+    perm_q = orc.permute(W, E, inp.recvCounts, inp.ataOut_q.view(torch.int16)).view(torch.uint8)
+    perm_s = orc.permute(W, E, inp.recvCounts, inp.ataOut_s.view(torch.int16)).view(torch.uint8)
+    _, _, groups, _ = orc.plan(W, E, inp.recvCounts, inp.A)
+    rows = sample_rows(groups, 400, seed=42)
+    rows = np.unique(np.concatenate([rows, np.arange(inp.A - 256, inp.A)])).astype(np.int64)
+    ref_y = orc.mx_grouped_matmul(groups, perm_q, perm_s, inp.gmmWeight_q, inp.gmmWeight_s, 0, 0, rows)
+    return inp, perm_q, perm_s, rows, ref_y
+
+
+@pytest.mark.parametrize("tiles,want_perm", [("pair", False), ("pair", True), ("single", False)])
+def test_mx_offsets_past_2_31(mx_case, tiles, want_perm):
+    inp, perm_q, perm_s, rows, ref_y = mx_case
+    dev = torch.device("cuda:0")
+    plan = binding.MxPlan(W, E, inp.A, H1, N1, 0, 0, 0, "e4m3fn", want_perm, dev, tiles)
+    y, _, pq, ps = plan.run(inp.ataOut_q.to(dev), inp.ataOut_s.to(dev), torch.from_numpy(inp.recvCounts).to(dev),
+                            inp.gmmWeight_q.to(dev), inp.gmmWeight_s.to(dev))
+    torch.cuda.synchronize()
+    assert binding.a2av_gmm_read_device_status(plan.workspace) == (0, 0)
+    if want_perm:
+        assert torch.equal(pq.cpu(), perm_q) and torch.equal(ps.cpu(), perm_s)
+    idx = torch.from_numpy(rows).to(dev)
+    assert_close(y.index_select(0, idx).cpu(), ref_y, f"mx gmmY sampled rows ({tiles})")
