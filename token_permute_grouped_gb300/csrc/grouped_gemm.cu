@@ -794,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                             pk.y = pack2<BF16>(r[v * 8 + 2], r[v * 8 + 3]);
                             pk.z = pack2<BF16>(r[v * 8 + 4], r[v * 8 + 5]);
                             pk.w = pack2<BF16>(r[v * 8 + 6], r[v * 8 + 7]);
-                            *reinterpret_cast<uint4 *>(out + col) = pk;
+                            st_stream_v4(out + col, pk);
                         }
                     }
                 }

@@ -677,7 +677,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                             pk.y = pack_bf16(r[2], r[3]);
                             pk.z = pack_bf16(r[4], r[5]);
                             pk.w = pack_bf16(r[6], r[7]);
-                            *reinterpret_cast<uint4 *>(out + col) = pk;
+                            st_stream_v4(out + col, pk);
                         }
                     }
                 }

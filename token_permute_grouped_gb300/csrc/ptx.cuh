@@ -87,6 +87,14 @@ __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// 16-byte global store with the streaming hint (.cs: evict first).  The
+// GEMM outputs are written once and not read again by the kernel, so they
+// should not push operands out of L2.
+__device__ __forceinline__ void st_stream_v4(void *ptr, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // TMA tiled loads.  The innermost coordinate must give a 16-byte aligned
 // start (x * element size a multiple of 16); out-of-range elements are filled
 // with zeros and still count toward the transaction bytes.
