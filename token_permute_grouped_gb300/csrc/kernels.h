@@ -19,8 +19,8 @@ struct PermuteLaunch {
     int32_t *status;      // device status word
     int32_t write_status; // 1: this kernel stores the word (first kernel of a call)
     int32_t only_straddling;  // 1: copy only 128-row halves that straddle a segment boundary
-    int32_t blocks_per_sm;    // grid cap per SM (0: 8, one full SM of threads); a GEMM that
-                              // starts while this kernel runs needs room beside it
+    int32_t blocks_per_sm;    // grid cap per SM (0: as many as are resident at once); a GEMM
+                              // that starts while this kernel runs needs room beside it
 };
 
 cudaError_t launch_permute(const PermuteLaunch &p, int num_sms, cudaStream_t stream);

@@ -4,6 +4,8 @@
 // A warp moves one 2 KB piece of a row at a time with 16-byte vector loads
 // and stores (coalesced across the warp); each CTA first rebuilds the segment table from
 // recvCounts in shared memory (one warp, a few hundred cycles).
+#include <algorithm>
+
 #include "kernels.h"
 #include "plan.cuh"
 
@@ -108,11 +110,30 @@ __global__ void __launch_bounds__(kPermuteThreads)
     }
 }
 
+// Blocks of the permute kernel resident on one SM at once (per device, queried once).
+int permute_blocks_per_sm() {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, permute_rows_kernel, kPermuteThreads, 0) !=
+            cudaSuccess)
+            return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 }  // namespace
 
 cudaError_t launch_permute(const PermuteLaunch &p, int num_sms, cudaStream_t stream) {
     int blocks = (p.A + kPermuteWarps - 1) / kPermuteWarps;
-    const int cap = num_sms * (p.blocks_per_sm > 0 ? p.blocks_per_sm : 2048 / kPermuteThreads);
+    // At most the blocks that are resident at once, so that none waits for a
+    // second wave.
+    const int resident = permute_blocks_per_sm();
+    if (resident <= 0) return cudaErrorUnknown;
+    const int cap = num_sms * (p.blocks_per_sm > 0 ? std::min<int>(p.blocks_per_sm, resident) : resident);
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     permute_rows_kernel<<<blocks, kPermuteThreads, 0, stream>>>(
