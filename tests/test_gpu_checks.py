@@ -73,3 +73,23 @@ def test_checked_build_agrees_and_reports_nothing(orc, libs, name, path, want_pe
     if perm is not None:
         assert_bits_equal(perm, perm0, "permuteOut")
     check_full(orc, inp, y, m, perm)
+
+
+@pytest.mark.parametrize("i", range(0, 200, 5))
+def test_checked_build_on_fuzz_shapes(orc, libs, i):
+    # Forty of the seeded random shapes of test_gpu_fuzz.py, each on its drawn
+    # path: no bounds check fires, and the bits equal the ordinary build's.
+    from test_gpu_fuzz import _draw
+    c = _draw(i)
+    inp = custom_inputs(c["W"], c["e"], c["H1"], c["N1"], c["rc"], c["dtype"], c["BS"], c["H2"], c["N2"],
+                        seed=c["seed"])
+    plain, checked = libs
+    st, code, y, m, perm = _run(checked, inp, c["path"], c["want_perm"])
+    assert (st, code) == (0, 0), (c, st, code)
+    _, _, y0, m0, perm0 = _run(plain, inp, c["path"], c["want_perm"])
+    assert_bits_equal(y, y0, "gmmY")
+    if m is not None:
+        assert_bits_equal(m, m0, "mmY")
+    if perm is not None:
+        assert_bits_equal(perm, perm0, "permuteOut")
+    check_full(orc, inp, y, m, perm)
