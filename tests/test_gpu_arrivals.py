@@ -111,6 +111,11 @@ CASES = {
     # 2048 row tiles (group order), 256-row pair tiles fewer (arrival order).
     "over_order_capacity": lambda: custom_inputs(4, 32, 128, 128, [2000 + (i * 37) % 400 for i in range(128)],
                                                  "bf16", 256, 128, 128, seed=34),
+    # 32 sources, a quarter of them sending nothing (their flags still
+    # arrive), runs of 0 to 300 rows.
+    "many_sources_some_empty": lambda: custom_inputs(
+        32, 2, 256, 192, [0 if (i // 2) % 4 == 3 else (i * 53) % 301 for i in range(64)], "fp16", 100, 128, 64,
+        seed=35),
 }
 
 
