@@ -99,11 +99,26 @@ struct Control {
     uint16_t order[kMaxOrder];     // routed row tiles by latest source (arrival-driven start)
 };
 
+// Epilogue staging: each epilogue warp turns its 32 rows x 32 columns of
+// 16-bit results around in 2 KB of shared memory, so that a store writes 8
+// rows of 64 contiguous bytes instead of 16 bytes in each of 32 rows.
+constexpr uint32_t kEpiStageBytes = 32 * 64;
+constexpr int kEpiWarps = 4;
+
+template <int STAGES>
+__host__ __device__ constexpr size_t epi_stage_offset() {
+    return (sizeof(Control<STAGES>) + 127) / 128 * 128;
+}
+
 template <bool PAIR, int CH>
 constexpr size_t smem_bytes() {
     using S = Shape<PAIR, CH>;
-    return 1024 + S::STAGES * (S::A_STAGE_BYTES + S::B_STAGE_BYTES) + sizeof(Control<S::STAGES>);
+    return 1024 + S::STAGES * (S::A_STAGE_BYTES + S::B_STAGE_BYTES) + epi_stage_offset<S::STAGES>() +
+           kEpiWarps * kEpiStageBytes;
 }
+static_assert(smem_bytes<true, 2>() <= 232448 && smem_bytes<true, 1>() <= 232448 &&
+                  smem_bytes<false, 1>() <= 232448 && smem_bytes<false, 2>() <= 232448,
+              "shared memory per CTA");
 
 struct Tile {
     int g, m, n;
@@ -380,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const uint32_t b_smem = base + STAGES * A_STAGE_BYTES;
     Control<STAGES> &C =
         *reinterpret_cast<Control<STAGES> *>(base_ptr + STAGES * (A_STAGE_BYTES + S::B_STAGE_BYTES));
+    const uint32_t epi0 = base + STAGES * (A_STAGE_BYTES + S::B_STAGE_BYTES) + epi_stage_offset<STAGES>();
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -776,28 +792,50 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                                              static_cast<int64_t>(shared ? p.BS : p.A),
                                          p.status);
             const int n0 = w.n * bn;
-            const size_t out_row = static_cast<size_t>(shared ? row : C.g[w.g].row0 + row);
-            uint16_t *out = static_cast<uint16_t *>(shared ? p.mmY : p.gmmY) + out_row * N + n0;
+            uint16_t *const out_base = static_cast<uint16_t *>(shared ? p.mmY : p.gmmY);
             const uint32_t t_base = C.tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
             const int nchunks = (bn + 31) / 32;
+            // This warp's 32 rows: lane l holds row0w + l of the tile's group.
+            // After the turn-around, lane l stores row row0w + 8k + l / 4,
+            // 16 bytes at column 8 (l % 4) of the chunk, for k = 0 .. 3.
+            const int row0w = row - lane;
+            bool ok_k[4];
+            uint16_t *out_k[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int rr = row0w + 8 * k + (lane >> 2);
+                ok_k[k] = __shfl_sync(0xffffffffu, valid, 8 * k + (lane >> 2));
+                const size_t orow = static_cast<size_t>(shared ? rr : C.g[w.g].row0 + rr);
+                out_k[k] = out_base + orow * N + n0;
+            }
+            // 64-byte rows; the 16-byte chunk index is XORed with (row / 2) % 4,
+            // so that both the row-wise writes and the column-wise reads touch
+            // eight distinct 16-byte slots of each 128 bytes.
+            const uint32_t stage = epi0 + static_cast<uint32_t>(warp - kMmaWarp - 1) * kEpiStageBytes;
             for (int c = 0; c < nchunks; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_base + c * 32, r);
                 tmem_ld_wait();
-                if (valid) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const int col = c * 32 + v * 8;
-                        if (col < bn && n0 + col < N) {
-                            uint4 pk;
-                            pk.x = pack2<BF16>(r[v * 8 + 0], r[v * 8 + 1]);
-                            pk.y = pack2<BF16>(r[v * 8 + 2], r[v * 8 + 3]);
-                            pk.z = pack2<BF16>(r[v * 8 + 4], r[v * 8 + 5]);
-                            pk.w = pack2<BF16>(r[v * 8 + 6], r[v * 8 + 7]);
-                            st_stream_v4(out + col, pk);
-                        }
-                    }
+                for (int v = 0; v < 4; ++v) {
+                    uint4 pk;
+                    pk.x = pack2<BF16>(r[v * 8 + 0], r[v * 8 + 1]);
+                    pk.y = pack2<BF16>(r[v * 8 + 2], r[v * 8 + 3]);
+                    pk.z = pack2<BF16>(r[v * 8 + 4], r[v * 8 + 5]);
+                    pk.w = pack2<BF16>(r[v * 8 + 6], r[v * 8 + 7]);
+                    st_shared_v4(stage + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4), pk);
                 }
+                __syncwarp();
+                const int v = lane & 3;
+                const int col = c * 32 + v * 8;
+                const bool col_ok = col < bn && n0 + col < N;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int rr = 8 * k + (lane >> 2);
+                    const uint4 val = ld_shared_v4(stage + rr * 64 + ((v ^ ((rr >> 1) & 3)) << 4));
+                    if (ok_k[k] && col_ok) st_stream_v4(out_k[k] + col, val);
+                }
+                __syncwarp();  // the next chunk rewrites the staging area
             }
             tc_fence_before_sync();
             __syncwarp();
