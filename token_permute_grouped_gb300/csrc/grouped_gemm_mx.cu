@@ -173,11 +173,17 @@ struct MxControl {
     SegmentTable seg;
 };
 
+// Epilogue staging: each epilogue warp turns a 32 x 32 block of bf16 results
+// around in 2 KB of shared memory (see the epilogue), after the control block.
+constexpr uint32_t kMxEpiStageBytes = 32 * 64;
+__host__ __device__ constexpr size_t mx_epi_offset() { return (sizeof(MxControl) + 127) / 128 * 128; }
+
 template <bool PAIR>
 constexpr size_t mx_smem_bytes() {
-    return 1024 + MX_STAGES * (2 * MX_TILE_BYTES + MxShape<PAIR>::kSfStageBytes) + sizeof(MxControl);
+    return 1024 + MX_STAGES * (2 * MX_TILE_BYTES + MxShape<PAIR>::kSfStageBytes) + mx_epi_offset() +
+           kMxEpiWarps * kMxEpiStageBytes;
 }
-static_assert(mx_smem_bytes<true>() <= 232448, "shared memory per CTA");
+static_assert(mx_smem_bytes<true>() <= 232448 && mx_smem_bytes<false>() <= 232448, "shared memory per CTA");
 
 struct MxTile {
     int g, m, n;
@@ -410,6 +416,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
     const uint32_t sf_smem = base + 2 * MX_STAGES * MX_TILE_BYTES;  // per stage: A atoms, then B atoms
     MxControl &C = *reinterpret_cast<MxControl *>(base_ptr + 2 * MX_STAGES * MX_TILE_BYTES +
                                                   MX_STAGES * S::kSfStageBytes);
+    const uint32_t epi0 = base + 2 * MX_STAGES * MX_TILE_BYTES + MX_STAGES * S::kSfStageBytes + mx_epi_offset();
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -650,8 +657,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
             const int row = w.m * TILE_M + static_cast<int>(rank) * MX_BM + q * 32 + lane;
             const bool valid = row < C.g[w.g].rows;
             const int n0 = w.n * TILE_N;
-            const size_t out_row = static_cast<size_t>(shared ? row : C.g[w.g].row0 + row);
-            uint16_t *out = static_cast<uint16_t *>(shared ? p.mmY : p.gmmY) + out_row * N + n0;
+            uint16_t *const out_base = static_cast<uint16_t *>(shared ? p.mmY : p.gmmY);
             const uint32_t t_base = C.tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * S::kAccCols;
             // All of this warp's columns come out of TMEM first (the loads are
             // asynchronous, one wait for all), then the accumulator is
@@ -664,23 +670,41 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mx_arrive_leader<PAIR>(smem_u32(&C.tempty[acc]), rank);
-            if (valid) {
+            // Each 32 x 32 block is turned around in this warp's 2 KB of
+            // shared memory (64-byte rows, the 16-byte chunk index XORed with
+            // (row / 2) % 4: no bank conflicts either way), then stored as 8
+            // rows of 64 contiguous bytes per instruction.  After the turn,
+            // lane l stores row 8k + l / 4 of the warp's 32, at column
+            // 8 (l % 4) of the block.
+            const uint32_t valid_mask = __ballot_sync(0xffffffffu, valid);
+            const int row0w = row - lane;
+            const uint32_t stage = epi0 + static_cast<uint32_t>(warp - kMxEpiWarp0) * kMxEpiStageBytes;
 #pragma unroll
-                for (int i = 0; i < kChunks; ++i) {
+            for (int i = 0; i < kChunks; ++i) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int col = (c0 + i) * 32 + j * 8;
-                        if (n0 + col < N) {
-                            const uint32_t *r = v[i] + j * 8;
-                            uint4 pk;
-                            pk.x = pack_bf16(r[0], r[1]);
-                            pk.y = pack_bf16(r[2], r[3]);
-                            pk.z = pack_bf16(r[4], r[5]);
-                            pk.w = pack_bf16(r[6], r[7]);
-                            st_stream_v4(out + col, pk);
-                        }
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t *r = v[i] + j * 8;
+                    uint4 pk;
+                    pk.x = pack_bf16(r[0], r[1]);
+                    pk.y = pack_bf16(r[2], r[3]);
+                    pk.z = pack_bf16(r[4], r[5]);
+                    pk.w = pack_bf16(r[6], r[7]);
+                    st_shared_v4(stage + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pk);
+                }
+                __syncwarp();
+                const int j = lane & 3;
+                const int col = (c0 + i) * 32 + j * 8;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int rr = 8 * k + (lane >> 2);
+                    const uint4 val = ld_shared_v4(stage + rr * 64 + ((j ^ ((rr >> 1) & 3)) << 4));
+                    if (((valid_mask >> rr) & 1u) && n0 + col < N) {
+                        const int grow = row0w + rr;
+                        const size_t orow = static_cast<size_t>(shared ? grow : C.g[w.g].row0 + grow);
+                        st_stream_v4(out_base + orow * N + n0 + col, val);
                     }
                 }
+                __syncwarp();  // the next block rewrites the staging area
             }
         }
     }
