@@ -17,10 +17,11 @@
 //              operand, and the stage's scale atoms (below).
 //   warp 1     one thread issues the MMAs of a stage once its codes have
 //              landed and its scale atoms are in TMEM.
-//   warp 10    one thread copies each stage's scale atoms from shared memory
-//              into TMEM (tcgen05.cp .32x128b.warpx4) as soon as they land,
-//              then commits to the stage's sfready barrier; the copies no
-//              longer sit in the MMA thread's issue stream.
+//   warps 10-11 one thread each copies a stage's scale atoms from shared
+//              memory into TMEM (tcgen05.cp .32x128b.warpx4) as soon as they
+//              land, warp 10 A's and warp 11 B's, then commits to the
+//              stage's sfready barrier (two arrivals); the copies do not sit
+//              in the MMA thread's issue stream.
 //   warps 2-9  epilogue, two warps per TMEM lane quarter, each draining half
 //              of the columns: TMEM -> registers -> bf16 (nearest even) ->
 //              global, rows past the group's end and columns past N masked.
@@ -59,10 +60,11 @@ constexpr int MX_CH = 2;         // K chunks per stage
 constexpr int MX_BK = MX_KCHUNK * MX_CH;
 constexpr int MX_STAGES = 3;
 constexpr int kMxEpiWarps = 8;  // two per TMEM lane quarter, each draining half of the columns
-constexpr int MX_THREADS = (3 + kMxEpiWarps) * 32;
+constexpr int MX_THREADS = (4 + kMxEpiWarps) * 32;
 constexpr int kMxMmaWarp = 1;
 constexpr int kMxEpiWarp0 = 2;
-constexpr int kMxScaleWarp = kMxEpiWarp0 + kMxEpiWarps;  // copies each stage's scale atoms into TMEM
+constexpr int kMxScaleWarp = kMxEpiWarp0 + kMxEpiWarps;  // copies each stage's A scale atoms into TMEM
+constexpr int kMxScaleWarpB = kMxScaleWarp + 1;          // and this one its B scale atoms
 constexpr int MX_ATOM_ROWS = 128;     // rows (columns) of a block that one scale atom covers
 constexpr uint32_t MX_ATOM_BYTES = 512;  // 32 rows of 16 bytes
 constexpr uint32_t kMxAtomLine = 128;    // atoms move as 128-byte lines: 8 atom rows each
@@ -469,7 +471,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
             for (int s = 0; s < MX_STAGES; ++s) {
                 mbar_init(smem_u32(&C.full[s]), 1);
                 mbar_init(smem_u32(&C.empty[s]), 1);
-                mbar_init(smem_u32(&C.sfready[s]), 1);
+                mbar_init(smem_u32(&C.sfready[s]), 2);
             }
             for (int a = 0; a < 2; ++a) {
                 mbar_init(smem_u32(&C.tfull[a]), 1);
@@ -605,8 +607,9 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 if (ok) mx_commit<PAIR>(smem_u32(&C.tfull[acc]));
             }
         }
-    } else if (warp == kMxScaleWarp) {
+    } else if (warp == kMxScaleWarp || warp == kMxScaleWarpB) {
         // =========================================================== scale atoms into TMEM
+        const bool copy_a = warp == kMxScaleWarp;
         if (lane == 0 && rank == 0) {
             uint32_t it = 0;
             bool ok = true;
@@ -627,13 +630,16 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     const uint32_t sfa = C.tmem_base + sfa_col<PAIR>(s);
                     const uint32_t sfb = C.tmem_base + sfb_col<PAIR>(s);
                     const uint32_t sf_st = sf_smem + s * S::kSfStageBytes;
+                    if (copy_a) {
 #pragma unroll
-                    for (int j = 0; j < MX_CH; ++j) {
-                        mx_sf_copy<PAIR>(sfa + 4 * j, sf_st + j * MX_ATOM_BYTES);
+                        for (int j = 0; j < MX_CH; ++j) mx_sf_copy<PAIR>(sfa + 4 * j, sf_st + j * MX_ATOM_BYTES);
+                    } else {
 #pragma unroll
-                        for (int i = 0; i < kCtas; ++i)
-                            mx_sf_copy<PAIR>(sfb + NB * j + 4 * i,
-                                             sf_st + S::kSfaBytes + (j * kCtas + i) * MX_ATOM_BYTES);
+                        for (int j = 0; j < MX_CH; ++j)
+#pragma unroll
+                            for (int i = 0; i < kCtas; ++i)
+                                mx_sf_copy<PAIR>(sfb + NB * j + 4 * i,
+                                                 sf_st + S::kSfaBytes + (j * kCtas + i) * MX_ATOM_BYTES);
                     }
                     mx_commit_own<PAIR>(smem_u32(&C.sfready[s]));
                 }
