@@ -730,9 +730,9 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
 // operands: the expert-major copy of rows' H1 code bytes (and, into
 // permuteOut, their H1/32 scale bytes), in 2 KB pieces per warp.  Without
 // permuteOut only rows of 128-row halves that straddle a segment boundary are
-// copied (the GEMM reads the others in place).  Then its threads write every
-// operand's scale atoms (see the top of this file), one 16-byte atom row at a
-// time.
+// copied (the GEMM reads the others in place).  Then its warps write every
+// operand's scale atoms (see the top of this file), four atoms of one block
+// per warp.
 constexpr int kMxPermThreads = 256;
 constexpr int kPieceVecs = 4;  // 16-byte vectors per lane in one work item (2 KB per warp)
 
@@ -757,20 +757,6 @@ __device__ __forceinline__ uint4 mx_ld_stream(const uint4 *ptr) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(ptr));
     return v;
-}
-
-// Row l of an atom: the quad's four scale bytes (byte offset q4 in each scale
-// row) of block rows l, 32 + l, 64 + l, 96 + l; 127 (a scale of 1) for rows at
-// or past `valid`.  row(r) is the scale row of block row r.
-template <typename Row>
-__device__ __forceinline__ uint4 mx_atom_row(const Row &row, int valid, int l, int q4) {
-    uint32_t w[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int r = 32 * c + l;
-        w[c] = r < valid ? *reinterpret_cast<const uint32_t *>(row(r) + q4) : 0x7F7F7F7Fu;
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 __global__ void __launch_bounds__(kMxPermThreads) mx_prep_kernel(const __grid_constant__ MxPrep p) {
@@ -878,46 +864,69 @@ __global__ void __launch_bounds__(kMxPermThreads) mx_prep_kernel(const __grid_co
     const int64_t rows_x = p.BS > 0 ? static_cast<int64_t>((p.BS + MX_ATOM_ROWS - 1) / MX_ATOM_ROWS) * nq2 * 32 : 0;
     const int64_t rows_b = p.A > 0 ? static_cast<int64_t>(e) * nq1 * ncb1 * 32 : 0;
     const int64_t rows_w = p.BS > 0 ? static_cast<int64_t>(nq2) * ncb2 * 32 : 0;
-    const int64_t all = rows_a + rows_x + rows_b + rows_w;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kMxPermThreads;
+    // Work items are groups of four atoms: one 128-row (column) block and
+    // quads 4k .. 4k + 3 (H is a multiple of 512, so the quads of a row
+    // come in fours).  A warp takes an item: lane l loads the 16 bytes of
+    // those quads from each of its rows l, 32 + l, 64 + l, 96 + l, and writes
+    // row l of each of the four atoms, so one store instruction fills an atom.
+    const int64_t items_a = rows_a / 128, items_x = rows_x / 128, items_b = rows_b / 128, items_w = rows_w / 128;
+    const int64_t items = items_a + items_x + items_b + items_w;
+    const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * (kMxPermThreads / 32) + threadIdx.x / 32;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kMxPermThreads / 32);
     const size_t kb1 = static_cast<size_t>(H1 / 32), kb2 = static_cast<size_t>(p.H2 / 32);
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kMxPermThreads + threadIdx.x; i < all; i += stride) {
-        const int l = static_cast<int>(i % 32);
-        if (i < rows_a) {
-            const int atom = static_cast<int>(i / 32);
-            const int h = atom / nq1, q = atom - h * nq1;
+    const int nk1 = nq1 / 4, nk2 = nq2 / 4;
+    // Row l of atoms (block, quads 4k .. 4k + 3) from the scale rows row(r):
+    // rows at or past `valid` read as 127 (a scale of 1).
+    const auto write_atoms = [&](const auto &row, int valid, int k, uint8_t *atoms, int64_t atom0, int64_t step) {
+        uint4 w[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int r = 32 * c + lane;
+            w[c] = r < valid ? *reinterpret_cast<const uint4 *>(row(r) + 16 * k)
+                             : make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 v = j == 0 ? make_uint4(w[0].x, w[1].x, w[2].x, w[3].x)
+                          : j == 1 ? make_uint4(w[0].y, w[1].y, w[2].y, w[3].y)
+                          : j == 2 ? make_uint4(w[0].z, w[1].z, w[2].z, w[3].z)
+                                   : make_uint4(w[0].w, w[1].w, w[2].w, w[3].w);
+            reinterpret_cast<uint4 *>(atoms + static_cast<size_t>(atom0 + j * step) * MX_ATOM_BYTES)[lane] = v;
+        }
+    };
+    for (int64_t i = gwarp; i < items; i += nwarps) {
+        if (i < items_a) {
+            const int h = static_cast<int>(i / nk1), k = static_cast<int>(i % nk1);
             int g = 0;
             while (h >= half0[g + 1]) ++g;  // the expert group holding half h
             const int first = table.dst[g * W] + (h - half0[g]) * MX_ATOM_ROWS;
             const int valid = min(MX_ATOM_ROWS, table.dst[(g + 1) * W] - first);
             const auto row = [&](int r) { return p.src_s + static_cast<size_t>(source_row(table, W, e, first + r)) * kb1; };
-            reinterpret_cast<uint4 *>(p.sfa + static_cast<size_t>(atom) * MX_ATOM_BYTES)[l] =
-                mx_atom_row(row, valid, l, 4 * q);
-        } else if (i < rows_a + rows_x) {
-            const int atom = static_cast<int>((i - rows_a) / 32);
-            const int h = atom / nq2, q = atom - h * nq2;
+            write_atoms(row, valid, k, p.sfa, static_cast<int64_t>(h) * nq1 + 4 * k, 1);
+        } else if (i < items_a + items_x) {
+            const int64_t ix = i - items_a;
+            const int h = static_cast<int>(ix / nk2), k = static_cast<int>(ix % nk2);
             const int first = h * MX_ATOM_ROWS;
             const auto row = [&](int r) { return p.x_s + static_cast<size_t>(first + r) * kb2; };
-            reinterpret_cast<uint4 *>(p.sfx + static_cast<size_t>(atom) * MX_ATOM_BYTES)[l] =
-                mx_atom_row(row, min(MX_ATOM_ROWS, p.BS - first), l, 4 * q);
-        } else if (i < rows_a + rows_x + rows_b) {
+            write_atoms(row, min(MX_ATOM_ROWS, p.BS - first), k, p.sfx, static_cast<int64_t>(h) * nq2 + 4 * k, 1);
+        } else if (i < items_a + items_x + items_b) {
             // Atom (z, q, cb) of gmmWeight: plane z * nq1 + q, block cb.
-            const int atom = static_cast<int>((i - rows_a - rows_x) / 32);
-            const int cb = atom % ncb1, plane = atom / ncb1;
-            const int z = plane / nq1, q = plane - z * nq1;
+            const int64_t ib = i - items_a - items_x;
+            const int cb = static_cast<int>(ib % ncb1);
+            const int64_t rest = ib / ncb1;
+            const int z = static_cast<int>(rest / nk1), k = static_cast<int>(rest % nk1);
             const int first = cb * MX_ATOM_ROWS;
             const auto row = [&](int r) {
                 return p.w_s + (static_cast<size_t>(z) * p.N1 + static_cast<size_t>(first + r)) * kb1;
             };
-            reinterpret_cast<uint4 *>(p.sfb + static_cast<size_t>(atom) * MX_ATOM_BYTES)[l] =
-                mx_atom_row(row, min(MX_ATOM_ROWS, p.N1 - first), l, 4 * q);
+            write_atoms(row, min(MX_ATOM_ROWS, p.N1 - first), k, p.sfb,
+                        (static_cast<int64_t>(z) * nq1 + 4 * k) * ncb1 + cb, ncb1);
         } else {
-            const int atom = static_cast<int>((i - rows_a - rows_x - rows_b) / 32);
-            const int cb = atom % ncb2, q = atom / ncb2;
+            const int64_t iw = i - items_a - items_x - items_b;
+            const int cb = static_cast<int>(iw % ncb2), k = static_cast<int>(iw / ncb2);
             const int first = cb * MX_ATOM_ROWS;
             const auto row = [&](int r) { return p.mw_s + static_cast<size_t>(first + r) * kb2; };
-            reinterpret_cast<uint4 *>(p.sfw + static_cast<size_t>(atom) * MX_ATOM_BYTES)[l] =
-                mx_atom_row(row, min(MX_ATOM_ROWS, p.N2 - first), l, 4 * q);
+            write_atoms(row, min(MX_ATOM_ROWS, p.N2 - first), k, p.sfw, static_cast<int64_t>(4 * k) * ncb2 + cb, ncb2);
         }
     }
 }
