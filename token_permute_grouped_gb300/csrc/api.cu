@@ -126,6 +126,21 @@ bool make_rows_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [rows, cols] row-major output; box = 32 columns x 32 rows, 64-byte
+// swizzle: the layout in which an epilogue warp turns a block around in
+// shared memory before the TMA store.
+bool make_out_map(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, int32_t dtype) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, tmap_type(dtype), 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // [groups, K, N] row-major weights; box = 64 columns (N) x 64 rows (K) x 1.
 bool make_weight_map(CUtensorMap *m, const void *ptr, int64_t groups, int64_t K, int64_t N, int32_t dtype) {
     auto fn = encode_fn();
@@ -271,6 +286,8 @@ a2av_status run_impl(const a2av_gmm_desc *desc, const void *ataOut, const int32_
     g.bn2 = has_shared ? pick_bn(d.N2, use_pair(&d) ? 2 : 1) : 0;
     g.gmmY = gmmY;
     g.mmY = mmY;
+    if (has_routed && !make_out_map(&g.tmY_routed, gmmY, d.A, d.N1, d.dtype)) return A2AV_ERR_CUDA;
+    if (has_shared && !make_out_map(&g.tmY_shared, mmY, d.BS, d.N2, d.dtype)) return A2AV_ERR_CUDA;
     g.status = status;
     g.bf16 = d.dtype == A2AV_BF16;
     g.gather = split ? 0 : 1;

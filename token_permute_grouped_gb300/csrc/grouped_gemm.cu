@@ -100,14 +100,17 @@ struct Control {
 };
 
 // Epilogue staging: each epilogue warp turns its 32 rows x 32 columns of
-// 16-bit results around in 2 KB of shared memory, so that a store writes 8
-// rows of 64 contiguous bytes instead of 16 bytes in each of 32 rows.
-constexpr uint32_t kEpiStageBytes = 32 * 64;
+// 16-bit results around in 2 KB of shared memory (two such buffers per warp,
+// alternating), in the TMA's 64-byte swizzle; a block whose 32 rows are all
+// in the group then goes out as one TMA store, any other as masked stores of
+// 8 rows of 64 contiguous bytes.
+constexpr uint32_t kEpiStageBytes = 2 * 32 * 64;
+constexpr uint32_t kEpiBufBytes = 32 * 64;
 constexpr int kEpiWarps = 4;
 
 template <int STAGES>
 __host__ __device__ constexpr size_t epi_stage_offset() {
-    return (sizeof(Control<STAGES>) + 127) / 128 * 128;
+    return (sizeof(Control<STAGES>) + 1023) / 1024 * 1024;  // the swizzle pattern repeats every 512 bytes
 }
 
 template <bool PAIR, int CH>
@@ -506,12 +509,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
     } else if (warp == 2) {
         if (lane == 0) {
-            if (p.A > 0) prefetch_tensormap(&p.tmA_routed);
+            if (p.A > 0) {
+                prefetch_tensormap(&p.tmA_routed);
+                prefetch_tensormap(&p.tmY_routed);
+            }
             if (p.direct_halves) prefetch_tensormap(&p.tmA_direct);
             prefetch_tensormap(p.b4_routed ? &p.tmB4_routed : &p.tmB_routed);
             if (p.BS > 0) {
                 prefetch_tensormap(&p.tmA_shared);
                 prefetch_tensormap(p.b4_shared ? &p.tmB4_shared : &p.tmB_shared);
+                prefetch_tensormap(&p.tmY_shared);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -777,6 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const int q = warp & 3;  // TMEM lane quarter this warp may read
         const uint32_t tempty0 = smem_u32(&C.tempty[0]);
         uint32_t tl = 0;
+        uint32_t nblk = 0;  // blocks staged so far: the buffer alternates across tiles too
         for (int t = unit; t < total; t += nunits, ++tl) {
             const Tile w = tile_at(t);
             const bool shared = w.g >= e;
@@ -808,13 +816,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const size_t orow = static_cast<size_t>(shared ? rr : C.g[w.g].row0 + rr);
                 out_k[k] = out_base + orow * N + n0;
             }
-            // 64-byte rows; the 16-byte chunk index is XORed with (row / 2) % 4,
-            // so that both the row-wise writes and the column-wise reads touch
-            // eight distinct 16-byte slots of each 128 bytes.
+            // 64-byte rows; the 16-byte chunk index is XORed with (row / 2) % 4
+            // (the TMA's 64-byte swizzle), so that both the row-wise writes and
+            // the column-wise reads touch eight distinct 16-byte slots of each
+            // 128 bytes.
             const uint32_t stage = epi0 + static_cast<uint32_t>(warp - kMmaWarp - 1) * kEpiStageBytes;
+            const bool all_rows = __all_sync(0xffffffffu, valid);
+            const CUtensorMap *tmy = shared ? &p.tmY_shared : &p.tmY_routed;
+            const int orow0 = shared ? row0w : C.g[w.g].row0 + row0w;
             for (int c = 0; c < nchunks; ++c) {
+                const uint32_t buf = stage + (nblk++ & 1u) * kEpiBufBytes;
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(t_base + c * 32, r);
+                // Every block commits one bulk group (empty unless it went out by
+                // TMA), so this wait leaves only the previous block's store
+                // pending: the store that read this buffer two blocks ago is done.
+                if (lane == 0) bulk_wait_read_1();
+                __syncwarp();
                 tmem_ld_wait();
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
@@ -823,19 +841,34 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     pk.y = pack2<BF16>(r[v * 8 + 2], r[v * 8 + 3]);
                     pk.z = pack2<BF16>(r[v * 8 + 4], r[v * 8 + 5]);
                     pk.w = pack2<BF16>(r[v * 8 + 6], r[v * 8 + 7]);
-                    st_shared_v4(stage + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4), pk);
+                    st_shared_v4(buf + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4), pk);
                 }
-                __syncwarp();
-                const int v = lane & 3;
-                const int col = c * 32 + v * 8;
-                const bool col_ok = col < bn && n0 + col < N;
+                // A block of whole rows inside this tile's columns goes out as
+                // one TMA store (columns past N are clipped by the map);
+                // anything else by masked stores.
+                if (all_rows && (c + 1) * 32 <= bn && n0 + c * 32 < N) {
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(tmy, buf, n0 + c * 32, orow0);
+                        bulk_commit_group();
+                    }
+                } else {
+                    // An empty group, so that "all but the most recent group"
+                    // above always means "all but the previous block's".
+                    if (lane == 0) bulk_commit_group();
+                    __syncwarp();
+                    const int v = lane & 3;
+                    const int col = c * 32 + v * 8;
+                    const bool col_ok = col < bn && n0 + col < N;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int rr = 8 * k + (lane >> 2);
-                    const uint4 val = ld_shared_v4(stage + rr * 64 + ((v ^ ((rr >> 1) & 3)) << 4));
-                    if (ok_k[k] && col_ok) st_stream_v4(out_k[k] + col, val);
+                    for (int k = 0; k < 4; ++k) {
+                        const int rr = 8 * k + (lane >> 2);
+                        const uint4 val = ld_shared_v4(buf + rr * 64 + ((v ^ ((rr >> 1) & 3)) << 4));
+                        if (ok_k[k] && col_ok) st_stream_v4(out_k[k] + col, val);
+                    }
                 }
-                __syncwarp();  // the next chunk rewrites the staging area
+                __syncwarp();  // the buffer is rewritten two blocks later
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -845,6 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 else mbar_arrive(te);
             }
         }
+        if (lane == 0) bulk_wait_all();  // this warp's TMA stores have landed
     }
 
     tc_fence_before_sync();

@@ -52,6 +52,8 @@ struct GemmLaunch {
     int32_t direct_halves;    // 1: halves inside one segment are read from ataOut directly
     CUtensorMap tmB4_routed;  // gmmWeight as 64-column atoms: one load per stage (when b4_routed)
     CUtensorMap tmB4_shared;  // mmWeight likewise (when b4_shared)
+    CUtensorMap tmY_routed;   // gmmY [A, N1], box 32 x 32, 64-byte swizzle (epilogue stores)
+    CUtensorMap tmY_shared;   // mmY [BS, N2], likewise
     int32_t b4_routed, b4_shared;
     int32_t after_permute;    // 1: launched to overlap the permute kernel before it (programmatic
                               // dependent launch); the producer waits for it before staged loads

@@ -108,6 +108,23 @@ __device__ __forceinline__ void st_stream_v4(void *ptr, uint4 v) {
                  : "memory");
 }
 
+// TMA tiled store of a 2-D box from shared memory (bulk async-group), and the
+// group bookkeeping around it.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// At most one of this thread's bulk groups still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Generic-proxy writes to shared memory, made visible to a later TMA read.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // TMA tiled loads.  The innermost coordinate must give a 16-byte aligned
 // start (x * element size a multiple of 16); out-of-range elements are filled
 // with zeros and still count toward the transaction bytes.
