@@ -136,6 +136,9 @@ struct MxLaunch {
     CUtensorMap tmSFX;  // mmX: halves of the BS rows
     CUtensorMap tmSFB;  // gmmWeight: 128-column blocks of each expert
     CUtensorMap tmSFW;  // mmWeight: 128-column blocks
+    // Outputs for the epilogue's TMA stores: 32 x 32 boxes, 64-byte swizzle.
+    CUtensorMap tmY_routed;  // gmmY [A, N1] bf16
+    CUtensorMap tmY_shared;  // mmY [BS, N2] bf16
     // Halves of a tile (this CTA's 128 rows) whose rows of the group lie in
     // one (source, expert) segment are read in place from ataOut; the permute
     // kernel staged only the others (see half_in_one_segment).
@@ -178,7 +181,8 @@ struct MxControl {
 // Epilogue staging: each epilogue warp turns a 32 x 32 block of bf16 results
 // around in 2 KB of shared memory (see the epilogue), after the control block.
 constexpr uint32_t kMxEpiStageBytes = 32 * 64;
-__host__ __device__ constexpr size_t mx_epi_offset() { return (sizeof(MxControl) + 127) / 128 * 128; }
+// 1024-aligned: the TMA's 64-byte swizzle pattern repeats every 512 bytes.
+__host__ __device__ constexpr size_t mx_epi_offset() { return (sizeof(MxControl) + 1023) / 1024 * 1024; }
 
 template <bool PAIR>
 constexpr size_t mx_smem_bytes() {
@@ -488,6 +492,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 prefetch_tensormap(&p.tmB);
                 prefetch_tensormap(&p.tmSFA);
                 prefetch_tensormap(&p.tmSFB);
+                prefetch_tensormap(&p.tmY_routed);
                 if (p.direct_halves) prefetch_tensormap(&p.tmA_direct);
             }
             if (p.BS > 0) {
@@ -495,6 +500,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 prefetch_tensormap(&p.tmMW);
                 prefetch_tensormap(&p.tmSFX);
                 prefetch_tensormap(&p.tmSFW);
+                prefetch_tensormap(&p.tmY_shared);
             }
         }
     }
@@ -685,8 +691,13 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
             const uint32_t valid_mask = __ballot_sync(0xffffffffu, valid);
             const int row0w = row - lane;
             const uint32_t stage = epi0 + static_cast<uint32_t>(warp - kMxEpiWarp0) * kMxEpiStageBytes;
+            const CUtensorMap *tmy = shared ? &p.tmY_shared : &p.tmY_routed;
+            const int orow0 = shared ? row0w : C.g[w.g].row0 + row0w;
 #pragma unroll
             for (int i = 0; i < kChunks; ++i) {
+                // The previous block's TMA store (if any) has read the buffer.
+                if (lane == 0) bulk_wait_read_0();
+                __syncwarp();
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const uint32_t *r = v[i] + j * 8;
@@ -697,17 +708,29 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     pk.w = pack_bf16(r[6], r[7]);
                     st_shared_v4(stage + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pk);
                 }
-                __syncwarp();
-                const int j = lane & 3;
-                const int col = (c0 + i) * 32 + j * 8;
+                const int blk_col = n0 + (c0 + i) * 32;
+                if (valid_mask == 0xffffffffu && blk_col < N) {
+                    // 32 whole rows of the group: one TMA store (columns past N
+                    // are clipped by the map).
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(tmy, stage, blk_col, orow0);
+                        bulk_commit_group();
+                    }
+                } else {
+                    __syncwarp();
+                    const int j = lane & 3;
+                    const int col = (c0 + i) * 32 + j * 8;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int rr = 8 * k + (lane >> 2);
-                    const uint4 val = ld_shared_v4(stage + rr * 64 + ((j ^ ((rr >> 1) & 3)) << 4));
-                    if (((valid_mask >> rr) & 1u) && n0 + col < N) {
-                        const int grow = row0w + rr;
-                        const size_t orow = static_cast<size_t>(shared ? grow : C.g[w.g].row0 + grow);
-                        st_stream_v4(out_base + orow * N + n0 + col, val);
+                    for (int k = 0; k < 4; ++k) {
+                        const int rr = 8 * k + (lane >> 2);
+                        const uint4 val = ld_shared_v4(stage + rr * 64 + ((j ^ ((rr >> 1) & 3)) << 4));
+                        if (((valid_mask >> rr) & 1u) && n0 + col < N) {
+                            const int grow = row0w + rr;
+                            const size_t orow = static_cast<size_t>(shared ? grow : C.g[w.g].row0 + grow);
+                            st_stream_v4(out_base + orow * N + n0 + col, val);
+                        }
                     }
                 }
                 __syncwarp();  // the next block rewrites the staging area
@@ -715,6 +738,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
         }
     }
 
+    if (warp >= kMxEpiWarp0 && warp < kMxEpiWarp0 + kMxEpiWarps && lane == 0)
+        bulk_wait_all();  // this warp's TMA stores have landed
     tc_fence_before_sync();
     if constexpr (PAIR) mx_cluster_sync();
     else __syncthreads();
@@ -999,6 +1024,20 @@ PFN_cuTensorMapEncodeTiled_v12000 mx_encode_fn() {
 // Byte codes [groups][rows][K] seen as 4-D {128 codes, rows, K / 128 chunks,
 // groups}; box 128 x 128 x MX_CH x 1, 128-byte swizzle: one load lands a
 // stage's K chunks as consecutive 16 KB K-major sub-tiles.  Needs K % 256 == 0.
+// bf16 outputs [rows, cols]; box 32 x 32, 64-byte swizzle (the epilogue's
+// staging layout).
+bool mx_out_map(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols) {
+    auto fn = mx_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 bool mx_codes_map(CUtensorMap *m, const void *ptr, int64_t groups, int64_t rows, int64_t K) {
     auto fn = mx_encode_fn();
     if (!fn) return false;
@@ -1114,6 +1153,8 @@ a2av_status mx_run_impl(const a2av_gmm_mx_desc *desc, const void *ataOut_q, cons
     g.N2 = shared ? static_cast<int32_t>(d.N2) : 0;
     g.gmmY = gmmY;
     g.mmY = mmY;
+    if (routed && !mx_out_map(&g.tmY_routed, gmmY, d.A, d.N1)) return A2AV_ERR_CUDA;
+    if (shared && !mx_out_map(&g.tmY_shared, mmY, d.BS, d.N2)) return A2AV_ERR_CUDA;
     g.status = status;
     g.qtype = d.qtype;
     const bool pair = d.tiles != A2AV_TILES_SINGLE;

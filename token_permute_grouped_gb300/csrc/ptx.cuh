@@ -119,6 +119,8 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // At most one of this thread's bulk groups still reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// None of this thread's bulk groups still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Generic-proxy writes to shared memory, made visible to a later TMA read.
 __device__ __forceinline__ void fence_proxy_async_shared() {
