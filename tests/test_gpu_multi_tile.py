@@ -42,6 +42,13 @@ SHAPES = {
     # 5.5 tiles of 256 columns), and a shared expert with its own K and a
     # width that is not a multiple of 64.
     "w4e8_a20k_h128_n1408_fp16": (4, 8, 128, 1408, 20000, 0.25, 1000, 384, 200, "fp16", 13),
+    # 32 experts of random size: nearly every group ends in a partial tile, whose
+    # output blocks take the masked path while whole blocks go out by TMA
+    # store; N1 = 288 gives 144-wide column tiles whose last 32-column chunk
+    # runs past the tile (masked), and the shared expert's 200 columns a
+    # 208-wide tile.  So full and masked blocks alternate within and across
+    # a unit's tiles, which is what the epilogue's buffer reuse must survive.
+    "w8e32_a40k_h128_n288": (8, 32, 128, 288, 40000, 0.1, 1500, 128, 200, "bf16", 14),
 }
 
 

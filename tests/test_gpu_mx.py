@@ -186,31 +186,42 @@ def test_full_size_headline(orc):
 
 _MULTI = {}
 
-
-def _multi_tile_case():
+# (W, e, H1, N1, A, zero_prob, BS, H2, N2, seed)
+MULTI_CASES = {
     # About 24K routed rows and a 4096-row shared expert: with 256 x 256 pair
     # tiles about six tiles per pair unit, with 128 x 128 single tiles about
     # eleven per CTA.  Each unit therefore reuses its accumulator and scale
     # columns across tiles and wraps its stage ring many times.
-    if not _MULTI:
-        rc = random_counts(8, 4, 24000, seed=21, zero_prob=0.05)
-        inp = _custom(8, 4, 512, 1024, rc, "e4m3fn", BS=4096, H2=512, N2=1024, seed=21)
-        _MULTI["inp"] = inp
-    return _MULTI["inp"]
+    "w8e4_a24k_n1024": (8, 4, 512, 1024, 24000, 0.05, 4096, 512, 1024, 21),
+    # 32 experts of random size, N1 = 288 and N2 = 200: partial row tiles and
+    # a last column tile only partly inside N, so blocks that go out by TMA
+    # store and blocks that take the masked path alternate in every unit.
+    "w8e32_a40k_n288": (8, 32, 512, 288, 40000, 0.1, 1500, 512, 200, 22),
+}
+
+
+def _multi_tile_case(name):
+    if name not in _MULTI:
+        W, e, H1, N1, A, zero, BS, H2, N2, seed = MULTI_CASES[name]
+        rc = random_counts(W, e, A, seed=seed, zero_prob=zero)
+        _MULTI[name] = {"inp": _custom(W, e, H1, N1, rc, "e4m3fn", BS=BS, H2=H2, N2=N2, seed=seed)}
+    return _MULTI[name]
 
 
 @pytest.mark.parametrize("tiles", TILES)
-def test_multi_tile_every_element(orc, tiles):
-    inp = _multi_tile_case()
+@pytest.mark.parametrize("name", sorted(MULTI_CASES))
+def test_multi_tile_every_element(orc, name, tiles):
+    case = _multi_tile_case(name)
+    inp = case["inp"]
     (y, m, _, _), st = run_mx(inp, tiles=tiles)
     assert st[0] == 0, st
-    if "ref" not in _MULTI:
-        _MULTI["ref"] = reference(orc, inp)
-        _MULTI["first"] = (y, m)
-    _, _, ref_y, ref_m = _MULTI["ref"]
+    if "ref" not in case:
+        case["ref"] = reference(orc, inp)
+        case["first"] = (y, m)
+    _, _, ref_y, ref_m = case["ref"]
     assert_close(y, ref_y, "gmmY")
     assert_close(m, ref_m, "mmY")
     # Both tile shapes give the same bits.
-    y0, m0 = _MULTI["first"]
+    y0, m0 = case["first"]
     assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
     assert torch.equal(m.view(torch.int16), m0.view(torch.int16))
