@@ -14,7 +14,8 @@
 //   warp 0     one thread issues a stage's TMA loads: the A rows (read in
 //              place from ataOut, or from the prep kernel's staging copy),
 //              the K-major weight columns, one 4-D load of both sub-tiles per
-//              operand, and the stage's scale atoms (below).
+//              operand, and before them the stage's scale atoms (below),
+//              which complete on a barrier of their own.
 //   warp 1     one thread issues the MMAs of a stage once its codes have
 //              landed and its scale atoms are in TMEM.
 //   warps 10-11 one thread each copies a stage's scale atoms from shared
@@ -166,7 +167,8 @@ struct MxGroup {
 };
 
 struct MxControl {
-    uint64_t full[MX_STAGES];   // a stage's codes and scale atoms landed (pair: both CTAs'; in the even CTA)
+    uint64_t full[MX_STAGES];   // a stage's codes landed (pair: both CTAs'; in the even CTA)
+    uint64_t sffull[MX_STAGES];   // a stage's scale atoms landed (the same)
     uint64_t empty[MX_STAGES];  // the copies and MMAs reading a stage completed
     uint64_t sfready[MX_STAGES];  // a stage's scale atoms are in TMEM (in the even CTA)
     uint64_t tfull[2];
@@ -474,6 +476,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
         if (lane == 0) {
             for (int s = 0; s < MX_STAGES; ++s) {
                 mbar_init(smem_u32(&C.full[s]), 1);
+                mbar_init(smem_u32(&C.sffull[s]), 1);
                 mbar_init(smem_u32(&C.empty[s]), 1);
                 mbar_init(smem_u32(&C.sfready[s]), 2);
             }
@@ -548,17 +551,24 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     }
                     const uint32_t fb_own = smem_u32(&C.full[s]);
                     const uint32_t fb = PAIR ? mx_map_to_rank(fb_own, 0) : fb_own;  // the MMA CTA's barrier
-                    if (rank == 0)
-                        mbar_arrive_expect_tx(fb_own, kCtas * (2 * MX_TILE_BYTES + S::kSfStageBytes));
+                    const uint32_t sb_own = smem_u32(&C.sffull[s]);
+                    const uint32_t sb = PAIR ? mx_map_to_rank(sb_own, 0) : sb_own;
+                    if (rank == 0) {
+                        mbar_arrive_expect_tx(sb_own, kCtas * S::kSfStageBytes);
+                        mbar_arrive_expect_tx(fb_own, kCtas * 2 * MX_TILE_BYTES);
+                    }
+                    // Scale atoms of quads 2kb and 2kb + 1 first, on their own
+                    // barrier: this half's, then each of the tile's column
+                    // blocks'.  They land while the stage's 64 KB of codes
+                    // are still streaming in, so the copier warps have them
+                    // in TMEM by the time the codes are complete.
+                    const uint32_t sf_st = sf_smem + s * S::kSfStageBytes;
+                    constexpr int kLines = 32 / kMxAtomLineRows;  // 128-byte lines per atom
+                    tma_load_3d_mx<PAIR>(sf_st, tsa, sb, 0, kLines * (half * nq + MX_CH * kb), 0);
+                    tma_load_3d_mx<PAIR>(sf_st + S::kSfaBytes, tsb, sb, 0, kLines * cb0, z * nq + MX_CH * kb);
                     // {chunk column, row, chunk, group}: both chunks of the stage.
                     tma_load_4d_mx<PAIR>(a_smem + s * MX_TILE_BYTES, ta, fb, 0, ya, kb * MX_CH, 0);
                     tma_load_4d_mx<PAIR>(b_smem + s * MX_TILE_BYTES, tb, fb, 0, xn, kb * MX_CH, z);
-                    // Scale atoms of quads 2kb and 2kb + 1: this half's, then
-                    // each of the tile's column blocks'.
-                    const uint32_t sf_st = sf_smem + s * S::kSfStageBytes;
-                    constexpr int kLines = 32 / kMxAtomLineRows;  // 128-byte lines per atom
-                    tma_load_3d_mx<PAIR>(sf_st, tsa, fb, 0, kLines * (half * nq + MX_CH * kb), 0);
-                    tma_load_3d_mx<PAIR>(sf_st + S::kSfaBytes, tsb, fb, 0, kLines * cb0, z * nq + MX_CH * kb);
                 }
             }
             // Wait until the MMAs released every stage that was filled.
@@ -624,7 +634,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                 const int K = w.g >= e ? p.H2 : p.H1;
                 for (int kb = 0; kb < K / MX_BK; ++kb, ++it) {
                     const int s = it % MX_STAGES;
-                    if (!mx_wait(&C.abort, &C.full[s], (it / MX_STAGES) & 1, p.status)) {
+                    if (!mx_wait(&C.abort, &C.sffull[s], (it / MX_STAGES) & 1, p.status)) {
                         ok = false;
                         break;
                     }
