@@ -21,8 +21,10 @@
 //   warps 10-11 one thread each copies a stage's scale atoms from shared
 //              memory into TMEM (tcgen05.cp .32x128b.warpx4) as soon as they
 //              land, warp 10 A's and warp 11 B's, then commits to the
-//              stage's sfready barrier (two arrivals); the copies do not sit
-//              in the MMA thread's issue stream.
+//              stage's full barrier, which the codes' bytes and the
+//              producer's arrival also complete (three arrivals): the MMA
+//              thread waits once per stage, and the copies do not sit in its
+//              issue stream.
 //   warps 2-9  epilogue, two warps per TMEM lane quarter, each draining half
 //              of the columns: TMEM -> registers -> bf16 (nearest even) ->
 //              global, rows past the group's end and columns past N masked.
@@ -167,10 +169,9 @@ struct MxGroup {
 };
 
 struct MxControl {
-    uint64_t full[MX_STAGES];   // a stage's codes landed (pair: both CTAs'; in the even CTA)
-    uint64_t sffull[MX_STAGES];   // a stage's scale atoms landed (the same)
+    uint64_t full[MX_STAGES];    // a stage's codes landed and its atoms are in TMEM (pair: in the even CTA)
+    uint64_t sffull[MX_STAGES];  // a stage's scale atoms landed (pair: both CTAs'; in the even CTA)
     uint64_t empty[MX_STAGES];  // the copies and MMAs reading a stage completed
-    uint64_t sfready[MX_STAGES];  // a stage's scale atoms are in TMEM (in the even CTA)
     uint64_t tfull[2];
     uint64_t tempty[2];           // epilogue drained the accumulator (pair: both CTAs; in the even CTA)
     uint32_t tmem_base;
@@ -475,10 +476,9 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
     } else if (warp == kMxMmaWarp) {
         if (lane == 0) {
             for (int s = 0; s < MX_STAGES; ++s) {
-                mbar_init(smem_u32(&C.full[s]), 1);
+                mbar_init(smem_u32(&C.full[s]), 3);  // the producer's arrival and both copiers' commits
                 mbar_init(smem_u32(&C.sffull[s]), 1);
                 mbar_init(smem_u32(&C.empty[s]), 1);
-                mbar_init(smem_u32(&C.sfready[s]), 2);
             }
             for (int a = 0; a < 2; ++a) {
                 mbar_init(smem_u32(&C.tfull[a]), 1);
@@ -600,10 +600,10 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                     const int s = it % MX_STAGES;
                     const uint32_t par = (it / MX_STAGES) & 1;
                     // Codes arrive by TMA (async proxy), as the MMAs read them:
-                    // the barrier phase orders the two.  The scale warp has
-                    // copied the stage's atoms into TMEM once sfready flips.
-                    if (!mx_wait(&C.abort, &C.full[s], par, p.status) ||
-                        !mx_wait(&C.abort, &C.sfready[s], par, p.status)) {
+                    // the barrier phase orders the two.  The same phase needs
+                    // both copier warps' commits, so the stage's atoms are in
+                    // TMEM too.
+                    if (!mx_wait(&C.abort, &C.full[s], par, p.status)) {
                         ok = false;
                         break;
                     }
@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1) grouped_gemm_mx_kernel(const __
                                 mx_sf_copy<PAIR>(sfb + NB * j + 4 * i,
                                                  sf_st + S::kSfaBytes + (j * kCtas + i) * MX_ATOM_BYTES);
                     }
-                    mx_commit_own<PAIR>(smem_u32(&C.sfready[s]));
+                    mx_commit_own<PAIR>(smem_u32(&C.full[s]));
                 }
             }
         }
