@@ -169,7 +169,7 @@ struct MxGroup {
 };
 
 struct MxControl {
-    uint64_t full[MX_STAGES];    // a stage's codes landed (pair: both CTAs'; in the even CTA), atoms in TMEM
+    uint64_t full[MX_STAGES];    // a stage's codes landed and its atoms are in TMEM (pair: in the even CTA)
     uint64_t sffull[MX_STAGES];  // a stage's scale atoms landed (pair: both CTAs'; in the even CTA)
     uint64_t empty[MX_STAGES];  // the copies and MMAs reading a stage completed
     uint64_t tfull[2];
