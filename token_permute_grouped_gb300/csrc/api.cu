@@ -373,6 +373,18 @@ a2av_status run_impl(const a2av_gmm_desc *desc, const void *ataOut, const int32_
     g.pair = pair ? 1 : 0;
     const int64_t n_units = std::max<int64_t>(1, std::min<int64_t>(units, tiles));
     g.grid = static_cast<int32_t>(n_units * (pair ? 2 : 1));
+    // Which operand of a stage to request first: the one a wave of units
+    // touches more of, as it is the likelier to come from DRAM rather than
+    // L2.  With tn column tiles per group, a wave covers about n_units / tn
+    // row tiles of a group's A and all tn of its column tiles, so the
+    // weights are the larger footprint when tn * tn > n_units.  Weights
+    // first only when that holds for every group with tiles.
+    {
+        const int64_t tn2 = has_shared ? (d.N2 + g.bn2 - 1) / g.bn2 : 0;
+        const bool routed_b = d.A == 0 || tn1 * tn1 > n_units;
+        const bool shared_b = !has_shared || tn2 * tn2 > n_units;
+        g.b_first = (g.kchunks == 2 && routed_b && shared_b && (d.A > 0 || has_shared)) ? 1 : 0;
+    }
     if (gemm_begin) {
         g.after_permute = 0;  // an event between the kernels: plain stream order
         if (cudaEventRecord(gemm_begin, stream) != cudaSuccess) return A2AV_ERR_CUDA;

@@ -380,9 +380,12 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
     }
 }
 
-template <bool BF16, bool GATHER, bool PAIR, int CH>
+// B_FIRST: each stage's weight load goes out before its A load (the host
+// picks it when the weights are the operand a wave of units touches more of).
+template <bool BF16, bool GATHER, bool PAIR, int CH, bool B_FIRST = false>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmLaunch p) {
     static_assert(CH == 1 || !GATHER, "row gathers use one-chunk stages");
+    static_assert(!B_FIRST || (CH == 2 && !GATHER), "weights first only on two-chunk TMA stages");
     using S = Shape<PAIR, CH>;
     constexpr int BK = S::BK;
     constexpr uint32_t A_STAGE_BYTES = S::A_STAGE_BYTES;
@@ -662,6 +665,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     const uint32_t a_st = a_smem + s * A_STAGE_BYTES;
                     if (lane == 0 && rank == 0) mbar_arrive_expect_tx(fb_own, bytes);
                     __syncwarp();
+                    // The stage's weight columns: all its atoms in one load
+                    // when the 4-D view applies.
+                    auto load_b = [&]() {
+                        if (b4)
+                            tma_4d<PAIR>(b_smem + s * S::B_STAGE_BYTES, tb4, fb, 0, kb * BK, xn / 64, z);
+                        else
+                            for (int c = 0; c < nb; ++c)
+                                tma_3d<PAIR>(b_smem + s * S::B_STAGE_BYTES + c * B_ATOM_BYTES, tb, fb,
+                                             xn + c * 64, kb * BK, z);
+                    };
+                    if (B_FIRST && lane == 0) load_b();
                     if (GATHER && !shared) {
                         if (box_level == 0)
                             tma_gather4<PAIR>(a_st + lane * 512, &p.tmA_routed, fb, kb * BK, src[0], src[1],
@@ -676,14 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         else  // 3-D view {64 columns, rows, K chunks}: CH chunks in one load
                             tma_3d<PAIR>(a_st, ta, fb, 0, ya, kb * CH);
                     }
-                    if (lane == 0) {
-                        if (b4)  // all the stage's weight atoms in one load
-                            tma_4d<PAIR>(b_smem + s * S::B_STAGE_BYTES, tb4, fb, 0, kb * BK, xn / 64, z);
-                        else
-                            for (int c = 0; c < nb; ++c)
-                                tma_3d<PAIR>(b_smem + s * S::B_STAGE_BYTES + c * B_ATOM_BYTES, tb, fb,
-                                             xn + c * 64, kb * BK, z);
-                    }
+                    if (!B_FIRST && lane == 0) load_b();
                 }
             }
             // Tail: wait until the MMAs released every stage we filled.
@@ -890,9 +897,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
 }
 
-template <bool BF16, bool GATHER, bool PAIR, int CH>
+template <bool BF16, bool GATHER, bool PAIR, int CH, bool B_FIRST = false>
 cudaError_t launch_variant(const GemmLaunch &p, cudaStream_t stream) {
-    auto kern = grouped_gemm_kernel<BF16, GATHER, PAIR, CH>;
+    auto kern = grouped_gemm_kernel<BF16, GATHER, PAIR, CH, B_FIRST>;
     constexpr size_t smem = smem_bytes<PAIR, CH>();
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
@@ -959,6 +966,9 @@ cudaError_t launch_grouped_gemm(const GemmLaunch &p, cudaStream_t stream) {
     const bool pair = p.pair != 0;
     if (p.kchunks == 2) {  // two-chunk stages: CTA pairs, TMA-fed A (no row gathers)
         if (!pair || p.gather) return cudaErrorInvalidValue;
+        if (p.b_first)
+            return p.bf16 ? launch_variant<true, false, true, 2, true>(p, stream)
+                          : launch_variant<false, false, true, 2, true>(p, stream);
         return p.bf16 ? launch_variant<true, false, true, 2>(p, stream)
                       : launch_variant<false, false, true, 2>(p, stream);
     }

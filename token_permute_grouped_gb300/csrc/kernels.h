@@ -43,6 +43,7 @@ struct GemmLaunch {
     int32_t pair;         // 1: 256-row tiles on CTA pairs (cta_group::2), 0: 128-row tiles
     int32_t kchunks;      // 64-wide K chunks per stage: 1, or 2 (pair, TMA-fed A, maps below in 3-D/4-D)
     int32_t grid;         // persistent CTAs (pair: an even number, two per cluster)
+    int32_t b_first;      // two-chunk stages: issue each stage's weight load before its A load
     CUtensorMap tmA_routed;   // split: expert-major A, 128-row box; fused: ataOut, 1-row box (gather)
     CUtensorMap tmA_box[5];   // fused: ataOut with 8, 16, 32, 64, 128-row boxes (contiguous runs)
     CUtensorMap tmB_routed;   // gmmWeight [e, H1, N1]
